@@ -1,0 +1,338 @@
+"""Checks that tie the CPU oracle to facts outside itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with a fact fixed by the samir-vllm pages or by
+mathematics: hand-derived closed forms (tests/golden), the single-token and
+zero-query special cases, normalisation of the softmax weights, a dominant
+key, invariance of the paged result under page permutations (against a
+contiguous-cache statement), a library routine (torch's scaled dot-product
+attention in float64 on the CPU), the split/merge algebra, and the closed-form
+address of the decode-time append. The same functions run against builds of
+the oracle with planted mistakes, each of which must fail at least one pin.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle as oracle_pkg
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+HQ, HKV, D, P = W.NUM_Q_HEADS, W.NUM_KV_HEADS, W.HEAD_DIM, W.PAGE_SIZE
+
+
+# ---------------------------------------------------------------- helpers
+def bits(t: torch.Tensor) -> np.ndarray:
+    """BF16 tensor -> uint16 bit patterns (numpy)."""
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def f64_to_bits(x: np.ndarray) -> np.ndarray:
+    """Exact for values representable in BF16 (used for hand-built cases only)."""
+    f = np.asarray(x, np.float32)
+    b = f.view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0), "value not exact in BF16"
+    return (b >> 16).astype(np.uint16)
+
+
+def normal_bits(rng, shape, scale=1.0):
+    x = (rng.standard_normal(shape) * scale).astype(np.float32)
+    return bits(torch.from_numpy(x).to(torch.bfloat16))
+
+
+def scatter_tokens(k_tokens, v_tokens, pages, num_pages, fill=W.BF16_NAN_BITS):
+    """Pools [num_pages][Hkv][P][D] holding token t of a contiguous cache
+    [len][Hkv][D] at page pages[t // P], slot t % P (the test's own statement
+    of the layout); every other slot holds `fill`."""
+    k_pool = np.full((num_pages, HKV, P, D), fill, np.uint16)
+    v_pool = np.full_like(k_pool, fill)
+    n = k_tokens.shape[0]
+    t = np.arange(n)
+    k_pool[np.asarray(pages)[t // P], :, t % P, :] = k_tokens
+    v_pool[np.asarray(pages)[t // P], :, t % P, :] = v_tokens
+    return k_pool, v_pool
+
+
+def one_sequence(orc, q, k_pool, v_pool, pages, seq_len, num_pages):
+    g = oracle_pkg.geometry(1, num_pages, 1)
+    table = np.full((1, 1, W.MAX_PAGES_PER_SEQ), -1, np.int32)
+    table[0, 0, :len(pages)] = pages
+    st, out, lse, wsum = orc.decode_attention(g, 0, q.reshape(1, HQ, D).copy(), k_pool, v_pool,
+                                              table, np.array([seq_len], np.int32))
+    assert st == oracle_pkg.OK, f"status {st}"
+    return out[0], lse[0], wsum[0]
+
+
+def tiny_state(alt=False):
+    """Tiny workload with the new tokens already appended (by the test's own
+    numpy scatter), as uint16 arrays."""
+    wl = W.tiny(alt)
+    kp, vp = (bits(p) for p in wl.pools("cpu", "nan"))
+    q, kn, vn = bits(wl.q()), bits(wl.k_new()), bits(wl.v_new())
+    pos = wl.positions
+    for b in range(wl.batch):
+        page = wl.block_tables[0, b, pos[b] // P]
+        kp[page, :, pos[b] % P, :] = kn[0, b]
+        vp[page, :, pos[b] % P, :] = vn[0, b]
+    return wl, q, kp, vp
+
+
+def gather(table_row, seq_len, pool):
+    """[len][Hkv][D] rows of one sequence, walked through its block table."""
+    t = np.arange(seq_len)
+    return pool[table_row[t // P], :, t % P, :]
+
+
+def sdpa_reference(q_bits, k_rows_bits, v_rows_bits):
+    """torch float64 scaled_dot_product_attention, GQA expanded by
+    repeat_interleave (query head h reads KV head h // 4)."""
+    group = HQ // HKV
+    qf = torch.from_numpy(bits_to_f64(q_bits)).reshape(1, HQ, 1, D)
+    k = torch.from_numpy(bits_to_f64(k_rows_bits)).permute(1, 0, 2)  # [Hkv][L][D]
+    v = torch.from_numpy(bits_to_f64(v_rows_bits)).permute(1, 0, 2)
+    k = k.repeat_interleave(group, dim=0).unsqueeze(0)
+    v = v.repeat_interleave(group, dim=0).unsqueeze(0)
+    out = torch.nn.functional.scaled_dot_product_attention(qf, k, v)
+    return out.reshape(HQ, D).numpy()
+
+
+# ---------------------------------------------------------------- pins
+def pin_golden_closed_form(orc):
+    with open(os.path.join(GOLDEN, "two_token_closed_form.json")) as f:
+        spec = json.load(f)
+    env = {"e": math.e}
+    for case in spec["cases"]:
+        k = np.zeros((case["num_pages"], HKV, P, D), np.float64)
+        v = np.zeros_like(k)
+        kv = case["kv_head"]
+        for t, row in case["k_rows"].items():
+            for d, x in row.items():
+                t_ = int(t)
+                k[case["block_table"][t_ // P], kv, t_ % P, int(d)] = x
+        for t, row in case["v_rows"].items():
+            for d, x in row.items():
+                t_ = int(t)
+                v[case["block_table"][t_ // P], kv, t_ % P, int(d)] = x
+        q = np.zeros((HQ, D), np.float64)
+        for h, row in case["q_heads"].items():
+            for d, x in row.items():
+                q[int(h), int(d)] = x
+        out, lse, _ = one_sequence(orc, f64_to_bits(q), f64_to_bits(k), f64_to_bits(v),
+                                   case["block_table"], case["seq_len"], case["num_pages"])
+        for e in case["expected"]:
+            closed = eval(e["formula"], {"__builtins__": {}}, env)  # formula text -> number
+            assert abs(closed - e["value"]) < 1e-15, f"fixture value disagrees with {e}"
+            got = out[e["head"], e["dim"]]
+            assert abs(got - e["value"]) < 1e-14, f"{case['name']}: {e} got {got}"
+        if case["seq_len"] == 2:  # lse of head 5 is log(1 + e), of head 4 is log 2
+            assert abs(lse[5] - math.log(1 + math.e)) < 1e-14
+            assert abs(lse[4] - math.log(2)) < 1e-14
+
+
+def pin_pool_geometry_facts(orc):
+    with open(os.path.join(GOLDEN, "pool_geometry.json")) as f:
+        spec = json.load(f)
+    facts, derived = spec["facts"], spec["derived"]
+    assert facts["page_size_tokens"]["value"] == P
+    assert facts["context_tokens"]["value"] // P == derived["max_pages_per_sequence"]["value"]
+    assert W.PAGE_BYTES_KV == derived["bytes_per_page_kv"]["value"]
+    assert W.pages_for_pool_mib(facts["default_pool_mib"]["value"]) == \
+        derived["pages_in_default_pool"]["value"]
+    assert HQ * D == facts["hidden_width"]["value"]
+    # two sequences at full context in every layer fill the default pool exactly
+    wl = W.llama_default()
+    assert wl.num_pages == derived["pages_for_two_full_sequences_all_layers"]["value"]
+    assert np.all(wl.block_tables >= 0)
+    assert np.unique(wl.block_tables).size == wl.num_pages
+
+
+def pin_single_token_returns_v_row(orc):
+    rng = np.random.default_rng(11)
+    q = normal_bits(rng, (HQ, D))
+    kt, vt = normal_bits(rng, (1, HKV, D)), normal_bits(rng, (1, HKV, D))
+    kp, vp = scatter_tokens(kt, vt, [3], 5)
+    out, lse, wsum = one_sequence(orc, q, kp, vp, [3], 1, 5)
+    for h in range(HQ):
+        assert np.array_equal(out[h], bits_to_f64(vt[0, h // (HQ // HKV)])), f"head {h}"
+    assert np.all(wsum == 1.0)
+
+
+def pin_zero_query_gives_mean_of_v(orc):
+    rng = np.random.default_rng(12)
+    n = 37
+    q = np.zeros((HQ, D), np.uint16)
+    kt, vt = normal_bits(rng, (n, HKV, D)), normal_bits(rng, (n, HKV, D))
+    pages = [4, 0, 2]
+    kp, vp = scatter_tokens(kt, vt, pages, 6)
+    out, lse, _ = one_sequence(orc, q, kp, vp, pages, n, 6)
+    mean = bits_to_f64(vt).mean(axis=0)  # [Hkv][D]
+    for h in range(HQ):
+        np.testing.assert_allclose(out[h], mean[h // (HQ // HKV)], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, math.log(n), rtol=0, atol=1e-13)
+
+
+def pin_weights_sum_to_one(orc):
+    wl, q, kp, vp = tiny_state()
+    g = oracle_pkg.geometry(1, wl.num_pages, wl.batch)
+    st, out, lse, wsum = orc.decode_attention(g, 0, q[0].copy(), kp, vp, wl.block_tables,
+                                              wl.seq_lens)
+    assert st == oracle_pkg.OK
+    assert np.all(np.isfinite(out))
+    np.testing.assert_allclose(wsum, 1.0, rtol=0, atol=1e-12)
+
+
+def pin_dominant_key(orc):
+    rng = np.random.default_rng(13)
+    n = 29
+    q = normal_bits(rng, (HQ, D))
+    kt, vt = normal_bits(rng, (n, HKV, D)), normal_bits(rng, (n, HKV, D))
+    star = 17
+    # key `star` of every KV head points along sign(q) of head 4*kv with
+    # magnitude 256: its score exceeds every other by > 1000, so the softmax
+    # puts all weight (to double precision) on it for those heads
+    qf = bits_to_f64(q)
+    for kv in range(HKV):
+        kt[star, kv] = f64_to_bits(256.0 * np.sign(qf[kv * (HQ // HKV)]))
+    pages = [1, 5]
+    kp, vp = scatter_tokens(kt, vt, pages, 7)
+    out, _, _ = one_sequence(orc, q, kp, vp, pages, n, 7)
+    for kv in range(HKV):
+        assert np.array_equal(out[kv * (HQ // HKV)], bits_to_f64(vt[star, kv]))
+
+
+def pin_paged_equals_contiguous(orc):
+    rng = np.random.default_rng(14)
+    for n in (1, 15, 16, 17, 40, 128, 300):
+        q = normal_bits(rng, (HQ, D))
+        kt, vt = normal_bits(rng, (n, HKV, D)), normal_bits(rng, (n, HKV, D))
+        st, ref = orc.contiguous_attention(q, kt, vt)
+        assert st == oracle_pkg.OK
+        need = -(-n // P)
+        results = []
+        for trial in range(2):
+            num_pages = need + 5
+            pages = rng.permutation(num_pages)[:need].astype(np.int32)
+            kp, vp = scatter_tokens(kt, vt, pages, num_pages)
+            out, _, _ = one_sequence(orc, q, kp, vp, pages, n, num_pages)
+            results.append(out)
+        assert np.array_equal(results[0], ref), f"len {n}"
+        assert np.array_equal(results[1], ref), f"len {n}"
+
+
+def pin_contiguous_matches_sdpa(orc):
+    rng = np.random.default_rng(15)
+    for n in (1, 33):
+        q = normal_bits(rng, (HQ, D))
+        kt, vt = normal_bits(rng, (n, HKV, D)), normal_bits(rng, (n, HKV, D))
+        st, out = orc.contiguous_attention(q, kt, vt)
+        assert st == oracle_pkg.OK
+        np.testing.assert_allclose(out, sdpa_reference(q, kt, vt), rtol=0, atol=1e-12)
+
+
+def pin_paged_matches_sdpa(orc):
+    for alt in (False, True):
+        wl, q, kp, vp = tiny_state(alt)
+        g = oracle_pkg.geometry(1, wl.num_pages, wl.batch)
+        st, out, _, _ = orc.decode_attention(g, 0, q[0].copy(), kp, vp, wl.block_tables,
+                                             wl.seq_lens)
+        assert st == oracle_pkg.OK
+        for b in range(wl.batch):
+            n = int(wl.seq_lens[b])
+            ref = sdpa_reference(q[0, b], gather(wl.block_tables[0, b], n, kp),
+                                 gather(wl.block_tables[0, b], n, vp))
+            np.testing.assert_allclose(out[b], ref, rtol=0, atol=1e-12)
+
+
+def pin_split_equals_unsplit(orc):
+    lens = [1, 16, 17, 40, 200, 2048]
+    wl = W.custom(lens, num_layers=2, seed=217)
+    kp, vp = (bits(p) for p in wl.pools("cpu", "zero"))
+    q = bits(wl.q())
+    g = oracle_pkg.geometry(2, wl.num_pages, wl.batch)
+    for layer in (0, 1):
+        st, ref, _, _ = orc.decode_attention(g, layer, q[layer].copy(), kp, vp,
+                                             wl.block_tables, wl.seq_lens)
+        assert st == oracle_pkg.OK
+        for S in (1, 2, 4, 16, 32):
+            st, out, po, pm, pl = orc.decode_attention_split(g, layer, q[layer].copy(), kp, vp,
+                                                            wl.block_tables, wl.seq_lens, S)
+            assert st == oracle_pkg.OK
+            np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+            # S = 1: the single partial normalised is the answer
+            if S == 1:
+                np.testing.assert_allclose(po[:, :, 0] / pl[:, :, 0:1], ref, rtol=1e-12,
+                                           atol=1e-13)
+            # empty splits carry m = -inf, l = 0
+            for b, n in enumerate(lens):
+                n_pages = -(-n // P)
+                chunk = -(-n_pages // S)
+                for s in range(S):
+                    if s * chunk >= n_pages:
+                        assert np.all(pl[b, :, s] == 0) and np.all(np.isneginf(pm[b, :, s]))
+                    else:
+                        assert np.all(pl[b, :, s] >= 1.0)  # the max term contributes exp(0)
+
+
+def pin_mt_matches_single_thread(orc):
+    wl = W.custom([5, 16, 33, 64, 100, 250, 1], num_layers=1, seed=218)
+    kp, vp = (bits(p) for p in wl.pools("cpu", "zero"))
+    q = bits(wl.q())
+    g = oracle_pkg.geometry(1, wl.num_pages, wl.batch)
+    st, ref, _, _ = orc.decode_attention(g, 0, q[0].copy(), kp, vp, wl.block_tables,
+                                         wl.seq_lens)
+    for nthreads in (1, 3):
+        st2, out = orc.decode_attention_mt(g, 0, q[0].copy(), kp, vp, wl.block_tables,
+                                           wl.seq_lens, nthreads)
+        assert st == st2 == oracle_pkg.OK
+        assert np.array_equal(out, ref)
+
+
+def pin_append_closed_form(orc):
+    wl = W.custom([1, 16, 17, 32, 2048, 100], num_layers=3, seed=219)
+    kp, vp = (bits(p) for p in wl.pools("cpu", "nan"))
+    kn, vn = bits(wl.k_new()), bits(wl.v_new())
+    g = oracle_pkg.geometry(3, wl.num_pages, wl.batch)
+    pos = wl.positions
+    for layer in range(3):
+        exp_k, exp_v = kp.copy(), vp.copy()
+        for b in range(wl.batch):
+            page = wl.block_tables[layer, b, pos[b] // P]
+            exp_k[page, :, pos[b] % P, :] = kn[layer, b]
+            exp_v[page, :, pos[b] % P, :] = vn[layer, b]
+        st = orc.append(g, layer, kn[layer].copy(), vn[layer].copy(), kp, vp, wl.block_tables,
+                        pos)
+        assert st == oracle_pkg.OK
+        assert np.array_equal(kp, exp_k) and np.array_equal(vp, exp_v), f"layer {layer}"
+
+
+def pin_append_rejects_out_of_range(orc):
+    wl = W.custom([20, 20], num_layers=1, seed=220)
+    kp, vp = (bits(p) for p in wl.pools("cpu", "zero"))
+    before_k, before_v = kp.copy(), vp.copy()
+    kn, vn = bits(wl.k_new()), bits(wl.v_new())
+    g = oracle_pkg.geometry(1, wl.num_pages, wl.batch)
+    table = wl.block_tables.copy()
+    table[0, 1, 1] = wl.num_pages  # page id past the pool
+    for pos in ([2048, 19], [-1, 19], [19, 19]):
+        st = orc.append(g, 0, kn[0].copy(), vn[0].copy(), kp, vp, table,
+                        np.array(pos, np.int32))
+        assert st == oracle_pkg.OUT_OF_RANGE
+        # sequence 1 (bad page) is never written; sequence 0 only when its position is valid
+        assert np.array_equal(kp[table[0, 1, 0]], before_k[table[0, 1, 0]])
+        if pos[0] < 0 or pos[0] >= 2048:
+            assert np.array_equal(kp, before_k) and np.array_equal(vp, before_v)
+
+
+ALL_PINS = [pin_golden_closed_form, pin_pool_geometry_facts, pin_single_token_returns_v_row,
+            pin_zero_query_gives_mean_of_v, pin_weights_sum_to_one, pin_dominant_key,
+            pin_paged_equals_contiguous, pin_contiguous_matches_sdpa, pin_paged_matches_sdpa,
+            pin_split_equals_unsplit, pin_mt_matches_single_thread, pin_append_closed_form,
+            pin_append_rejects_out_of_range]
