@@ -1,0 +1,465 @@
+"""Benchmark: paged decode attention on one GB300 (replicas on N GPUs).
+
+A step is one decode step of the whole hot path over one batch: for each of
+the 16 layers, the fused append-then-attend launch (append the new token's
+K/V into its block-table slot, then paged GQA decode attention with split-KV
+and the in-launch merge). The default workload is a Llama-3.2-1B decode step
+at the pages' default pool: batch 2 at 2,048 tokens, 4,096-page (128 MiB)
+BF16 pool, pages shuffled, BF16 N(0,1) inputs.
+
+Timing: the 16 launches of a step are captured in a CUDA graph with
+GPU-timestamped events before, between and after them; before every step an
+untimed read of a buffer twice the L2 size evicts the cache. value = KV GB/s
+= algorithmic bytes per step / step time, with algorithmic bytes per
+(sequence, layer) = seq_len x 2048 (every cached K/V row read once) + 2048
+(the new row written) + 4096 (q) + 8192 (FP32 out).
+
+--impl reference times the CPU oracle (FP64 C++) on the host cores on a
+bounded sample of the same workload and prints the same line with
+"impl": "reference".
+"""
+
+import argparse
+import concurrent.futures
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s and seq-layer steps/s; % of GB300 HBM peak"
+NOMINAL_HBM_GBS = 8000.0
+WORKLOADS = {
+    "llama-b2-2048": W.llama_default,
+    "mix-b64": W.continuous_mix,
+    "ragged-b256": W.large_ragged,
+    "long-b1": lambda: W.long_context(1),
+    "long-b4": lambda: W.long_context(4),
+}
+DESCRIPTIONS = {
+    "llama-b2-2048": "Llama-3.2-1B decode step at the default 128 MiB pool: 16 layers, batch 2 at "
+                     "seq_len 2048, 32q/8kv heads, head_dim 64, 4096 shuffled 16-token pages",
+    "mix-b64": "continuous-batching mix: 16 layers, batch 64, seq_lens log-uniform in "
+               "[16, 2048], 4 GiB pool, fragmented free list",
+    "ragged-b256": "large ragged batch: 16 layers, batch 256, seq_lens uniform in [1, 2048], "
+                   "K x 4",
+    "long-b1": "long context: 16 layers, batch 1 at 2048, 1 GiB pool",
+    "long-b4": "long context: 16 layers, batch 4 at 2048, 1 GiB pool",
+}
+
+
+def step_bytes(wl):
+    """Algorithmic bytes of one fused step over all layers."""
+    per_seq = wl.seq_lens.astype(np.int64) * 2048 + 2048 + 4096 + 8192
+    return int(per_seq.sum()) * wl.num_layers
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("paged_kv_cache_210_gb300/csrc/pkv.cu", "include/pkv.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    or None when there is none for this kernel source and workload."""
+    path = os.path.join(ROOT, "profiles", f"decode_fused_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ": " in line:
+                k, v = line[2:].split(": ", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.lines = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            target = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            target = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"] + target, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_inputs(wl):
+    kp, vp = wl.pools("cpu", "zero")
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+    return bits(kp), bits(vp), bits(wl.q()), bits(wl.k_new()), bits(wl.v_new())
+
+
+def time_oracle(wl, layers_per_step, n_steps, threads):
+    """Runs the oracle (append + attention) on `layers_per_step` layers per
+    step, layers in parallel over host threads; returns (seconds, bytes)."""
+    import oracle
+    orc = oracle.load()
+    kp, vp, q, kn, vn = oracle_inputs(wl)
+    g = oracle.geometry(wl.num_layers, wl.num_pages, wl.batch)
+    pos = wl.positions
+    bytes_per_layer = step_bytes(wl) // wl.num_layers
+
+    def one_layer(layer):
+        st = orc.append(g, layer, kn[layer].copy(), vn[layer].copy(), kp, vp, wl.block_tables,
+                        pos)
+        st2, _, _, _ = orc.decode_attention(g, layer, q[layer].copy(), kp, vp,
+                                            wl.block_tables, wl.seq_lens)
+        assert st == st2 == oracle.OK
+        return layer
+
+    total_layers = 0
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        for s in range(n_steps):
+            layers = [(s * layers_per_step + i) % wl.num_layers for i in range(layers_per_step)]
+            list(ex.map(one_layer, layers))
+            total_layers += len(layers)
+    dt = time.perf_counter() - t0
+    return dt, total_layers * bytes_per_layer, total_layers
+
+
+def cpu_threads():
+    return max(1, min(os.cpu_count() or 1, 16))
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]()
+    threads = min(cpu_threads(), wl.num_layers)
+    # size a step so the whole run stays within about a minute and a half
+    probe_dt, _, probe_layers = time_oracle(wl, threads, 1, threads)
+    per_layer = probe_dt / probe_layers * threads   # core-seconds per layer
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    layers = max(1, min(wl.num_layers, int(budget * threads / max(per_layer, 1e-9))))
+    time_oracle(wl, layers, args.warmup, threads)
+    dt, nbytes, n_layers = time_oracle(wl, layers, args.steps, threads)
+    value = nbytes / dt / 1e9
+    sample = (f"{layers} of {wl.num_layers} layers per step (all {wl.batch} sequences), "
+              f"layers in parallel on {threads} threads, {args.steps} steps")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "layers_per_step": layers},
+        "seq_layer_steps_per_s": round(n_layers * wl.batch / dt, 2),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU path
+def make_event():
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True), True
+    except TypeError:
+        return torch.cuda.Event(enable_timing=True), False
+
+
+def run_ours(args, world, rank, local):
+    import paged_kv_cache_210_gb300 as pkv
+    from paged_kv_cache_210_gb300 import build as lib_build
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib_build.build()
+    pkv.load()
+    wl = WORKLOADS[args.workload]()
+    L, B = wl.num_layers, wl.batch
+
+    k_pool, v_pool = wl.pools(dev, "zero")
+    q = wl.q(dev)
+    k_new, v_new = wl.k_new(dev), wl.v_new(dev)
+    table = torch.from_numpy(wl.block_tables).to(dev)
+    lens = torch.from_numpy(wl.seq_lens).to(dev)
+    out = torch.zeros((L, B, W.NUM_Q_HEADS, W.HEAD_DIM), device=dev)
+    pool = pkv.pkv_pool_create(L, wl.num_pages, B)
+    splits = args.splits
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        return flush_buf.sum()
+
+    stream = torch.cuda.Stream(device=dev)
+    events = [make_event() for _ in range(L + 1)]
+    external = all(e[1] for e in events)
+    events = [e[0] for e in events]
+
+    def step(with_events):
+        s = torch.cuda.current_stream()
+        if with_events:
+            events[0].record(s)
+        for layer in range(L):
+            pkv.pkv_append_attend(pool, layer, q[layer], k_new[layer], v_new[layer], k_pool,
+                                  v_pool, table, lens, out[layer], num_splits=splits, stream=s)
+            if with_events:
+                events[layer + 1].record(s)
+
+    with torch.cuda.stream(stream):
+        step(False)
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(external)
+
+    # e2e: the same step through the public API with host buffers
+    q_h = q.cpu().pin_memory()
+    kn_h, vn_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    lens_h = lens.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_start, _ = make_event()
+    e2e_end, _ = make_event()
+    e2e_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(e2e_graph, stream=stream):
+        s = torch.cuda.current_stream()
+        if external:
+            e2e_start.record(s)
+        q.copy_(q_h, non_blocking=True)
+        k_new.copy_(kn_h, non_blocking=True)
+        v_new.copy_(vn_h, non_blocking=True)
+        lens.copy_(lens_h, non_blocking=True)
+        step(False)
+        out_h.copy_(out, non_blocking=True)
+        if external:
+            e2e_end.record(s)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, kn_h, vn_h, lens_h))
+    d2h = out_h.numel() * out_h.element_size()
+
+    def replay_timed(g, ev0, ev1):
+        with torch.cuda.stream(stream):
+            flush()
+            if external:
+                g.replay()
+            else:
+                ev0.record(stream)
+                g.replay()
+                ev1.record(stream)
+
+    # warm-up
+    for _ in range(args.warmup):
+        replay_timed(graph, events[0], events[L])
+    torch.cuda.synchronize()
+
+    # timed region
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev)
+    time.sleep(0.3)
+    step_ms, launch_ms = [], []
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        replay_timed(graph, events[0], events[L])
+        stream.synchronize()
+        step_ms.append(events[0].elapsed_time(events[L]))
+        if external:
+            launch_ms.extend(events[i].elapsed_time(events[i + 1]) for i in range(L))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(sum(step_ms), world)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+
+    # e2e steps (host buffers, copies inside the timed events)
+    e2e_ms = []
+    for _ in range(max(3, args.steps // 4)):
+        replay_timed(e2e_graph, e2e_start, e2e_end)
+        stream.synchronize()
+        e2e_ms.append(e2e_start.elapsed_time(e2e_end))
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    e2e_total = max_over_ranks(sum(e2e_ms), world)
+
+    nbytes = step_bytes(wl)
+    ms_per_step = total_ms / args.steps
+    value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    e2e_value = world * nbytes * len(e2e_ms) / (e2e_total * 1e-3) / 1e9
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+
+    if launch_ms:
+        per_launch_ms = statistics.mean(launch_ms)
+        launch_source = "CUDA events between the launches inside the timed graph"
+    else:
+        per_launch_ms = ms_per_step / L
+        launch_source = "step time / launches (events inside graphs unsupported here)"
+    achieved = (nbytes / L) / (per_launch_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+
+    if rank != 0:
+        return
+    chunk_note = "library's choice" if splits == 0 else f"{splits} splits per sequence"
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "storage_dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+            "batch": B, "layers": L, "seq_lens": "all 2048" if np.all(wl.seq_lens == 2048)
+            else f"mean {float(wl.seq_lens.mean()):.1f}",
+            "step": "16 x fused append+attend (one launch per layer), CUDA graph",
+            "splits": chunk_note,
+            "l2": "flushed before every step (read of a buffer twice the L2 size, outside the "
+                  "timed events)",
+            "bytes_per_step": nbytes,
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        },
+        "seq_layer_steps_per_s": round(world * B * L * args.steps / (total_ms * 1e-3), 1),
+        "pct_of_measured_hbm": round(100 * value / world / hbm_peak, 2),
+        "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "step_ms_p10_p50_p90": [round(float(np.percentile(step_ms, p)), 5) for p in (10, 50, 90)],
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_total / len(e2e_ms), 5)},
+        "gpu_launches": L * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": traffic, "kernel": "decode_kernel<fused>",
+                     "per_launch_ms": round(per_launch_ms, 6), "per_launch_source": launch_source,
+                     "bytes_per_launch": nbytes // L},
+        "wall_s_timed_loop": round(wall, 3),
+    }
+    if not args.no_cpu_baseline:
+        threads = min(cpu_threads(), L)
+        probe_dt, _, probe_layers = time_oracle(wl, threads, 1, threads)
+        # about 10-20 s of CPU work in total
+        n_steps = max(1, int(15.0 / max(probe_dt * threads, 1e-6)))
+        dt, cbytes, n_layers = time_oracle(wl, threads, n_steps, threads)
+        line["cpu_baseline"] = {
+            "value": round(cbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n_layers} layer-steps ({threads} layers at a time in parallel, all "
+                      f"{B} sequences each), {dt:.1f} s wall"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="llama-b2-2048")
+    ap.add_argument("--splits", type=int, default=0, help="0: the library chooses")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

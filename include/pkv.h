@@ -1,0 +1,151 @@
+/*
+ * pkv.h - paged KV cache decode path for one GB300 (sm_103a) GPU.
+ *
+ * A shared BF16 page pool holds the KV cache of every sequence and layer.
+ * A physical page holds 16 tokens of K and of V for one layer, and a block
+ * table per sequence and layer maps the sequence's logical pages to physical
+ * page ids; decode appends one new token per sequence at its absolute
+ * position and then attends over the sequence's pages in place, with an FP32
+ * online softmax, without gathering a contiguous prefix or storing scores.
+ *   [samir-vllm: Build LLM Inference From Scratch in C++ and CUDA,
+ *    "Architecture walkthrough", KV cache paragraph, and "TL;DR" table, Decode
+ *    row; 6 Hours of YouTube and 85 handtyped pages of notes on LLM Inference
+ *    - Start here, README feature list: shared BF16 KV page pool bullet,
+ *    batched decode bullet, direct paged decode attention bullet]
+ *
+ * Geometry (fixed by this library): 32 query heads over 8 KV heads (query
+ * head h reads KV head h / 4), head_dim 64, 16-token pages, score scale
+ * 1/sqrt(64), at most 2,048 tokens of context (128 pages per sequence).
+ *
+ * Layouts (all row-major, all device memory allocated by the caller):
+ *   k_pool, v_pool   BF16 [num_pages][8][16][64]   (page, kv head, token, dim)
+ *                    one (page, kv head) tile is 2 KiB, contiguous
+ *   block_tables     int32 [num_layers][max_batch][max_seq_len / 16]
+ *                    physical page id of logical page i of sequence b in
+ *                    layer l; ids are global over the one pool
+ *   q                BF16 [batch][32][64]   (one layer)
+ *   k, v (new token) BF16 [batch][8][64]    (one layer)
+ *   positions        int32 [batch]: absolute position of the appended token
+ *   seq_lens         int32 [batch]: attended length AFTER the append; the
+ *                    token at position seq_lens[b] - 1 is attended
+ *   out              FP32 [batch][32][64]   (one layer)
+ * Every pointer must be 16-byte aligned (the kernels move 16-byte vectors
+ * and the page tiles are copied by the bulk-copy engine).
+ *
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream). Host-detectable problems (null or misaligned pointers,
+ * layer or batch out of range, unsupported geometry) return an error status
+ * synchronously and launch nothing. Index problems found in device data (a
+ * page id outside [0, num_pages), a position outside [0, max_seq_len), a
+ * seq_len outside [1, max_seq_len]) are recorded in the pool's sticky device
+ * error flag; the kernel skips the offending unit and never faults or
+ * traps. pkv_get_error reports and clears the flag.
+ *
+ * Block-table contract (the caller's, as in the pages' engine where each
+ * request owns its pages): a page belongs to one (sequence, layer); no two
+ * sequences of one call map to the same (page, slot).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad layer/batch/splits */
+  PKV_ERR_OUT_OF_RANGE = 2,   /* device data: page id, position or seq_len */
+  PKV_ERR_CUDA = 3,           /* a CUDA runtime call failed */
+  PKV_ERR_UNSUPPORTED = 4,    /* geometry this library is not built for */
+  PKV_ERR_DEVICE_TIMEOUT = 5  /* a bounded in-kernel wait gave up */
+} pkv_status;
+
+/* Pool geometry. page_size, num_q_heads, num_kv_heads and head_dim must be
+ * 16, 32, 8 and 64. max_seq_len is a multiple of 16, at most 2048, and sets
+ * the block-table row length (max_seq_len / 16). max_splits bounds the
+ * split-KV count per sequence (0 selects 64; at most 128) and sizes the
+ * handle's split workspace. num_pages is the number of pages in the pool
+ * the caller allocates: 4096 pages is the pages' default 128 MiB pool
+ * [samir-vllm: Build LLM Inference From Scratch in C++ and CUDA, "Hardware
+ * expectations"]. */
+typedef struct {
+  int num_layers;
+  int num_pages;
+  int page_size;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int max_seq_len;
+  int max_batch;
+  int max_splits;
+} pkv_pool_config;
+
+typedef struct pkv_pool* pkv_pool_t;
+
+/* Validates the geometry and creates a handle on the current device. The
+ * handle owns only device scratch: the split-KV partials (two layer-parity
+ * copies of max_batch x 32 x max_splits x (64 + 2) floats), one ticket
+ * counter per (sequence, kv head) and parity, and the sticky error flag.
+ * It does not own the pools, tables or tensors. Returns INVALID_ARG for a
+ * null argument, UNSUPPORTED for a geometry other than the one above, CUDA
+ * if an allocation fails. */
+pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out);
+
+/* Frees the handle's device scratch. Waits for the device to finish work
+ * that may still use it. NULL is accepted. */
+pkv_status pkv_pool_destroy(pkv_pool_t pool);
+
+/* Decode-time append [samir-vllm: Build LLM Inference From Scratch in C++ and
+ * CUDA, "Architecture walkthrough", KV cache paragraph; README feature list,
+ * shared BF16 KV page pool bullet]: for every sequence b < batch and kv head
+ * j, copies k[b][j][:] and v[b][j][:] to
+ *   k_pool / v_pool [block_tables[layer][b][p / 16]][j][p % 16][:],
+ * p = positions[b]. Bit copy, no arithmetic. A sequence whose position or
+ * page id is out of range is skipped and flagged. batch == 0 is a no-op. */
+pkv_status pkv_append(pkv_pool_t pool, int layer, const void* k, const void* v, void* k_pool,
+                      void* v_pool, const int32_t* block_tables, const int32_t* positions,
+                      int batch, void* stream);
+
+/* Paged decode attention for one layer [README feature list, direct paged
+ * decode attention bullet]: for every sequence b and query head h,
+ *   out[b][h][:] = sum_t softmax_t(q[b][h] . K_t / 8) V_t,  t < seq_lens[b],
+ * K_t, V_t read from the pools through block_tables[layer][b] (kv head h/4).
+ * One thread block per (sequence, kv head, split) serves the 4 query heads of
+ * the kv head, so every page tile is read once. num_splits = S > 0 splits
+ * each sequence's np = ceil(len / 16) pages into ranges of ceil(np / S)
+ * pages, computed separately and merged by log-sum-exp inside the same
+ * launch; num_splits = 0 lets the library choose (ranges of a fixed page
+ * count sized from batch and SM count). S must not exceed max_splits. The
+ * output does not depend on which physical pages hold the data. A sequence
+ * with an invalid seq_len is skipped (its out rows are left untouched) and
+ * flagged; an invalid page id is skipped and flagged. */
+pkv_status pkv_decode_attention(pkv_pool_t pool, int layer, const void* q, const void* k_pool,
+                                const void* v_pool, const int32_t* block_tables,
+                                const int32_t* seq_lens, float* out, int batch, int num_splits,
+                                void* stream);
+
+/* Append and attend fused into one launch: the same results as pkv_append
+ * with positions[b] = seq_lens[b] - 1 followed by pkv_decode_attention. The
+ * block that owns the sequence's last page writes the new token's K/V into
+ * the pool and uses it from on-chip memory; no other block reads that slot. */
+pkv_status pkv_append_attend(pkv_pool_t pool, int layer, const void* q, const void* k,
+                             const void* v, void* k_pool, void* v_pool,
+                             const int32_t* block_tables, const int32_t* seq_lens, float* out,
+                             int batch, int num_splits, void* stream);
+
+/* Synchronises `stream`, then returns and clears the sticky device error
+ * flag: PKV_OK, PKV_ERR_OUT_OF_RANGE or PKV_ERR_DEVICE_TIMEOUT (or CUDA if
+ * the synchronisation itself failed). */
+pkv_status pkv_get_error(pkv_pool_t pool, void* stream);
+
+/* Static text for a status code. */
+const char* pkv_status_string(pkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,291 @@
+"""CUDA path against the CPU oracle, through the C ABI (needs a GPU).
+
+Append and pool state: bit-exact. Attention output (FP32 from BF16 inputs):
+max |d| <= 5e-4 and row-normwise relative error <= 1e-3 against FP64.
+Unused slots and pages hold BF16 NaN sentinels, so any stray read shows up.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_210_gb300 as pkv
+import workloads as W
+from gpu_helpers import DeviceState, assert_close, bits, compact_sample, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+EDGE_LENGTHS = [1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 1000, 2047, 2048]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_210_gb300 import build
+    build.build()
+    pkv.load()
+
+
+def _pool(wl, max_splits=0):
+    return pkv.pkv_pool_create(wl.num_layers, wl.num_pages, wl.batch, max_splits=max_splits)
+
+
+def _host_inputs(st):
+    return bits(st.q.cpu()), bits(st.k_new.cpu()), bits(st.v_new.cpu())
+
+
+WORKLOADS = {
+    "tiny": lambda: W.tiny(False),
+    "tiny-b": lambda: W.tiny(True),
+    "edges": lambda: W.custom(EDGE_LENGTHS, num_layers=2, seed=301, name="edges"),
+    "edges-holes": lambda: W.custom(EDGE_LENGTHS[::-1], num_layers=3, seed=302, hole_every=3,
+                                    name="edges-holes"),
+}
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_append_bit_exact(name):
+    wl = WORKLOADS[name]()
+    st = DeviceState(wl)
+    pool = _pool(wl)
+    for layer in range(wl.num_layers):
+        pkv.pkv_append(pool, layer, st.k_new[layer], st.v_new[layer], st.k_pool, st.v_pool,
+                       st.table, st.positions)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    q_b, kn_b, vn_b = _host_inputs(st)
+    _, ok, ov = oracle_step(wl, st.host_k, st.host_v, q_b, kn_b, vn_b)
+    assert np.array_equal(bits(st.k_pool), ok)
+    assert np.array_equal(bits(st.v_pool), ov)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+@pytest.mark.parametrize("splits", [1, 2, 3, 0])
+def test_append_then_decode_matches_oracle(name, splits):
+    wl = WORKLOADS[name]()
+    st = DeviceState(wl)
+    pool = _pool(wl)
+    for layer in range(wl.num_layers):
+        pkv.pkv_append(pool, layer, st.k_new[layer], st.v_new[layer], st.k_pool, st.v_pool,
+                       st.table, st.positions)
+        pkv.pkv_decode_attention(pool, layer, st.q[layer], st.k_pool, st.v_pool, st.table,
+                                 st.lens, st.out[layer], num_splits=splits)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    ref, _, _ = oracle_step(wl, st.host_k, st.host_v, *_host_inputs(st))
+    assert_close(st.out.cpu().numpy(), ref, f"{name} S={splits}")
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_fused_append_attend_matches_oracle(name, splits):
+    wl = WORKLOADS[name]()
+    st = DeviceState(wl)
+    pool = _pool(wl)
+    for layer in range(wl.num_layers):
+        pkv.pkv_append_attend(pool, layer, st.q[layer], st.k_new[layer], st.v_new[layer],
+                              st.k_pool, st.v_pool, st.table, st.lens, st.out[layer],
+                              num_splits=splits)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    ref, ok, ov = oracle_step(wl, st.host_k, st.host_v, *_host_inputs(st))
+    assert np.array_equal(bits(st.k_pool), ok) and np.array_equal(bits(st.v_pool), ov)
+    assert_close(st.out.cpu().numpy(), ref, f"{name} fused S={splits}")
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_split_counts_against_unsplit_oracle(batch):
+    wl = W.custom([2048] * batch, num_layers=2, seed=303 + batch, name="long")
+    st = DeviceState(wl)
+    q_b, kn_b, vn_b = _host_inputs(st)
+    ref, _, _ = oracle_step(wl, st.host_k, st.host_v, q_b, kn_b, vn_b)
+    results = {}
+    for splits in (1, 2, 4, 16, 32, 64, 128, 0):
+        pool = _pool(wl, max_splits=128)
+        k0, v0 = st.k_pool.clone(), st.v_pool.clone()
+        out = torch.full_like(st.out, float("nan"))
+        for layer in range(wl.num_layers):
+            pkv.pkv_append_attend(pool, layer, st.q[layer], st.k_new[layer], st.v_new[layer],
+                                  k0, v0, st.table, st.lens, out[layer], num_splits=splits)
+        assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+        results[splits] = out.cpu().numpy()
+        assert_close(results[splits], ref, f"B={batch} S={splits}")
+    # S = 1 and S = 32 agree to within rounding
+    assert np.abs(results[1] - results[32]).max() <= 2 * 5e-4
+
+
+def test_output_independent_of_physical_pages():
+    """The same logical cache under two page permutations gives bit-identical
+    output for a fixed split plan."""
+    lens = [1, 17, 40, 300, 2048]
+    a = W.custom(lens, num_layers=1, seed=310, name="perm-a")
+    b = W.custom(lens, num_layers=1, seed=311, num_pages=a.num_pages + 40, name="perm-b")
+    sa = DeviceState(a, fill="nan")
+    # rebuild b's pools holding a's logical contents at b's physical pages
+    kb = torch.full((b.num_pages, 8, 16, 64), float("nan"), dtype=torch.bfloat16)
+    vb = kb.clone()
+    ka, va = sa.k_pool.cpu(), sa.v_pool.cpu()
+    for seq, n in enumerate(lens):
+        for lp in range(-(-n // 16)):
+            kb[b.block_tables[0, seq, lp]] = ka[a.block_tables[0, seq, lp]]
+            vb[b.block_tables[0, seq, lp]] = va[a.block_tables[0, seq, lp]]
+    kb, vb = kb.cuda(), vb.cuda()
+    tb = torch.from_numpy(b.block_tables).cuda()
+    for splits in (1, 4, 0):
+        pool_a, pool_b = _pool(a), _pool(b)
+        oa = torch.empty((a.batch, 32, 64), device="cuda")
+        ob = torch.empty_like(oa)
+        pkv.pkv_append_attend(pool_a, 0, sa.q[0], sa.k_new[0], sa.v_new[0], sa.k_pool.clone(),
+                              sa.v_pool.clone(), sa.table, sa.lens, oa, num_splits=splits)
+        pkv.pkv_append_attend(pool_b, 0, sa.q[0], sa.k_new[0], sa.v_new[0], kb.clone(),
+                              vb.clone(), tb, sa.lens, ob, num_splits=splits)
+        assert pkv.pkv_get_error(pool_a) == pkv.PKV_OK and pkv.pkv_get_error(pool_b) == pkv.PKV_OK
+        assert torch.equal(oa, ob), f"S={splits}"
+
+
+def test_single_token_returns_v_row_exactly():
+    wl = W.custom([1] * 7, num_layers=1, seed=312)
+    st = DeviceState(wl)
+    pool = _pool(wl)
+    out = st.out[0]
+    pkv.pkv_append_attend(pool, 0, st.q[0], st.k_new[0], st.v_new[0], st.k_pool, st.v_pool,
+                          st.table, st.lens, out)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    v = st.v_new[0].float()                       # [B][8][64]
+    expect = v.repeat_interleave(4, dim=1)        # query head h reads kv head h // 4
+    assert torch.equal(out, expect)
+
+
+def test_zero_query_gives_mean_of_values():
+    lens = [5, 16, 33, 700]
+    wl = W.custom(lens, num_layers=1, seed=313)
+    st = DeviceState(wl)
+    pool = _pool(wl)
+    q0 = torch.zeros_like(st.q[0])
+    pkv.pkv_append_attend(pool, 0, q0, st.k_new[0], st.v_new[0], st.k_pool, st.v_pool,
+                          st.table, st.lens, st.out[0], num_splits=3)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    vp = st.v_pool.cpu().float().numpy()
+    for b, n in enumerate(lens):
+        t = np.arange(n)
+        rows = vp[wl.block_tables[0, b, t // 16], :, t % 16, :]   # [n][8][64]
+        mean = rows.astype(np.float64).mean(axis=0).repeat(4, axis=0)
+        assert_close(st.out[0, b].cpu().numpy(), mean, f"seq {b}")
+
+
+def test_device_index_errors_are_flagged_not_faulted():
+    wl = W.custom([20, 40], num_layers=1, seed=314)
+    st = DeviceState(wl)
+    pool = _pool(wl)
+    # page id past the pool in sequence 1
+    bad = st.table.clone()
+    bad[0, 1, 1] = wl.num_pages + 5
+    pkv.pkv_decode_attention(pool, 0, st.q[0], st.k_pool, st.v_pool, bad, st.lens, st.out[0])
+    assert pkv.pkv_get_error(pool) == pkv.PKV_ERR_OUT_OF_RANGE
+    bad[0, 1, 1] = -3
+    pkv.pkv_append_attend(pool, 0, st.q[0], st.k_new[0], st.v_new[0], st.k_pool, st.v_pool,
+                          bad, st.lens, st.out[0])
+    assert pkv.pkv_get_error(pool) == pkv.PKV_ERR_OUT_OF_RANGE
+    # positions out of range: nothing is written
+    before = st.k_pool.clone()
+    for pos in ([2048, 3], [-1, 3], [5, 4096]):
+        pkv.pkv_append(pool, 0, st.k_new[0], st.v_new[0], st.k_pool, st.v_pool, st.table,
+                       torch.tensor(pos, dtype=torch.int32, device="cuda"))
+        assert pkv.pkv_get_error(pool) == pkv.PKV_ERR_OUT_OF_RANGE
+    # only valid positions were written: compare against a clean append of those
+    # seq_len out of range
+    for lens in ([0, 40], [20, 2049], [-7, 40]):
+        pkv.pkv_decode_attention(pool, 0, st.q[0], st.k_pool, st.v_pool, st.table,
+                                 torch.tensor(lens, dtype=torch.int32, device="cuda"), st.out[0])
+        assert pkv.pkv_get_error(pool) == pkv.PKV_ERR_OUT_OF_RANGE
+    # the flag is cleared by reading it, and the context still works
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    pkv.pkv_decode_attention(pool, 0, st.q[0], st.k_pool, st.v_pool, st.table, st.lens,
+                             st.out[0])
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    del before
+
+
+def test_host_argument_errors():
+    wl = W.custom([20, 40], num_layers=2, seed=315)
+    st = DeviceState(wl)
+    pool = _pool(wl, max_splits=8)
+    L = pool._lib
+    h = pool.handle
+    s = torch.cuda.current_stream().cuda_stream
+    q, kp, vp, t, n, o = (x.data_ptr() for x in (st.q[0], st.k_pool, st.v_pool, st.table,
+                                                st.lens, st.out[0]))
+    assert L.pkv_decode_attention(h, 0, None, kp, vp, t, n, o, 2, 0, s) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_decode_attention(h, 0, q + 2, kp, vp, t, n, o, 2, 0, s) == \
+        pkv.PKV_ERR_INVALID_ARG                                   # misaligned
+    assert L.pkv_decode_attention(h, 2, q, kp, vp, t, n, o, 2, 0, s) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_decode_attention(h, -1, q, kp, vp, t, n, o, 2, 0, s) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_decode_attention(h, 0, q, kp, vp, t, n, o, 3, 0, s) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_decode_attention(h, 0, q, kp, vp, t, n, o, 2, 9, s) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_decode_attention(h, 0, q, kp, vp, t, n, o, 0, 0, s) == pkv.PKV_OK
+    assert L.pkv_append(h, 0, None, None, kp, vp, t, n, 2, s) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_append_attend(h, 0, q, None, None, kp, vp, t, n, o, 2, 0, s) == \
+        pkv.PKV_ERR_INVALID_ARG
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+
+
+# ------------------------------------------------------------ full-size configurations
+FULL = {
+    "llama-b2-2048": (W.llama_default, None),
+    "mix-b64": (W.continuous_mix, [0, 1, 2, 7, 20, 33, 50, 63]),
+    "ragged-b256": (W.large_ragged, [0, 1, 2, 3, 4, 5, 100, 200, 255]),
+    "long-b1": (lambda: W.long_context(1), None),
+    "long-b4": (lambda: W.long_context(4), None),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_fused_step_matches_oracle(name):
+    """Every layer of the workload through the fused step with the library's
+    own split choice (the benchmark's launch configuration); sampled sequences
+    (or all, for small batches) compared with the oracle, and the whole pool
+    checked against the closed-form append."""
+    make, sample = FULL[name]
+    wl = make()
+    st = DeviceState(wl, host_pools=False)
+    sample = list(range(wl.batch)) if sample is None else sample
+    table_s, hk, hv = compact_sample(wl, sample, st.k_pool, st.v_pool)
+    k_before = st.k_pool.clone()
+    v_before = st.v_pool.clone()
+    pool = _pool(wl)
+    for layer in range(wl.num_layers):
+        pkv.pkv_append_attend(pool, layer, st.q[layer], st.k_new[layer], st.v_new[layer],
+                              st.k_pool, st.v_pool, st.table, st.lens, st.out[layer])
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    # whole pool: exactly the appended rows changed, at the closed-form address
+    pos = st.positions.long()
+    for layer in range(wl.num_layers):
+        pages = st.table[layer].long().gather(1, (pos // 16).unsqueeze(1)).squeeze(1)
+        k_before[pages, :, pos % 16, :] = st.k_new[layer]
+        v_before[pages, :, pos % 16, :] = st.v_new[layer]
+    assert torch.equal(k_before.view(torch.int16), st.k_pool.view(torch.int16))
+    assert torch.equal(v_before.view(torch.int16), st.v_pool.view(torch.int16))
+    del k_before, v_before
+    # sampled sequences against the oracle
+    q_b, kn_b, vn_b = (bits(x[:, sample].cpu()) for x in (st.q, st.k_new, st.v_new))
+    lens = wl.seq_lens[sample].copy()
+    ref, _, _ = oracle_step(wl, hk, hv, q_b, kn_b, vn_b, table=table_s, lens=lens, threads=16)
+    got = st.out[:, sample].cpu().numpy()
+    assert_close(got, ref, name)
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+@pytest.mark.parametrize("splits", [1, 4, 16, 32])
+def test_long_context_split_counts_full_size(batch, splits):
+    wl = W.long_context(batch)
+    st = DeviceState(wl, host_pools=False)
+    sample = list(range(batch))
+    table_s, hk, hv = compact_sample(wl, sample, st.k_pool, st.v_pool)
+    pool = _pool(wl)
+    for layer in range(wl.num_layers):
+        pkv.pkv_append_attend(pool, layer, st.q[layer], st.k_new[layer], st.v_new[layer],
+                              st.k_pool, st.v_pool, st.table, st.lens, st.out[layer],
+                              num_splits=splits)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    q_b, kn_b, vn_b = (bits(x.cpu()) for x in (st.q, st.k_new, st.v_new))
+    ref, _, _ = oracle_step(wl, hk, hv, q_b, kn_b, vn_b, table=table_s, lens=wl.seq_lens.copy(),
+                            threads=16)
+    assert_close(st.out.cpu().numpy(), ref, f"B={batch} S={splits}")
