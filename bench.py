@@ -8,8 +8,10 @@ at the pages' default pool: batch 2 at 2,048 tokens, 4,096-page (128 MiB)
 BF16 pool, pages shuffled, BF16 N(0,1) inputs.
 
 Timing: the 16 launches of a step are captured in a CUDA graph with
-GPU-timestamped events before, between and after them; before every step an
-untimed read of a buffer twice the L2 size evicts the cache. value = KV GB/s
+GPU-timestamped events before and after them; before every step an untimed
+read of a buffer twice the L2 size evicts the cache. A second graph of the
+same step with events between the launches gives the per-launch durations of
+the kernel for the roofline. value = KV GB/s
 = algorithmic bytes per step / step time, with algorithmic bytes per
 (sequence, layer) = seq_len x 2048 (every cached K/V row read once) + 2048
 (the new row written) + 4096 (q) + 8192 (FP32 out).
@@ -272,7 +274,7 @@ def run_ours(args, world, rank, local):
     table = torch.from_numpy(wl.block_tables).to(dev)
     lens = torch.from_numpy(wl.seq_lens).to(dev)
     out = torch.zeros((L, B, W.NUM_Q_HEADS, W.HEAD_DIM), device=dev)
-    pool = pkv.pkv_pool_create(L, wl.num_pages, B)
+    pool = pkv.pkv_pool_create(L, wl.num_pages, B, flags=0 if args.no_pdl else pkv.PKV_FLAG_PDL)
     splits = args.splits
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -282,28 +284,37 @@ def run_ours(args, world, rank, local):
         return flush_buf.sum()
 
     stream = torch.cuda.Stream(device=dev)
-    events = [make_event() for _ in range(L + 1)]
-    external = all(e[1] for e in events)
-    events = [e[0] for e in events]
+    made = [make_event() for _ in range(L + 3)]
+    external = all(e[1] for e in made)
+    events = [e[0] for e in made[:L + 1]]       # between the launches (per-launch pass)
+    t_start, t_end = made[L + 1][0], made[L + 2][0]
 
-    def step(with_events):
+    def step(marks=None):
+        """The 16 launches; `marks` = events recorded before, between and after."""
         s = torch.cuda.current_stream()
-        if with_events:
-            events[0].record(s)
+        if marks:
+            marks[0].record(s)
         for layer in range(L):
             pkv.pkv_append_attend(pool, layer, q[layer], k_new[layer], v_new[layer], k_pool,
                                   v_pool, table, lens, out[layer], num_splits=splits, stream=s)
-            if with_events:
-                events[layer + 1].record(s)
+            if marks and len(marks) > 2:
+                marks[layer + 1].record(s)
+        if marks and len(marks) == 2:
+            marks[1].record(s)
 
     with torch.cuda.stream(stream):
-        step(False)
+        step()
     torch.cuda.synchronize()
     assert pkv.pkv_get_error(pool) == pkv.PKV_OK
 
+    # timed graph: events only before and after the 16 launches
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        step(external)
+        step([t_start, t_end] if external else None)
+    # per-launch graph: the same launches with an event between each pair
+    launch_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(launch_graph, stream=stream):
+        step(events if external else None)
 
     # e2e: the same step through the public API with host buffers
     q_h = q.cpu().pin_memory()
@@ -321,7 +332,7 @@ def run_ours(args, world, rank, local):
         k_new.copy_(kn_h, non_blocking=True)
         v_new.copy_(vn_h, non_blocking=True)
         lens.copy_(lens_h, non_blocking=True)
-        step(False)
+        step()
         out_h.copy_(out, non_blocking=True)
         if external:
             e2e_end.record(s)
@@ -340,7 +351,7 @@ def run_ours(args, world, rank, local):
 
     # warm-up
     for _ in range(args.warmup):
-        replay_timed(graph, events[0], events[L])
+        replay_timed(graph, t_start, t_end)
     torch.cuda.synchronize()
 
     # timed region
@@ -348,20 +359,27 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     sampler = ClockSampler(dev)
     time.sleep(0.3)
-    step_ms, launch_ms = [], []
+    step_ms = []
     wall0 = time.perf_counter()
     for _ in range(args.steps):
-        replay_timed(graph, events[0], events[L])
+        replay_timed(graph, t_start, t_end)
         stream.synchronize()
-        step_ms.append(events[0].elapsed_time(events[L]))
-        if external:
-            launch_ms.extend(events[i].elapsed_time(events[i + 1]) for i in range(L))
+        step_ms.append(t_start.elapsed_time(t_end))
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(world)
     clocks = sampler.stop()
     total_ms = max_over_ranks(sum(step_ms), world)
     assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+
+    # per-launch durations of the dominant kernel (same launches, same flush)
+    launch_ms, launch_step_ms = [], []
+    if external:
+        for _ in range(max(3, min(args.steps, 400))):
+            replay_timed(launch_graph, events[0], events[L])
+            stream.synchronize()
+            launch_ms.extend(events[i].elapsed_time(events[i + 1]) for i in range(L))
+            launch_step_ms.append(events[0].elapsed_time(events[L]))
 
     # e2e steps (host buffers, copies inside the timed events)
     e2e_ms = []
@@ -379,12 +397,11 @@ def run_ours(args, world, rank, local):
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
 
-    if launch_ms:
-        per_launch_ms = statistics.mean(launch_ms)
-        launch_source = "CUDA events between the launches inside the timed graph"
-    else:
-        per_launch_ms = ms_per_step / L
-        launch_source = "step time / launches (events inside graphs unsupported here)"
+    # average launch duration: the timed region's events / launches (includes
+    # the graph's gaps between launches, so an upper bound on kernel time)
+    per_launch_ms = ms_per_step / L
+    launch_source = "timed-region CUDA events (start/end of each step) / 16 launches"
+    events_between = (round(statistics.mean(launch_ms), 6) if launch_ms else None)
     achieved = (nbytes / L) / (per_launch_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
 
@@ -400,7 +417,8 @@ def run_ours(args, world, rank, local):
             "workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
             "batch": B, "layers": L, "seq_lens": "all 2048" if np.all(wl.seq_lens == 2048)
             else f"mean {float(wl.seq_lens.mean()):.1f}",
-            "step": "16 x fused append+attend (one launch per layer), CUDA graph",
+            "step": "16 x fused append+attend (one launch per layer), CUDA graph" +
+                    ("" if args.no_pdl else ", programmatic dependent launch between layers"),
             "splits": chunk_note,
             "l2": "flushed before every step (read of a buffer twice the L2 size, outside the "
                   "timed events)",
@@ -422,6 +440,7 @@ def run_ours(args, world, rank, local):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "traffic": traffic, "kernel": "decode_kernel<fused>",
                      "per_launch_ms": round(per_launch_ms, 6), "per_launch_source": launch_source,
+                     "per_launch_ms_with_events_between_launches": events_between,
                      "bytes_per_launch": nbytes // L},
         "wall_s_timed_loop": round(wall, 3),
     }
@@ -448,6 +467,8 @@ def main():
     ap.add_argument("--workload", choices=list(WORKLOADS), default="llama-b2-2048")
     ap.add_argument("--splits", type=int, default=0, help="0: the library chooses")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch without programmatic dependent launch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

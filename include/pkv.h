@@ -67,8 +67,9 @@ typedef enum {
  * 16, 32, 8 and 64. max_seq_len is a multiple of 16, at most 2048, and sets
  * the block-table row length (max_seq_len / 16). max_splits bounds the
  * split-KV count per sequence (0 selects 64; at most 128) and sizes the
- * handle's split workspace. num_pages is the number of pages in the pool
- * the caller allocates: 4096 pages is the pages' default 128 MiB pool
+ * handle's split workspace. flags: PKV_FLAG_* below (0 for none).
+ * num_pages is the number of pages in the pool the caller allocates: 4096
+ * pages is the pages' default 128 MiB pool
  * [samir-vllm: Build LLM Inference From Scratch in C++ and CUDA, "Hardware
  * expectations"]. */
 typedef struct {
@@ -81,7 +82,18 @@ typedef struct {
   int max_seq_len;
   int max_batch;
   int max_splits;
+  int flags;        /* PKV_FLAG_* bits */
 } pkv_pool_config;
+
+/* Launch decode kernels with programmatic dependent launch: a launch may
+ * start while the kernel before it in the stream is still running, and
+ * before waiting for that kernel it reads block_tables, seq_lens and the
+ * pool rows below position seq_lens[b] - 1 (the unfused decode defers the
+ * page holding that position). q, k, v, out and the appended slot are read
+ * or written only after the wait. Contract: the kernel immediately before a
+ * decode launch in the stream must not write block_tables, seq_lens or those
+ * pool rows. Off by default. */
+#define PKV_FLAG_PDL 1
 
 typedef struct pkv_pool* pkv_pool_t;
 
@@ -117,8 +129,13 @@ pkv_status pkv_append(pkv_pool_t pool, int layer, const void* k, const void* v, 
  * the kv head, so every page tile is read once. num_splits = S > 0 splits
  * each sequence's np = ceil(len / 16) pages into ranges of ceil(np / S)
  * pages, computed separately and merged by log-sum-exp inside the same
- * launch; num_splits = 0 lets the library choose (ranges of a fixed page
- * count sized from batch and SM count). S must not exceed max_splits. The
+ * launch: for 2 <= S <= 16 (where the device schedules such clusters) the S
+ * blocks of a (sequence, kv head) form a thread-block cluster and merge
+ * through distributed shared memory; otherwise through the handle's global
+ * partials and a ticket (the last block to finish merges). num_splits = 0
+ * lets the library choose: a cluster split sized so the batch fits one wave
+ * of resident blocks, or for large batches ranges of a fixed page count.
+ * S must not exceed max_splits. The
  * output does not depend on which physical pages hold the data. A sequence
  * with an invalid seq_len is skipped (its out rows are left untouched) and
  * flagged; an invalid page id is skipped and flagged. */

@@ -37,7 +37,10 @@ class PkvError(RuntimeError):
 class PoolConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "num_layers", "num_pages", "page_size", "num_q_heads", "num_kv_heads", "head_dim",
-        "max_seq_len", "max_batch", "max_splits")]
+        "max_seq_len", "max_batch", "max_splits", "flags")]
+
+
+PKV_FLAG_PDL = 1
 
 
 _lib = None
@@ -116,10 +119,10 @@ class Pool:
 
 
 def pkv_pool_create(num_layers, num_pages, max_batch, max_seq_len=MAX_SEQ_LEN, max_splits=0,
-                    lib=None) -> Pool:
+                    flags=0, lib=None) -> Pool:
     lib = lib or load()
     cfg = PoolConfig(num_layers, num_pages, PAGE_SIZE, NUM_Q_HEADS, NUM_KV_HEADS, HEAD_DIM,
-                     max_seq_len, max_batch, max_splits)
+                     max_seq_len, max_batch, max_splits, flags)
     handle = ctypes.c_void_p()
     _check(lib.pkv_pool_create(ctypes.byref(cfg), ctypes.byref(handle)), "pkv_pool_create")
     return Pool(handle.value, cfg, lib)

@@ -45,13 +45,15 @@ constexpr int kHkv = 8;
 constexpr int kGroup = kHq / kHkv;
 constexpr int kDim = 64;
 constexpr int kMaxSeqLen = 2048;
+constexpr int kMaxPages = kMaxSeqLen / 16;
 constexpr int kRowBytes = kDim * 2;             // one token of one kv head: 128 B
 constexpr int kTileBytes = kPage * kRowBytes;   // one (page, kv head) tile: 2 KiB
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 4;                       // page stages per warp
+constexpr int kStages = 3;                       // page stages per warp
 constexpr int kDefaultMaxSplits = 64;
 constexpr int kMaxSplitsLimit = 128;
+constexpr int kMaxClusterSize = 16;                // non-portable cluster size limit
 
 // device error flag bits
 constexpr int kErrPage = 1;
@@ -62,7 +64,7 @@ constexpr int kErrTimeout = 8;
 // about two seconds at the maximum SM clock
 constexpr long long kWaitCycles = 4000000000LL;
 
-struct WarpSmem {
+struct alignas(16) WarpSmem {
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
   float2 p[kPage][kGroup];   // (p, p) per token and head
@@ -70,15 +72,36 @@ struct WarpSmem {
   unsigned long long bar[kStages];
 };
 
-struct BlockSmem {
-  WarpSmem warp[kWarps];
+// scratch of the last block's split merge (the page rings are idle by then)
+struct MergeSmem {
+  float2 ml[kGroup][kMaxSplitsLimit];
+  float w[kGroup][kMaxSplitsLimit];
+  float l[kGroup];
+};
+
+// The cluster leader's inbox: every block of the cluster stores its (m, l, o)
+// for the 4 heads here (placed after BlockSmem, cluster kernels only).
+struct ClusterInbox {
+  float o[kMaxClusterSize][kGroup][kDim];
+  float m[kMaxClusterSize][kGroup];
+  float l[kMaxClusterSize][kGroup];
+};
+
+struct alignas(16) BlockSmem {
+  union {
+    WarpSmem warp[kWarps];
+    MergeSmem merge;
+  };
   float m[kWarps][kGroup];
   float l[kWarps][kGroup];
   float acc[kWarps][kGroup][kDim];
+  int pages[kMaxPages];      // this sequence's block-table row
   int last;
 };
 
 static_assert(sizeof(WarpSmem) % 16 == 0, "warp slab must keep 16-byte alignment");
+static_assert(sizeof(BlockSmem) % 16 == 0, "the cluster inbox follows BlockSmem 16-byte aligned");
+static_assert(sizeof(ClusterInbox) % 16 == 0, "inbox size keeps 16-byte alignment");
 
 struct DecodeParams {
   const uint16_t* q;          // [B][32][64]
@@ -147,6 +170,51 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Thread-block cluster barrier, split: arrive (release) and wait (acquire).
+// A wait completes once every non-exited thread of the cluster has arrived.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store to the same shared-memory offset in cluster block `rank`.
+__device__ __forceinline__ void st_cluster(float* p, uint32_t rank, float v) {
+  uint32_t addr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster2(float* p, uint32_t rank, float2 v) {
+  uint32_t addr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+               : "memory");
+}
+
+// Pull a 128-byte line into L2 (no register result; L2 is coherent, so this
+// cannot return stale data to a later load).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// own prologue, and wait until the previous kernel's results are visible.
+// Both are no-ops when the launch did not opt in.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Bulk copy global -> shared (the copy engine), completion counted in bytes
 // on `bar`. dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -204,8 +272,11 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t* __restrict_
 }
 
 // ---------------------------------------------------------------- decode
-template <bool kFused>
-__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams prm) {
+// kCluster: the splits of one (sequence, kv head) form one thread-block
+// cluster (gridDim.x == cluster size) and merge through distributed shared
+// memory; otherwise splits merge through global partials and a ticket.
+template <bool kFused, bool kCluster>
+__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams prm) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   BlockSmem& sm = *reinterpret_cast<BlockSmem*>(smem_raw);
 
@@ -215,6 +286,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // Before griddepcontrol.wait (programmatic dependent launch) this block
+  // reads only seq_lens, the block table and pool rows below the appended
+  // position; q, the new k/v, the appended slot and out come after it.
+  const int32_t* row = prm.table + static_cast<size_t>(b) * prm.table_stride;
+  // the whole block-table row (at most 512 B) is read alongside seq_len, so
+  // no global read waits on another
+  for (int i = threadIdx.x; i < prm.table_stride; i += kThreads) sm.pages[i] = row[i];
   const int len = prm.seq_lens[b];
   if (len < 1 || len > prm.max_seq_len) {
     if (split == 0 && kvh == 0 && threadIdx.x == 0) set_error(prm.err, kErrSeqLen);
@@ -224,12 +302,16 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
   const int chunk = prm.num_splits > 0 ? (n_pages + prm.num_splits - 1) / prm.num_splits
                                        : prm.chunk_pages;
   const int n_splits = (n_pages + chunk - 1) / chunk;   // non-empty splits of this sequence
-  if (split >= n_splits) return;
-  const int page_begin = split * chunk;
-  const int page_end = min(n_pages, page_begin + chunk);
+  if (kCluster) {
+    if (n_splits == 1 && split > 0) return;   // the same decision in every block of the cluster
+  } else {
+    if (split >= n_splits) return;
+  }
+  const bool active = split < n_splits;       // an idle cluster block only joins the merge
+  const int page_begin = active ? split * chunk : 0;
+  const int page_end = active ? min(n_pages, page_begin + chunk) : 0;
   const int last_page = n_pages - 1;
   const int new_slot = (len - 1) % kPage;               // slot of the appended token
-  const int32_t* row = prm.table + static_cast<size_t>(b) * prm.table_stride;
 
   WarpSmem& ws = sm.warp[warp];
   // pages of this warp: page_begin + warp + 4 i
@@ -241,46 +323,78 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
     for (int s = 0; s < kStages; ++s) mbar_init(&ws.bar[s], 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();   // the block-table row is in shared memory
 
-  // Issue the copies of this warp's i-th page into stage i % kStages. Every
-  // lane calls it; lane 0 drives the copy engine, lanes 0..15 place the
-  // appended token in the fused step.
-  auto issue = [&](int i) {
+  // Physical page of this warp's i-th page (i < mine <= 32) sits in lane i:
+  // one parallel read of the block table instead of one per page.
+  int my_phys = -1;
+  if (lane < mine) my_phys = sm.pages[page_begin + warp + kWarps * lane];
+
+  // Copy engine: rows of this warp's i-th page into stage i % kStages (lane 0
+  // issues). In the fused step the appended row is not copied from the pool.
+  auto issue_copy = [&](int i, int phys) {
+    if (lane != 0) return;
     const int stage = i % kStages;
     const int lp = page_begin + warp + kWarps * i;
-    const int phys = row[lp];
     const bool ok = phys >= 0 && phys < prm.num_pages;
     int rows = lp == last_page ? len - lp * kPage : kPage;
     if (kFused && lp == last_page) rows = new_slot;     // the new row comes from k/v
-    if (lane == 0) {
-      if (!ok) set_error(prm.err, kErrPage);
-      if (ok && rows > 0) {
-        const uint32_t bytes = static_cast<uint32_t>(rows) * kRowBytes;
-        const size_t tile = (static_cast<size_t>(phys) * kHkv + kvh) * (kPage * kDim);
-        mbar_arrive_expect_tx(&ws.bar[stage], 2 * bytes);
-        bulk_load(ws.k[stage], prm.k_pool + tile, bytes, &ws.bar[stage]);
-        bulk_load(ws.v[stage], prm.v_pool + tile, bytes, &ws.bar[stage]);
-      } else {
-        mbar_arrive(&ws.bar[stage]);
-      }
-    }
-    if (kFused && lp == last_page && ok && lane < 16) {
-      const bool is_v = lane >= 8;
-      const int c = lane & 7;
-      const uint16_t* src = (is_v ? prm.v_new : prm.k_new) +
-                            (static_cast<size_t>(b) * kHkv + kvh) * kDim + c * 8;
-      const uint4 val = __ldg(reinterpret_cast<const uint4*>(src));
-      uint16_t* pool = is_v ? prm.v_pool : prm.k_pool;
-      *reinterpret_cast<uint4*>(pool + ((static_cast<size_t>(phys) * kHkv + kvh) * kPage +
-                                        new_slot) * kDim + c * 8) = val;
-      uint8_t* tile = is_v ? ws.v[stage] : ws.k[stage];
-      *reinterpret_cast<uint4*>(tile + new_slot * kRowBytes + c * 16) = val;
+    if (!ok) set_error(prm.err, kErrPage);
+    if (ok && rows > 0) {
+      const uint32_t bytes = static_cast<uint32_t>(rows) * kRowBytes;
+      const size_t tile = (static_cast<size_t>(phys) * kHkv + kvh) * (kPage * kDim);
+      mbar_arrive_expect_tx(&ws.bar[stage], 2 * bytes);
+      bulk_load(ws.k[stage], prm.k_pool + tile, bytes, &ws.bar[stage]);
+      bulk_load(ws.v[stage], prm.v_pool + tile, bytes, &ws.bar[stage]);
+    } else {
+      mbar_arrive(&ws.bar[stage]);
     }
   };
+  // Fused step: lanes 0..15 write the appended token's K/V row to the pool and
+  // to the stage tile (only after the wait: k/v may come from the previous kernel).
+  auto place_new_row = [&](int i, int phys) {
+    const int lp = page_begin + warp + kWarps * i;
+    if (!kFused || lp != last_page || lane >= 16) return;
+    if (phys < 0 || phys >= prm.num_pages) return;
+    const int stage = i % kStages;
+    const bool is_v = lane >= 8;
+    const int c = lane & 7;
+    const uint16_t* src = (is_v ? prm.v_new : prm.k_new) +
+                          (static_cast<size_t>(b) * kHkv + kvh) * kDim + c * 8;
+    const uint4 val = __ldg(reinterpret_cast<const uint4*>(src));
+    uint16_t* pool = is_v ? prm.v_pool : prm.k_pool;
+    *reinterpret_cast<uint4*>(pool + ((static_cast<size_t>(phys) * kHkv + kvh) * kPage +
+                                      new_slot) * kDim + c * 8) = val;
+    uint8_t* tile = is_v ? ws.v[stage] : ws.k[stage];
+    *reinterpret_cast<uint4*>(tile + new_slot * kRowBytes + c * 16) = val;
+  };
 
+  // prefetch; the unfused kernel defers the page holding the appended slot,
+  // which the preceding append kernel may still be writing
   const int n_prefetch = min(mine, kStages);
-  for (int i = 0; i < n_prefetch; ++i) issue(i);
+  int deferred = -1;
+  for (int i = 0; i < n_prefetch; ++i) {
+    const int phys = __shfl_sync(0xffffffffu, my_phys, i);
+    if (!kFused && page_begin + warp + kWarps * i == last_page) {
+      deferred = i;
+    } else {
+      issue_copy(i, phys);
+    }
+  }
+  // q of the 4 heads (512 B) and, fused, the new k/v rows into L2 ahead of the wait
+  if (warp == 0 && lane < 6 && active) {
+    const uint16_t* line = nullptr;
+    if (lane < 4) {
+      line = prm.q + (static_cast<size_t>(b) * kHq + kvh * kGroup + lane) * kDim;
+    } else if (kFused) {
+      line = (lane == 4 ? prm.k_new : prm.v_new) + (static_cast<size_t>(b) * kHkv + kvh) * kDim;
+    }
+    if (line) prefetch_l2(line);
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  if (deferred >= 0) issue_copy(deferred, __shfl_sync(0xffffffffu, my_phys, deferred));
+  for (int i = 0; i < n_prefetch; ++i) place_new_row(i, __shfl_sync(0xffffffffu, my_phys, i));
   int issued = n_prefetch;
   __syncwarp();   // the appended row written by lanes 0..15 is read by every lane
 
@@ -327,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
     const int stage = i % kStages;
     const int lp = page_begin + warp + kWarps * i;
     const int valid = lp == last_page ? len - lp * kPage : kPage;   // tokens in this page
-    const int phys = row[lp];
+    const int phys = __shfl_sync(0xffffffffu, my_phys, i);
     const bool ok = phys >= 0 && phys < prm.num_pages;
     if (!mbar_wait(&ws.bar[stage], (i / kStages) & 1)) {
       timed_out = true;
@@ -436,7 +550,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
     }
     __syncwarp();
     if (i + kStages < mine) {
-      issue(i + kStages);
+      const int next_phys = __shfl_sync(0xffffffffu, my_phys, i + kStages);
+      issue_copy(i + kStages, next_phys);
+      place_new_row(i + kStages, next_phys);
+      __syncwarp();
       issued = i + kStages + 1;
     }
   }
@@ -501,8 +618,55 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
     return;
   }
 
+  if (kCluster) {
+    // ---- cluster merge: every block stores its (m, l, o) into the inbox of
+    // block 0 of the cluster (remote shared-memory stores), arrives on the
+    // cluster barrier and exits; block 0 waits for all arrivals and combines.
+    ClusterInbox& inbox = *reinterpret_cast<ClusterInbox*>(smem_raw + sizeof(BlockSmem));
+    const uint32_t rank = cluster_rank();
+    st_cluster2(&inbox.o[rank][g][d0], 0, O);
+    if (d0 == 0) {
+      st_cluster(&inbox.m[rank][g], 0, M);
+      st_cluster(&inbox.l[rank][g], 0, L);
+    }
+    cluster_arrive_release();
+    if (rank != 0) return;
+    cluster_wait_acquire();
+    const int S = gridDim.x;
+    float mj[kMaxClusterSize], lj[kMaxClusterSize];
+    float2 oj[kMaxClusterSize];
+    #pragma unroll
+    for (int j = 0; j < kMaxClusterSize; ++j) {
+      if (j < S) {
+        mj[j] = inbox.m[j][g];
+        lj[j] = inbox.l[j][g];
+        oj[j] = *reinterpret_cast<const float2*>(&inbox.o[j][g][d0]);
+      } else {
+        mj[j] = -INFINITY;
+        lj[j] = 0.f;
+        oj[j] = make_float2(0.f, 0.f);
+      }
+    }
+    float mx = -INFINITY;
+    #pragma unroll
+    for (int j = 0; j < kMaxClusterSize; ++j) mx = fmaxf(mx, mj[j]);
+    float LL = 0.f;
+    float2 OO = make_float2(0.f, 0.f);
+    #pragma unroll
+    for (int j = 0; j < kMaxClusterSize; ++j) {
+      const float w = mj[j] == -INFINITY ? 0.f : exp2f(mj[j] - mx);
+      LL += w * lj[j];
+      OO.x += w * oj[j].x;
+      OO.y += w * oj[j].y;
+    }
+    const float inv = LL > 0.f ? 1.f / LL : 0.f;
+    *reinterpret_cast<float2*>(prm.out + out_row + d0) = make_float2(OO.x * inv, OO.y * inv);
+    return;
+  }
+
   // ---- split partial, ticket, and the last block's log-sum-exp merge
-  const size_t prow = (static_cast<size_t>(b) * kHq + head) * prm.max_splits;
+  const size_t head0 = (static_cast<size_t>(b) * kHq + kvh * kGroup) * prm.max_splits;
+  const size_t prow = head0 + static_cast<size_t>(g) * prm.max_splits;
   *reinterpret_cast<float2*>(prm.part_o + (prow + split) * kDim + d0) = O;
   if (d0 == 0) prm.part_ml[prow + split] = make_float2(M, L);
   __threadfence();
@@ -517,21 +681,72 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
   __syncthreads();
   if (!sm.last) return;
   __threadfence();
-  float MM = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) MM = fmaxf(MM, __ldcg(&prm.part_ml[prow + s]).x);
-  float LL = 0.f;
-  float2 OO = make_float2(0.f, 0.f);
-  for (int s = 0; s < n_splits; ++s) {
-    const float2 ml = __ldcg(&prm.part_ml[prow + s]);
-    if (ml.x == -INFINITY) continue;
-    const float f = exp2f(ml.x - MM);
-    const float2 o = __ldcg(reinterpret_cast<const float2*>(prm.part_o + (prow + s) * kDim + d0));
-    LL += f * ml.y;
-    OO.x += f * o.x;
-    OO.y += f * o.y;
+
+  // (m, l) of every split and head into shared memory (one parallel pass)
+  MergeSmem& mg = sm.merge;   // aliases the page rings: every copy has landed
+  for (int idx = threadIdx.x; idx < kGroup * n_splits; idx += kThreads) {
+    const int hg = idx / n_splits;
+    const int s = idx - hg * n_splits;
+    mg.ml[hg][s] = __ldcg(&prm.part_ml[head0 + static_cast<size_t>(hg) * prm.max_splits + s]);
   }
-  const float inv = LL > 0.f ? 1.f / LL : 0.f;
-  *reinterpret_cast<float2*>(prm.out + out_row + d0) = make_float2(OO.x * inv, OO.y * inv);
+  __syncthreads();
+  // warp hg: global max, split weights and their sum for head hg
+  {
+    const int hg = warp;
+    float mx = -INFINITY;
+    for (int s = lane; s < n_splits; s += 32) mx = fmaxf(mx, mg.ml[hg][s].x);
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = 0.f;
+    for (int s = lane; s < n_splits; s += 32) {
+      const float2 ml = mg.ml[hg][s];
+      const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mx);
+      mg.w[hg][s] = w;
+      sum += w * ml.y;
+    }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) mg.l[hg] = sum;
+  }
+  __syncthreads();
+  // warp hg, lane: dims 4 quad .. 4 quad + 3 over the splits of one parity
+  {
+    const int hg = warp;
+    const int quad = lane & 15;
+    const int half = lane >> 4;
+    const float* base = prm.part_o + (head0 + static_cast<size_t>(hg) * prm.max_splits) * kDim +
+                        4 * quad;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = half; s0 < n_splits; s0 += 16) {
+      float4 v[8];
+      #pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int s = s0 + 2 * j;
+        v[j] = s < n_splits ? __ldcg(reinterpret_cast<const float4*>(base + s * kDim))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      #pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int s = s0 + 2 * j;
+        const float w = s < n_splits ? mg.w[hg][s] : 0.f;
+        o.x += w * v[j].x;
+        o.y += w * v[j].y;
+        o.z += w * v[j].z;
+        o.w += w * v[j].w;
+      }
+    }
+    o.x += __shfl_xor_sync(0xffffffffu, o.x, 16);
+    o.y += __shfl_xor_sync(0xffffffffu, o.y, 16);
+    o.z += __shfl_xor_sync(0xffffffffu, o.z, 16);
+    o.w += __shfl_xor_sync(0xffffffffu, o.w, 16);
+    if (half == 0) {
+      const float LL = mg.l[hg];
+      const float inv = LL > 0.f ? 1.f / LL : 0.f;
+      *reinterpret_cast<float4*>(prm.out + (static_cast<size_t>(b) * kHq + kvh * kGroup + hg) *
+                                               kDim + 4 * quad) =
+          make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+    }
+  }
 }
 
 }  // namespace
@@ -542,6 +757,9 @@ struct pkv_pool {
   pkv_pool_config cfg;
   int device;
   int num_sms;
+  int blocks_per_sm;           // resident decode blocks per SM (occupancy API)
+  int cluster_blocks_per_sm;   // the same for the cluster-merge kernel
+  int max_cluster;     // largest cluster size (power of two <= 16) the device schedules
   float* part_o;     // [2][max_batch][32][max_splits][64]
   float2* part_ml;   // [2][max_batch][32][max_splits]
   int* tickets;      // [2][max_batch][8]
@@ -552,25 +770,54 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-size_t smem_bytes() { return sizeof(BlockSmem); }
+size_t smem_bytes(bool cluster) {
+  return sizeof(BlockSmem) + (cluster ? sizeof(ClusterInbox) : 0);
+}
+
+template <typename Kernel>
+bool set_kernel_attributes(Kernel kernel, bool cluster) {
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes(cluster))) != cudaSuccess)
+    return false;
+  if (cluster &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess)
+    return false;
+  return true;
+}
 
 pkv_status check_launch() {
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-// Pages per split when the caller leaves the choice to the library: enough
-// blocks to keep every SM busy when all sequences are at full length,
-// capped so that one block's range stays short.
+// Pages per split when the caller leaves the choice to the library: the
+// fewest pages per block (at least one per warp) for which a batch of
+// full-length sequences still fits in one wave of resident blocks; past 16
+// pages a block's range would make long sequences the tail, so large
+// batches take 16 and run several waves.
 int auto_chunk_pages(const pkv_pool* pool, int batch) {
   const int max_pages = pool->cfg.max_seq_len / kPage;
-  const long long tiles = static_cast<long long>(batch) * kHkv * max_pages;
-  const long long target_blocks = 4LL * pool->num_sms;
-  long long chunk = (tiles + target_blocks - 1) / target_blocks;
   const int min_chunk = (max_pages + pool->cfg.max_splits - 1) / pool->cfg.max_splits;
-  if (chunk < 2) chunk = 2;
-  if (chunk > 16) chunk = 16;
-  if (chunk < min_chunk) chunk = min_chunk;
-  return static_cast<int>(chunk);
+  const long long resident = static_cast<long long>(pool->blocks_per_sm) * pool->num_sms;
+  for (int chunk = kWarps > min_chunk ? kWarps : min_chunk; chunk < 16; ++chunk) {
+    const long long blocks =
+        static_cast<long long>(batch) * kHkv * ((max_pages + chunk - 1) / chunk);
+    if (blocks <= resident) return chunk;
+  }
+  return 16 > min_chunk ? 16 : min_chunk;
+}
+
+// Splits per sequence for a cluster merge when the library chooses: the
+// largest cluster (16, 8, 4, 2) for which batch x 8 kv heads x S blocks fit in
+// one wave of resident blocks; 0 when even S = 2 would not (large batches).
+int auto_cluster_splits(const pkv_pool* pool, int batch) {
+  const long long resident = static_cast<long long>(pool->cluster_blocks_per_sm) * pool->num_sms;
+  const int max_pages = pool->cfg.max_seq_len / kPage;
+  for (int s = pool->max_cluster; s >= 2; s /= 2) {
+    if (s > pool->cfg.max_splits || s > max_pages) continue;
+    if (static_cast<long long>(batch) * kHkv * s <= resident) return s;
+  }
+  return 0;
 }
 
 template <bool kFused>
@@ -613,12 +860,53 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   prm.table_stride = max_pages;
   prm.max_seq_len = c.max_seq_len;
   prm.max_splits = c.max_splits;
-  prm.num_splits = num_splits;
-  prm.chunk_pages = num_splits > 0 ? 0 : auto_chunk_pages(pool, batch);
-  const int grid_splits = num_splits > 0 ? num_splits
-                                         : (max_pages + prm.chunk_pages - 1) / prm.chunk_pages;
-  dim3 grid(grid_splits, kHkv, batch);
-  decode_kernel<kFused><<<grid, kThreads, smem_bytes(), static_cast<cudaStream_t>(stream)>>>(prm);
+
+  // Plan: S splits per sequence merged in a cluster when 2 <= S <= the
+  // largest cluster this device schedules; otherwise (S = 1, S larger, or a
+  // batch too large for one wave of clusters) global partials and a ticket.
+  int cluster = 0;
+  if (num_splits == 0) {
+    cluster = auto_cluster_splits(pool, batch);
+    if (cluster >= 2) {
+      prm.num_splits = cluster;
+      prm.chunk_pages = 0;
+    } else {
+      cluster = 0;
+      prm.num_splits = 0;
+      prm.chunk_pages = auto_chunk_pages(pool, batch);
+    }
+  } else {
+    prm.num_splits = num_splits;
+    prm.chunk_pages = 0;
+    if (num_splits >= 2 && num_splits <= pool->max_cluster) cluster = num_splits;
+  }
+  const int grid_splits = prm.num_splits > 0 ? prm.num_splits
+                                             : (max_pages + prm.chunk_pages - 1) / prm.chunk_pages;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_splits, kHkv, batch);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes(cluster != 0);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attrs[2];
+  int n_attrs = 0;
+  if (cluster) {
+    attrs[n_attrs].id = cudaLaunchAttributeClusterDimension;
+    attrs[n_attrs].val.clusterDim.x = cluster;
+    attrs[n_attrs].val.clusterDim.y = 1;
+    attrs[n_attrs].val.clusterDim.z = 1;
+    ++n_attrs;
+  }
+  if (c.flags & PKV_FLAG_PDL) {
+    attrs[n_attrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n_attrs].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attrs;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n_attrs;
+  cudaError_t e = cluster ? cudaLaunchKernelEx(&cfg, decode_kernel<kFused, true>, prm)
+                          : cudaLaunchKernelEx(&cfg, decode_kernel<kFused, false>, prm);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
   return check_launch();
 }
 
@@ -668,10 +956,37 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
   ok = ok && cudaMemset(pool->tickets, 0, 2 * static_cast<size_t>(c.max_batch) * kHkv * sizeof(int)) ==
                  cudaSuccess;
   ok = ok && cudaMemset(pool->err, 0, sizeof(int)) == cudaSuccess;
-  ok = ok && cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(smem_bytes())) == cudaSuccess;
-  ok = ok && cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(smem_bytes())) == cudaSuccess;
+  ok = ok && set_kernel_attributes(decode_kernel<false, false>, false);
+  ok = ok && set_kernel_attributes(decode_kernel<true, false>, false);
+  ok = ok && set_kernel_attributes(decode_kernel<false, true>, true);
+  ok = ok && set_kernel_attributes(decode_kernel<true, true>, true);
+  ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                  &pool->blocks_per_sm, decode_kernel<true, false>, kThreads, smem_bytes(false)) ==
+                  cudaSuccess;
+  ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                  &pool->cluster_blocks_per_sm, decode_kernel<true, true>, kThreads,
+                  smem_bytes(true)) == cudaSuccess;
+  pool->max_cluster = 0;
+  for (int size = kMaxClusterSize; ok && size >= 2 && !pool->max_cluster; size /= 2) {
+    cudaLaunchConfig_t probe = {};
+    probe.gridDim = dim3(size, kHkv, 1);
+    probe.blockDim = dim3(kThreads, 1, 1);
+    probe.dynamicSmemBytes = smem_bytes(true);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = size;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    probe.attrs = &attr;
+    probe.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, decode_kernel<true, true>, &probe) ==
+            cudaSuccess && clusters > 0)
+      pool->max_cluster = size;
+    cudaGetLastError();   // a size the device refuses is not an error here
+  }
+  if (ok && pool->blocks_per_sm < 1) pool->blocks_per_sm = 1;
+  if (ok && pool->cluster_blocks_per_sm < 1) pool->cluster_blocks_per_sm = 1;
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     pkv_pool_destroy(pool);

@@ -59,18 +59,18 @@ def test_create_rejects_bad_geometry_without_touching_the_device(lib):
                                     ctypes.POINTER(ctypes.c_void_p)]
     h = ctypes.c_void_p()
     bad = [
-        pkv.PoolConfig(16, 4096, 8, 32, 8, 64, 2048, 2, 0),    # page size 8
-        pkv.PoolConfig(16, 4096, 16, 32, 4, 64, 2048, 2, 0),   # 4 kv heads
-        pkv.PoolConfig(16, 4096, 16, 32, 8, 128, 2048, 2, 0),  # head_dim 128
+        pkv.PoolConfig(16, 4096, 8, 32, 8, 64, 2048, 2, 0, 0),    # page size 8
+        pkv.PoolConfig(16, 4096, 16, 32, 4, 64, 2048, 2, 0, 0),   # 4 kv heads
+        pkv.PoolConfig(16, 4096, 16, 32, 8, 128, 2048, 2, 0, 0),  # head_dim 128
     ]
     for cfg in bad:
         assert lib.pkv_pool_create(ctypes.byref(cfg), ctypes.byref(h)) == pkv.PKV_ERR_UNSUPPORTED
     invalid = [
-        pkv.PoolConfig(0, 4096, 16, 32, 8, 64, 2048, 2, 0),    # no layers
-        pkv.PoolConfig(16, 4096, 16, 32, 8, 64, 4096, 2, 0),   # context past 2048
-        pkv.PoolConfig(16, 4096, 16, 32, 8, 64, 2040, 2, 0),   # not a page multiple
-        pkv.PoolConfig(16, 4096, 16, 32, 8, 64, 2048, 0, 0),   # no batch
-        pkv.PoolConfig(16, 4096, 16, 32, 8, 64, 2048, 2, 129), # too many splits
+        pkv.PoolConfig(0, 4096, 16, 32, 8, 64, 2048, 2, 0, 0),    # no layers
+        pkv.PoolConfig(16, 4096, 16, 32, 8, 64, 4096, 2, 0, 0),   # context past 2048
+        pkv.PoolConfig(16, 4096, 16, 32, 8, 64, 2040, 2, 0, 0),   # not a page multiple
+        pkv.PoolConfig(16, 4096, 16, 32, 8, 64, 2048, 0, 0, 0),   # no batch
+        pkv.PoolConfig(16, 4096, 16, 32, 8, 64, 2048, 2, 129, 0), # too many splits
     ]
     for cfg in invalid:
         assert lib.pkv_pool_create(ctypes.byref(cfg), ctypes.byref(h)) == pkv.PKV_ERR_INVALID_ARG

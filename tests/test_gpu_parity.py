@@ -27,8 +27,9 @@ def _library():
     pkv.load()
 
 
-def _pool(wl, max_splits=0):
-    return pkv.pkv_pool_create(wl.num_layers, wl.num_pages, wl.batch, max_splits=max_splits)
+def _pool(wl, max_splits=0, flags=0):
+    return pkv.pkv_pool_create(wl.num_layers, wl.num_pages, wl.batch, max_splits=max_splits,
+                               flags=flags)
 
 
 def _host_inputs(st):
@@ -98,7 +99,7 @@ def test_split_counts_against_unsplit_oracle(batch):
     q_b, kn_b, vn_b = _host_inputs(st)
     ref, _, _ = oracle_step(wl, st.host_k, st.host_v, q_b, kn_b, vn_b)
     results = {}
-    for splits in (1, 2, 4, 16, 32, 64, 128, 0):
+    for splits in (1, 2, 3, 4, 5, 8, 16, 32, 64, 128, 0):
         pool = _pool(wl, max_splits=128)
         k0, v0 = st.k_pool.clone(), st.v_pool.clone()
         out = torch.full_like(st.out, float("nan"))
@@ -110,6 +111,48 @@ def test_split_counts_against_unsplit_oracle(batch):
         assert_close(results[splits], ref, f"B={batch} S={splits}")
     # S = 1 and S = 32 agree to within rounding
     assert np.abs(results[1] - results[32]).max() <= 2 * 5e-4
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("graph", [False, True])
+def test_programmatic_dependent_launch_chain_matches_oracle(fused, graph):
+    """Layers launched back to back with programmatic dependent launch (each
+    launch may start before the previous one ends): the unfused chain
+    alternates append and decode, so decode must not prefetch the page the
+    preceding append writes."""
+    wl = W.custom([1, 16, 17, 300, 2047, 2048, 2048, 40], num_layers=4, seed=320,
+                  name="pdl-chain")
+    st = DeviceState(wl)
+    ref, ok, ov = oracle_step(wl, st.host_k, st.host_v, *_host_inputs(st))
+    for splits in (0, 4, 32):
+        pool = _pool(wl, flags=pkv.PKV_FLAG_PDL)
+        kp, vp = st.k_pool.clone(), st.v_pool.clone()
+        out = torch.full_like(st.out, float("nan"))
+
+        def chain():
+            for layer in range(wl.num_layers):
+                if fused:
+                    pkv.pkv_append_attend(pool, layer, st.q[layer], st.k_new[layer],
+                                          st.v_new[layer], kp, vp, st.table, st.lens, out[layer],
+                                          num_splits=splits)
+                else:
+                    pkv.pkv_append(pool, layer, st.k_new[layer], st.v_new[layer], kp, vp,
+                                   st.table, st.positions)
+                    pkv.pkv_decode_attention(pool, layer, st.q[layer], kp, vp, st.table, st.lens,
+                                             out[layer], num_splits=splits)
+
+        if graph:
+            s = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                chain()
+            g.replay()
+            torch.cuda.synchronize()
+        else:
+            chain()
+        assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+        assert np.array_equal(bits(kp), ok) and np.array_equal(bits(vp), ov)
+        assert_close(out.cpu().numpy(), ref, f"pdl fused={fused} graph={graph} S={splits}")
 
 
 def test_output_independent_of_physical_pages():
