@@ -48,9 +48,16 @@ constexpr int kMaxSeqLen = 2048;
 constexpr int kMaxPages = kMaxSeqLen / 16;
 constexpr int kRowBytes = kDim * 2;             // one token of one kv head: 128 B
 constexpr int kTileBytes = kPage * kRowBytes;   // one (page, kv head) tile: 2 KiB
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;                       // page stages per warp
+// Block shapes: 4 warps with 3 page stages per warp. The ticket-merge kernel
+// fits 4 blocks per SM; the cluster-merge kernel (plus its inbox) 3, which
+// leaves room for the next launch's blocks to become resident and prefetch
+// while this one finishes (8-warp cluster blocks, 2 per SM, measured slower
+// for 2 sequences because the next layer could not start early).
+constexpr int kTicketWarps = 4;
+constexpr int kTicketStages = 3;
+constexpr int kClusterWarps = 4;
+constexpr int kClusterStages = 3;
+constexpr int kMergeThreads = 128;               // one thread per (head, dim pair)
 constexpr int kDefaultMaxSplits = 64;
 constexpr int kMaxSplitsLimit = 128;
 constexpr int kMaxClusterSize = 16;                // non-portable cluster size limit
@@ -64,6 +71,7 @@ constexpr int kErrTimeout = 8;
 // about two seconds at the maximum SM clock
 constexpr long long kWaitCycles = 4000000000LL;
 
+template <int kStages>
 struct alignas(16) WarpSmem {
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
@@ -87,9 +95,10 @@ struct ClusterInbox {
   float l[kMaxClusterSize][kGroup];
 };
 
+template <int kWarps, int kStages>
 struct alignas(16) BlockSmem {
   union {
-    WarpSmem warp[kWarps];
+    WarpSmem<kStages> warp[kWarps];
     MergeSmem merge;
   };
   float m[kWarps][kGroup];
@@ -99,8 +108,10 @@ struct alignas(16) BlockSmem {
   int last;
 };
 
-static_assert(sizeof(WarpSmem) % 16 == 0, "warp slab must keep 16-byte alignment");
-static_assert(sizeof(BlockSmem) % 16 == 0, "the cluster inbox follows BlockSmem 16-byte aligned");
+static_assert(sizeof(WarpSmem<kTicketStages>) % 16 == 0 && sizeof(WarpSmem<kClusterStages>) % 16 == 0,
+              "warp slabs keep 16-byte alignment");
+static_assert(sizeof(BlockSmem<kClusterWarps, kClusterStages>) % 16 == 0,
+              "the cluster inbox follows BlockSmem 16-byte aligned");
 static_assert(sizeof(ClusterInbox) % 16 == 0, "inbox size keeps 16-byte alignment");
 
 struct DecodeParams {
@@ -275,10 +286,12 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t* __restrict_
 // kCluster: the splits of one (sequence, kv head) form one thread-block
 // cluster (gridDim.x == cluster size) and merge through distributed shared
 // memory; otherwise splits merge through global partials and a ticket.
-template <bool kFused, bool kCluster>
-__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams prm) {
+template <bool kFused, bool kCluster, int kWarps, int kStages>
+__global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const DecodeParams prm) {
+  constexpr int kThreads = kWarps * 32;
+  using Smem = BlockSmem<kWarps, kStages>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  BlockSmem& sm = *reinterpret_cast<BlockSmem*>(smem_raw);
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
 
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
@@ -313,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
   const int last_page = n_pages - 1;
   const int new_slot = (len - 1) % kPage;               // slot of the appended token
 
-  WarpSmem& ws = sm.warp[warp];
+  WarpSmem<kStages>& ws = sm.warp[warp];
   // pages of this warp: page_begin + warp + 4 i
   const int mine = page_begin + warp < page_end
                        ? (page_end - (page_begin + warp) + kWarps - 1) / kWarps
@@ -593,8 +606,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
   }
   __syncthreads();
 
-  // ---- merge the 4 warps: thread -> (head g, dims d0, d0 + 1)
-  const int g = threadIdx.x >> 5;
+  // ---- merge the warps: threads 0..127 own (head g, dims d0, d0 + 1); the
+  // rest of an 8-warp block computes an alias and writes nothing
+  const bool merger = threadIdx.x < kMergeThreads;
+  const int g = (threadIdx.x >> 5) & (kGroup - 1);
   const int d0 = 2 * (threadIdx.x & 31);
   float M = -INFINITY;
   #pragma unroll
@@ -614,23 +629,26 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
   const size_t out_row = (static_cast<size_t>(b) * kHq + head) * kDim;
   if (n_splits == 1) {
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    *reinterpret_cast<float2*>(prm.out + out_row + d0) = make_float2(O.x * inv, O.y * inv);
+    if (merger)
+      *reinterpret_cast<float2*>(prm.out + out_row + d0) = make_float2(O.x * inv, O.y * inv);
     return;
   }
 
-  if (kCluster) {
+  if constexpr (kCluster) {
     // ---- cluster merge: every block stores its (m, l, o) into the inbox of
     // block 0 of the cluster (remote shared-memory stores), arrives on the
     // cluster barrier and exits; block 0 waits for all arrivals and combines.
-    ClusterInbox& inbox = *reinterpret_cast<ClusterInbox*>(smem_raw + sizeof(BlockSmem));
+    ClusterInbox& inbox = *reinterpret_cast<ClusterInbox*>(smem_raw + sizeof(Smem));
     const uint32_t rank = cluster_rank();
-    st_cluster2(&inbox.o[rank][g][d0], 0, O);
-    if (d0 == 0) {
-      st_cluster(&inbox.m[rank][g], 0, M);
-      st_cluster(&inbox.l[rank][g], 0, L);
+    if (merger) {
+      st_cluster2(&inbox.o[rank][g][d0], 0, O);
+      if (d0 == 0) {
+        st_cluster(&inbox.m[rank][g], 0, M);
+        st_cluster(&inbox.l[rank][g], 0, L);
+      }
     }
     cluster_arrive_release();
-    if (rank != 0) return;
+    if (rank != 0 || !merger) return;
     cluster_wait_acquire();
     const int S = gridDim.x;
     float mj[kMaxClusterSize], lj[kMaxClusterSize];
@@ -662,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
     const float inv = LL > 0.f ? 1.f / LL : 0.f;
     *reinterpret_cast<float2*>(prm.out + out_row + d0) = make_float2(OO.x * inv, OO.y * inv);
     return;
-  }
-
+  } else {
+  static_assert(kWarps == kGroup, "the ticket merge maps one warp to each head");
   // ---- split partial, ticket, and the last block's log-sum-exp merge
   const size_t head0 = (static_cast<size_t>(b) * kHq + kvh * kGroup) * prm.max_splits;
   const size_t prow = head0 + static_cast<size_t>(g) * prm.max_splits;
@@ -747,6 +765,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
           make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
     }
   }
+  }  // ticket merge
 }
 
 }  // namespace
@@ -770,9 +789,19 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The two kernel shapes: ticket merge (4 warps, 3 stages) and cluster merge
+// (8 warps, 2 stages, plus the leader's inbox).
+template <bool kFused>
+constexpr auto ticket_kernel = decode_kernel<kFused, false, kTicketWarps, kTicketStages>;
+template <bool kFused>
+constexpr auto cluster_kernel = decode_kernel<kFused, true, kClusterWarps, kClusterStages>;
+
 size_t smem_bytes(bool cluster) {
-  return sizeof(BlockSmem) + (cluster ? sizeof(ClusterInbox) : 0);
+  return cluster ? sizeof(BlockSmem<kClusterWarps, kClusterStages>) + sizeof(ClusterInbox)
+                 : sizeof(BlockSmem<kTicketWarps, kTicketStages>);
 }
+
+int block_threads(bool cluster) { return 32 * (cluster ? kClusterWarps : kTicketWarps); }
 
 template <typename Kernel>
 bool set_kernel_attributes(Kernel kernel, bool cluster) {
@@ -799,7 +828,7 @@ int auto_chunk_pages(const pkv_pool* pool, int batch) {
   const int max_pages = pool->cfg.max_seq_len / kPage;
   const int min_chunk = (max_pages + pool->cfg.max_splits - 1) / pool->cfg.max_splits;
   const long long resident = static_cast<long long>(pool->blocks_per_sm) * pool->num_sms;
-  for (int chunk = kWarps > min_chunk ? kWarps : min_chunk; chunk < 16; ++chunk) {
+  for (int chunk = kTicketWarps > min_chunk ? kTicketWarps : min_chunk; chunk < 16; ++chunk) {
     const long long blocks =
         static_cast<long long>(batch) * kHkv * ((max_pages + chunk - 1) / chunk);
     if (blocks <= resident) return chunk;
@@ -885,7 +914,7 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid_splits, kHkv, batch);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(block_threads(cluster != 0), 1, 1);
   cfg.dynamicSmemBytes = smem_bytes(cluster != 0);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attrs[2];
@@ -904,8 +933,8 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   }
   cfg.attrs = attrs;
   cfg.numAttrs = n_attrs;
-  cudaError_t e = cluster ? cudaLaunchKernelEx(&cfg, decode_kernel<kFused, true>, prm)
-                          : cudaLaunchKernelEx(&cfg, decode_kernel<kFused, false>, prm);
+  cudaError_t e = cluster ? cudaLaunchKernelEx(&cfg, cluster_kernel<kFused>, prm)
+                          : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused>, prm);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return check_launch();
 }
@@ -956,21 +985,21 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
   ok = ok && cudaMemset(pool->tickets, 0, 2 * static_cast<size_t>(c.max_batch) * kHkv * sizeof(int)) ==
                  cudaSuccess;
   ok = ok && cudaMemset(pool->err, 0, sizeof(int)) == cudaSuccess;
-  ok = ok && set_kernel_attributes(decode_kernel<false, false>, false);
-  ok = ok && set_kernel_attributes(decode_kernel<true, false>, false);
-  ok = ok && set_kernel_attributes(decode_kernel<false, true>, true);
-  ok = ok && set_kernel_attributes(decode_kernel<true, true>, true);
+  ok = ok && set_kernel_attributes(ticket_kernel<false>, false);
+  ok = ok && set_kernel_attributes(ticket_kernel<true>, false);
+  ok = ok && set_kernel_attributes(cluster_kernel<false>, true);
+  ok = ok && set_kernel_attributes(cluster_kernel<true>, true);
   ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                  &pool->blocks_per_sm, decode_kernel<true, false>, kThreads, smem_bytes(false)) ==
-                  cudaSuccess;
+                  &pool->blocks_per_sm, ticket_kernel<true>, block_threads(false),
+                  smem_bytes(false)) == cudaSuccess;
   ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                  &pool->cluster_blocks_per_sm, decode_kernel<true, true>, kThreads,
+                  &pool->cluster_blocks_per_sm, cluster_kernel<true>, block_threads(true),
                   smem_bytes(true)) == cudaSuccess;
   pool->max_cluster = 0;
   for (int size = kMaxClusterSize; ok && size >= 2 && !pool->max_cluster; size /= 2) {
     cudaLaunchConfig_t probe = {};
     probe.gridDim = dim3(size, kHkv, 1);
-    probe.blockDim = dim3(kThreads, 1, 1);
+    probe.blockDim = dim3(block_threads(true), 1, 1);
     probe.dynamicSmemBytes = smem_bytes(true);
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -980,7 +1009,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
     probe.attrs = &attr;
     probe.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, decode_kernel<true, true>, &probe) ==
+    if (cudaOccupancyMaxActiveClusters(&clusters, cluster_kernel<true>, &probe) ==
             cudaSuccess && clusters > 0)
       pool->max_cluster = size;
     cudaGetLastError();   // a size the device refuses is not an error here
