@@ -60,7 +60,8 @@ typedef enum {
   PKV_ERR_OUT_OF_RANGE = 2,   /* device data: page id, position or seq_len */
   PKV_ERR_CUDA = 3,           /* a CUDA runtime call failed */
   PKV_ERR_UNSUPPORTED = 4,    /* geometry this library is not built for */
-  PKV_ERR_DEVICE_TIMEOUT = 5  /* a bounded in-kernel wait gave up */
+  PKV_ERR_DEVICE_TIMEOUT = 5, /* a bounded in-kernel wait gave up */
+  PKV_ERR_STATIC_LIMIT = 6    /* request larger than pkv_decode_attention_noalloc's scratch */
 } pkv_status;
 
 /* Pool geometry. page_size, num_q_heads, num_kv_heads and head_dim must be
@@ -157,6 +158,40 @@ pkv_status pkv_append_attend(pkv_pool_t pool, int layer, const void* q, const vo
  * flag: PKV_OK, PKV_ERR_OUT_OF_RANGE or PKV_ERR_DEVICE_TIMEOUT (or CUDA if
  * the synchronisation itself failed). */
 pkv_status pkv_get_error(pkv_pool_t pool, void* stream);
+
+/* Decode attention that allocates no device memory. This entry point has no
+ * counterpart in the pages; it exists for callers that may not allocate:
+ * code running under another component's memory allocator (a framework or
+ * server that owns every device allocation and forbids direct cudaMalloc),
+ * latency-critical loops that cannot afford the implicit synchronisation and
+ * possible failure of an allocation, and hosts that must never hit
+ * out-of-memory after start-up. It needs no pool handle.
+ *
+ * It computes what pkv_decode_attention computes, with the same argument
+ * meanings and layouts, and always merges splits through partials and
+ * tickets. Those live in one file-scope device array of this library,
+ * about 2.1 MiB, which every GPU that loads the library holds until the
+ * process exits. Limits: 1 <= num_splits <= 16, batch <= 256 and
+ * batch x num_splits <= 256; larger requests return PKV_ERR_STATIC_LIMIT
+ * and launch nothing. Geometry arguments describe the caller's pool and
+ * tables (num_layers, num_pages, max_batch = block-table rows per layer,
+ * max_seq_len = 16 x block-table row length).
+ *
+ * error_bits: optional device int the caller allocates and zeroes; device
+ * index errors (page id, seq_len) are OR-ed into it. NULL: not reported.
+ *
+ * The first call on each device does a one-time set-up (looks up the
+ * array's device address and sets the kernel's shared-memory limit); make
+ * that first call before any stream capture. The ticket counters are
+ * cleared on the stream at every call. All calls share the one array, so
+ * calls that may overlap on the GPU (on different streams, or from several
+ * host threads) race and must be serialised by the caller. */
+pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_pool,
+                                        const void* v_pool, const int32_t* block_tables,
+                                        const int32_t* seq_lens, float* out, int num_layers,
+                                        int num_pages, int max_batch, int max_seq_len,
+                                        int batch, int num_splits, int* error_bits,
+                                        void* stream);
 
 /* Static text for a status code. */
 const char* pkv_status_string(pkv_status status);

@@ -20,12 +20,13 @@ HEAD_DIM = 64
 MAX_SEQ_LEN = 2048
 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_OUT_OF_RANGE", 3: "PKV_ERR_CUDA",
-          4: "PKV_ERR_UNSUPPORTED", 5: "PKV_ERR_DEVICE_TIMEOUT"}
+          4: "PKV_ERR_UNSUPPORTED", 5: "PKV_ERR_DEVICE_TIMEOUT", 6: "PKV_ERR_STATIC_LIMIT"}
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OUT_OF_RANGE, PKV_ERR_CUDA, PKV_ERR_UNSUPPORTED, \
-    PKV_ERR_DEVICE_TIMEOUT = range(6)
+    PKV_ERR_DEVICE_TIMEOUT, PKV_ERR_STATIC_LIMIT = range(7)
 
 EXPORTED = ("pkv_pool_create", "pkv_pool_destroy", "pkv_append", "pkv_decode_attention",
-            "pkv_append_attend", "pkv_get_error", "pkv_status_string")
+            "pkv_append_attend", "pkv_get_error", "pkv_decode_attention_noalloc",
+            "pkv_status_string")
 
 
 class PkvError(RuntimeError):
@@ -66,6 +67,7 @@ def load(path: str = None):
     lib.pkv_decode_attention.argtypes = [P, i, P, P, P, P, P, P, i, i, P]
     lib.pkv_append_attend.argtypes = [P, i, P, P, P, P, P, P, P, P, i, i, P]
     lib.pkv_get_error.argtypes = [P, P]
+    lib.pkv_decode_attention_noalloc.argtypes = [i, P, P, P, P, P, P, i, i, i, i, i, i, P, P]
     lib.pkv_status_string.argtypes = [i]
     lib.pkv_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -168,3 +170,19 @@ def pkv_append_attend(pool: Pool, layer, q, k, v, k_pool, v_pool, block_tables, 
 def pkv_get_error(pool: Pool, stream=None) -> int:
     """Synchronises the stream; returns (and clears) the sticky device status."""
     return pool._lib.pkv_get_error(pool.handle, _stream(stream))
+
+
+def pkv_decode_attention_noalloc(layer, q, k_pool, v_pool, block_tables, seq_lens, out,
+                                 num_layers, num_pages, max_batch, max_seq_len=MAX_SEQ_LEN,
+                                 batch=None, num_splits=1, error_bits=None, stream=None,
+                                 lib=None):
+    """Decode attention for callers that may not allocate device memory: no
+    pool handle, scratch in the library's own static device array (limits and
+    the one-time set-up on first use are described in include/pkv.h)."""
+    lib = lib or load()
+    st = lib.pkv_decode_attention_noalloc(int(layer), _addr(q), _addr(k_pool), _addr(v_pool),
+                                          _addr(block_tables), _addr(seq_lens), _addr(out),
+                                          int(num_layers), int(num_pages), int(max_batch),
+                                          int(max_seq_len), _batch(seq_lens, batch),
+                                          int(num_splits), _addr(error_bits), _stream(stream))
+    _check(st, "pkv_decode_attention_noalloc")

@@ -35,6 +35,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "pkv.h"
 
 namespace {
@@ -939,9 +941,98 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   return check_launch();
 }
 
+// ---------------------------------------------------------------- no-allocation entry point
+// Scratch of pkv_decode_attention_noalloc: split partials and tickets for up
+// to kStaticRows (sequence, split) pairs, plus a sink for unreported errors.
+constexpr int kStaticRows = 256;        // batch x num_splits
+constexpr int kStaticMaxSplits = 16;
+
+struct StaticScratch {
+  float part_o[kStaticRows * kHq][kDim];
+  float2 part_ml[kStaticRows * kHq];
+  int tickets[kStaticRows * kHkv];
+  int error_sink;
+};
+
+static __device__ __align__(256) unsigned char g_static_scratch[sizeof(StaticScratch)];
+
+// Device address of g_static_scratch per device, looked up once (the array's
+// name in host code is only a stand-in, not a device address).
+pkv_status static_scratch_address(StaticScratch** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex lock;
+  static StaticScratch* address[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> guard(lock);
+  if (!address[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return PKV_ERR_CUDA;
+    if (!set_kernel_attributes(ticket_kernel<false>, false)) return PKV_ERR_CUDA;
+    address[dev] = static_cast<StaticScratch*>(ptr);
+  }
+  *out = address[dev];
+  return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_pool,
+                                        const void* v_pool, const int32_t* block_tables,
+                                        const int32_t* seq_lens, float* out, int num_layers,
+                                        int num_pages, int max_batch, int max_seq_len,
+                                        int batch, int num_splits, int* error_bits,
+                                        void* stream) {
+  if (num_layers < 1 || num_pages < 1 || max_batch < 1 || max_seq_len < kPage ||
+      max_seq_len > kMaxSeqLen || max_seq_len % kPage != 0 || max_batch > 65535)
+    return PKV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= num_layers || batch < 0 || batch > max_batch)
+    return PKV_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > kStaticMaxSplits || batch > kStaticRows ||
+      static_cast<long long>(batch) * num_splits > kStaticRows)
+    return PKV_ERR_STATIC_LIMIT;
+  if (batch == 0) return PKV_OK;
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(block_tables) ||
+      !aligned16(seq_lens) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(error_bits) & 3u) != 0)
+    return PKV_ERR_INVALID_ARG;
+
+  StaticScratch* scratch = nullptr;
+  const pkv_status st = static_scratch_address(&scratch);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // tickets must start at zero; the array keeps whatever the last call left
+  if (cudaMemsetAsync(scratch->tickets, 0, static_cast<size_t>(batch) * kHkv * sizeof(int), s) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+
+  const int max_pages = max_seq_len / kPage;
+  DecodeParams prm;
+  prm.q = static_cast<const uint16_t*>(q);
+  prm.k_new = nullptr;
+  prm.v_new = nullptr;
+  prm.k_pool = const_cast<uint16_t*>(static_cast<const uint16_t*>(k_pool));
+  prm.v_pool = const_cast<uint16_t*>(static_cast<const uint16_t*>(v_pool));
+  prm.table = block_tables + static_cast<size_t>(layer) * max_batch * max_pages;
+  prm.seq_lens = seq_lens;
+  prm.out = out;
+  prm.part_o = &scratch->part_o[0][0];
+  prm.part_ml = scratch->part_ml;
+  prm.tickets = scratch->tickets;
+  prm.err = error_bits ? error_bits : &scratch->error_sink;
+  prm.num_pages = num_pages;
+  prm.table_stride = max_pages;
+  prm.max_seq_len = max_seq_len;
+  prm.max_splits = num_splits;     // partial rows are (sequence, head) x num_splits
+  prm.num_splits = num_splits;
+  prm.chunk_pages = 0;
+  ticket_kernel<false><<<dim3(num_splits, kHkv, batch), block_threads(false), smem_bytes(false),
+                         s>>>(prm);
+  return check_launch();
+}
 
 const char* pkv_status_string(pkv_status status) {
   switch (status) {
@@ -951,6 +1042,7 @@ const char* pkv_status_string(pkv_status status) {
     case PKV_ERR_CUDA: return "CUDA runtime error";
     case PKV_ERR_UNSUPPORTED: return "unsupported geometry";
     case PKV_ERR_DEVICE_TIMEOUT: return "bounded device wait timed out";
+    case PKV_ERR_STATIC_LIMIT: return "request exceeds the no-allocation entry point's scratch";
   }
   return "unknown status";
 }
