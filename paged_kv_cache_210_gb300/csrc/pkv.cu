@@ -89,12 +89,14 @@ struct MergeSmem {
   float l[kGroup];
 };
 
-// The cluster leader's inbox: every block of the cluster stores its (m, l, o)
-// for the 4 heads here (placed after BlockSmem, cluster kernels only).
+// A head leader's inbox (placed after BlockSmem, cluster kernels only): every
+// warp of the cluster stores its (m, l, o) for the heads this block leads.
+// Slot of warp w of block r for head g: (g / S) * (S * warps) + r * warps + w.
+constexpr int kInboxSlots = kMaxClusterSize * 4;   // cluster blocks x warps per block
 struct ClusterInbox {
-  float o[kMaxClusterSize][kGroup][kDim];
-  float m[kMaxClusterSize][kGroup];
-  float l[kMaxClusterSize][kGroup];
+  float o[kInboxSlots][kDim];
+  float m[kInboxSlots];
+  float l[kInboxSlots];
 };
 
 template <int kWarps, int kStages>
@@ -157,14 +159,18 @@ __device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One try_wait on an mbarrier phase. The thread may sleep inside it until the
+// phase completes, for at most the hint (10 ms), so a waiting warp takes no
+// issue slots from the warps that compute.
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+  constexpr uint32_t kSuspendHintNs = 10000000;
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return done != 0;
 }
@@ -200,10 +206,11 @@ __device__ __forceinline__ void st_cluster(float* p, uint32_t rank, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-__device__ __forceinline__ void st_cluster2(float* p, uint32_t rank, float2 v) {
+__device__ __forceinline__ void st_cluster4(float* p, uint32_t rank, float4 v) {
   uint32_t addr;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(p)), "r"(rank));
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
                : "memory");
 }
 
@@ -241,6 +248,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // BF16 pair (low half = element 0) -> two FP32 values, exact.
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// 2^x by the SFU's approximate exponential (PTX ex2.approx.ftz.f32: relative
+// error about 2^-22; results below 2^-126, i.e. softmax weights that cannot
+// contribute, flush to zero; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -347,9 +363,8 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
 
   // Copy engine: rows of this warp's i-th page into stage i % kStages (lane 0
   // issues). In the fused step the appended row is not copied from the pool.
-  auto issue_copy = [&](int i, int phys) {
+  auto issue_copy = [&](int i, int stage, int phys) {
     if (lane != 0) return;
-    const int stage = i % kStages;
     const int lp = page_begin + warp + kWarps * i;
     const bool ok = phys >= 0 && phys < prm.num_pages;
     int rows = lp == last_page ? len - lp * kPage : kPage;
@@ -367,11 +382,10 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
   };
   // Fused step: lanes 0..15 write the appended token's K/V row to the pool and
   // to the stage tile (only after the wait: k/v may come from the previous kernel).
-  auto place_new_row = [&](int i, int phys) {
+  auto place_new_row = [&](int i, int stage, int phys) {
     const int lp = page_begin + warp + kWarps * i;
     if (!kFused || lp != last_page || lane >= 16) return;
     if (phys < 0 || phys >= prm.num_pages) return;
-    const int stage = i % kStages;
     const bool is_v = lane >= 8;
     const int c = lane & 7;
     const uint16_t* src = (is_v ? prm.v_new : prm.k_new) +
@@ -393,7 +407,7 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
     if (!kFused && page_begin + warp + kWarps * i == last_page) {
       deferred = i;
     } else {
-      issue_copy(i, phys);
+      issue_copy(i, i, phys);
     }
   }
   // q of the 4 heads (512 B) and, fused, the new k/v rows into L2 ahead of the wait
@@ -408,8 +422,8 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
   }
   pdl_launch_dependents();
   pdl_wait();
-  if (deferred >= 0) issue_copy(deferred, __shfl_sync(0xffffffffu, my_phys, deferred));
-  for (int i = 0; i < n_prefetch; ++i) place_new_row(i, __shfl_sync(0xffffffffu, my_phys, i));
+  if (deferred >= 0) issue_copy(deferred, deferred, __shfl_sync(0xffffffffu, my_phys, deferred));
+  for (int i = 0; i < n_prefetch; ++i) place_new_row(i, i, __shfl_sync(0xffffffffu, my_phys, i));
   int issued = n_prefetch;
   __syncwarp();   // the appended row written by lanes 0..15 is read by every lane
 
@@ -452,13 +466,14 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
 
   bool timed_out = false;
   int consumed = 0;
+  int stage = 0;            // i % kStages
+  uint32_t phase = 0;       // (i / kStages) & 1
   for (int i = 0; i < mine; ++i) {
-    const int stage = i % kStages;
     const int lp = page_begin + warp + kWarps * i;
     const int valid = lp == last_page ? len - lp * kPage : kPage;   // tokens in this page
     const int phys = __shfl_sync(0xffffffffu, my_phys, i);
     const bool ok = phys >= 0 && phys < prm.num_pages;
-    if (!mbar_wait(&ws.bar[stage], (i / kStages) & 1)) {
+    if (!mbar_wait(&ws.bar[stage], phase)) {
       timed_out = true;
       break;
     }
@@ -518,9 +533,9 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
     const float m_new = fmaxf(m_run, pm);
     const float m_use = m_new == -INFINITY ? 0.f : m_new;
-    const float alpha = exp2f(m_run - m_use);
-    const float p0 = exp2f(sc[0] - m_use);
-    const float p1 = exp2f(sc[1] - m_use);
+    const float alpha = fast_exp2(m_run - m_use);
+    const float p0 = fast_exp2(sc[0] - m_use);
+    const float p1 = fast_exp2(sc[1] - m_use);
     l_run = l_run * alpha + p0 + p1;
     m_run = m_new;
     ws.p[tp][gh] = make_float2(p0, p0);
@@ -566,10 +581,14 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
     __syncwarp();
     if (i + kStages < mine) {
       const int next_phys = __shfl_sync(0xffffffffu, my_phys, i + kStages);
-      issue_copy(i + kStages, next_phys);
-      place_new_row(i + kStages, next_phys);
+      issue_copy(i + kStages, stage, next_phys);
+      place_new_row(i + kStages, stage, next_phys);
       __syncwarp();
       issued = i + kStages + 1;
+    }
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
     }
   }
   if (timed_out) {
@@ -595,6 +614,80 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
     m_run = -INFINITY;
     l_run = 0.f;
   }
+  if constexpr (kCluster) {
+    if (n_splits > 1) {
+      // ---- cluster merge: each warp stores its (m, l, o) for head g straight
+      // into the inbox of the head's leader, block g mod S of the cluster;
+      // every thread arrives on the cluster barrier, blocks that lead no head
+      // exit, and each leader waits for all arrivals and combines its heads.
+      static_assert(kWarps * kMaxClusterSize <= kInboxSlots, "inbox slots");
+      ClusterInbox& inbox = *reinterpret_cast<ClusterInbox*>(smem_raw + sizeof(Smem));
+      const int S = gridDim.x;
+      const int rank = static_cast<int>(cluster_rank());
+      const int slot = rank * kWarps + warp;
+      if (tp == 0) {
+        const int at = (gh / S) * (S * kWarps) + slot;
+        st_cluster(&inbox.m[at], gh % S, m_run);
+        st_cluster(&inbox.l[at], gh % S, l_run);
+      }
+      if (tpar == 0) {
+        #pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+          const int at = (g / S) * (S * kWarps) + slot;
+          st_cluster4(&inbox.o[at][4 * dq], g % S,
+                      make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y));
+        }
+      }
+      cluster_arrive_release();
+      if (rank >= kGroup) return;   // leads no head
+      cluster_wait_acquire();
+      // combine: warp qq sums the slots p = qq, qq + 4, ... of a head for dims
+      // (d0, d0 + 1); the four warps' sums meet in shared memory
+      const int parts = S * kWarps;
+      const int qq = warp;
+      const int d0 = 2 * lane;
+      for (int hg = rank; hg < kGroup; hg += S) {
+        const int base = (hg / S) * parts;
+        float mx = -INFINITY;
+        for (int p = lane; p < parts; p += 32) mx = fmaxf(mx, inbox.m[base + p]);
+        #pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float LL = 0.f;
+        float2 OO = make_float2(0.f, 0.f);
+        #pragma unroll 4
+        for (int p = qq; p < parts; p += kWarps) {
+          const float mp = inbox.m[base + p];
+          const float w = mp == -INFINITY ? 0.f : fast_exp2(mp - mx);
+          const float2 op = *reinterpret_cast<const float2*>(&inbox.o[base + p][d0]);
+          LL += w * inbox.l[base + p];
+          OO.x += w * op.x;
+          OO.y += w * op.y;
+        }
+        sm.acc[qq][0][d0] = OO.x;
+        sm.acc[qq][0][d0 + 1] = OO.y;
+        if (lane == 0) sm.l[qq][0] = LL;
+        __syncthreads();
+        if (qq == 0) {
+          float L4 = 0.f, ox = 0.f, oy = 0.f;
+          #pragma unroll
+          for (int w = 0; w < kWarps; ++w) {
+            L4 += sm.l[w][0];
+            ox += sm.acc[w][0][d0];
+            oy += sm.acc[w][0][d0 + 1];
+          }
+          const float inv = L4 > 0.f ? 1.f / L4 : 0.f;
+          *reinterpret_cast<float2*>(
+              prm.out + (static_cast<size_t>(b) * kHq + kvh * kGroup + hg) * kDim + d0) =
+              make_float2(ox * inv, oy * inv);
+        }
+        __syncthreads();
+      }
+      return;
+    }
+  }
+
+  // ---- block merge (every ticket-mode block; a cluster whose sequence has
+  // a single split)
   if (tp == 0) {
     sm.m[warp][gh] = m_run;
     sm.l[warp][gh] = l_run;
@@ -622,7 +715,7 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
   for (int w = 0; w < kWarps; ++w) {
     const float mw = sm.m[w][g];
     if (mw == -INFINITY) continue;
-    const float f = exp2f(mw - M);
+    const float f = fast_exp2(mw - M);
     L += f * sm.l[w][g];
     O.x += f * sm.acc[w][g][d0];
     O.y += f * sm.acc[w][g][d0 + 1];
@@ -636,53 +729,7 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
     return;
   }
 
-  if constexpr (kCluster) {
-    // ---- cluster merge: every block stores its (m, l, o) into the inbox of
-    // block 0 of the cluster (remote shared-memory stores), arrives on the
-    // cluster barrier and exits; block 0 waits for all arrivals and combines.
-    ClusterInbox& inbox = *reinterpret_cast<ClusterInbox*>(smem_raw + sizeof(Smem));
-    const uint32_t rank = cluster_rank();
-    if (merger) {
-      st_cluster2(&inbox.o[rank][g][d0], 0, O);
-      if (d0 == 0) {
-        st_cluster(&inbox.m[rank][g], 0, M);
-        st_cluster(&inbox.l[rank][g], 0, L);
-      }
-    }
-    cluster_arrive_release();
-    if (rank != 0 || !merger) return;
-    cluster_wait_acquire();
-    const int S = gridDim.x;
-    float mj[kMaxClusterSize], lj[kMaxClusterSize];
-    float2 oj[kMaxClusterSize];
-    #pragma unroll
-    for (int j = 0; j < kMaxClusterSize; ++j) {
-      if (j < S) {
-        mj[j] = inbox.m[j][g];
-        lj[j] = inbox.l[j][g];
-        oj[j] = *reinterpret_cast<const float2*>(&inbox.o[j][g][d0]);
-      } else {
-        mj[j] = -INFINITY;
-        lj[j] = 0.f;
-        oj[j] = make_float2(0.f, 0.f);
-      }
-    }
-    float mx = -INFINITY;
-    #pragma unroll
-    for (int j = 0; j < kMaxClusterSize; ++j) mx = fmaxf(mx, mj[j]);
-    float LL = 0.f;
-    float2 OO = make_float2(0.f, 0.f);
-    #pragma unroll
-    for (int j = 0; j < kMaxClusterSize; ++j) {
-      const float w = mj[j] == -INFINITY ? 0.f : exp2f(mj[j] - mx);
-      LL += w * lj[j];
-      OO.x += w * oj[j].x;
-      OO.y += w * oj[j].y;
-    }
-    const float inv = LL > 0.f ? 1.f / LL : 0.f;
-    *reinterpret_cast<float2*>(prm.out + out_row + d0) = make_float2(OO.x * inv, OO.y * inv);
-    return;
-  } else {
+  if constexpr (!kCluster) {
   static_assert(kWarps == kGroup, "the ticket merge maps one warp to each head");
   // ---- split partial, ticket, and the last block's log-sum-exp merge
   const size_t head0 = (static_cast<size_t>(b) * kHq + kvh * kGroup) * prm.max_splits;
@@ -720,7 +767,7 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
     float sum = 0.f;
     for (int s = lane; s < n_splits; s += 32) {
       const float2 ml = mg.ml[hg][s];
-      const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mx);
+      const float w = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mx);
       mg.w[hg][s] = w;
       sum += w * ml.y;
     }
