@@ -82,13 +82,6 @@ struct alignas(16) WarpSmem {
   unsigned long long bar[kStages];
 };
 
-// scratch of the last block's split merge (the page rings are idle by then)
-struct MergeSmem {
-  float2 ml[kGroup][kMaxSplitsLimit];
-  float w[kGroup][kMaxSplitsLimit];
-  float l[kGroup];
-};
-
 // A head leader's inbox (placed after BlockSmem, cluster kernels only): every
 // warp of the cluster stores its (m, l, o) for the heads this block leads.
 // Slot of warp w of block r for head g: (g / S) * (S * warps) + r * warps + w.
@@ -101,10 +94,7 @@ struct ClusterInbox {
 
 template <int kWarps, int kStages>
 struct alignas(16) BlockSmem {
-  union {
-    WarpSmem<kStages> warp[kWarps];
-    MergeSmem merge;
-  };
+  WarpSmem<kStages> warp[kWarps];
   float m[kWarps][kGroup];
   float l[kWarps][kGroup];
   float acc[kWarps][kGroup][kDim];
@@ -137,6 +127,7 @@ struct DecodeParams {
   int max_splits;
   int num_splits;             // > 0: S ranges per sequence
   int chunk_pages;            // > 0: ranges of this many pages (used when num_splits == 0)
+  int early_trigger;          // let the next launch start right after the prefetch (one wave)
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -420,7 +411,11 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
     }
     if (line) prefetch_l2(line);
   }
-  pdl_launch_dependents();
+  // A launch that fits in one wave of resident blocks lets the next launch
+  // start now, so its blocks prefetch while this one computes; a larger
+  // launch triggers after its page loop, so waiting blocks of the next
+  // launch do not take slots this launch's later blocks need.
+  if (prm.early_trigger) pdl_launch_dependents();
   pdl_wait();
   if (deferred >= 0) issue_copy(deferred, deferred, __shfl_sync(0xffffffffu, my_phys, deferred));
   for (int i = 0; i < n_prefetch; ++i) place_new_row(i, i, __shfl_sync(0xffffffffu, my_phys, i));
@@ -597,6 +592,8 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
     for (int j = consumed; j < issued; ++j) mbar_wait(&ws.bar[j % kStages], (j / kStages) & 1);
   }
 
+  if (!prm.early_trigger) pdl_launch_dependents();
+
   // ---- warp state -> shared memory
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 4);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 8);
@@ -736,82 +733,82 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
   const size_t prow = head0 + static_cast<size_t>(g) * prm.max_splits;
   *reinterpret_cast<float2*>(prm.part_o + (prow + split) * kDim + d0) = O;
   if (d0 == 0) prm.part_ml[prow + split] = make_float2(M, L);
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    // One acquire-release atomic after the barrier: its release publishes the
+    // partials every thread of this block wrote; for the last block its
+    // acquire makes the other blocks' partials visible (the barrier below
+    // passes that on to the block's other threads).
     int* ticket = prm.tickets + static_cast<size_t>(b) * kHkv + kvh;
-    const int arrived = atomicAdd(ticket, 1);
+    int arrived;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                 : "=r"(arrived)
+                 : "l"(ticket)
+                 : "memory");
     const int last = arrived == n_splits - 1;
     if (last) *ticket = 0;   // every split has arrived: reset for the next launch
     sm.last = last;
   }
   __syncthreads();
   if (!sm.last) return;
-  __threadfence();
 
-  // (m, l) of every split and head into shared memory (one parallel pass)
-  MergeSmem& mg = sm.merge;   // aliases the page rings: every copy has landed
-  for (int idx = threadIdx.x; idx < kGroup * n_splits; idx += kThreads) {
-    const int hg = idx / n_splits;
-    const int s = idx - hg * n_splits;
-    mg.ml[hg][s] = __ldcg(&prm.part_ml[head0 + static_cast<size_t>(hg) * prm.max_splits + s]);
-  }
-  __syncthreads();
-  // warp hg: global max, split weights and their sum for head hg
-  {
-    const int hg = warp;
-    float mx = -INFINITY;
-    for (int s = lane; s < n_splits; s += 32) mx = fmaxf(mx, mg.ml[hg][s].x);
-    #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float sum = 0.f;
-    for (int s = lane; s < n_splits; s += 32) {
-      const float2 ml = mg.ml[hg][s];
-      const float w = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mx);
-      mg.w[hg][s] = w;
-      sum += w * ml.y;
-    }
-    #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) mg.l[hg] = sum;
-  }
-  __syncthreads();
-  // warp hg, lane: dims 4 quad .. 4 quad + 3 over the splits of one parity
+  // Warp hg merges head hg; lane (quad, half) owns dims 4 quad .. 4 quad + 3
+  // over the splits s = half, half + 2, ...: an online log-sum-exp merge of
+  // (m_s, l_s, o_s) loaded straight from L2 (bypassing L1, which may hold
+  // lines of an earlier launch), then the two halves combine by shuffle.
   {
     const int hg = warp;
     const int quad = lane & 15;
     const int half = lane >> 4;
-    const float* base = prm.part_o + (head0 + static_cast<size_t>(hg) * prm.max_splits) * kDim +
-                        4 * quad;
+    const size_t hrow = head0 + static_cast<size_t>(hg) * prm.max_splits;
+    float mrun = -INFINITY, lrun = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = half; s0 < n_splits; s0 += 16) {
+      float2 ml[8];
       float4 v[8];
       #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int s = s0 + 2 * j;
-        v[j] = s < n_splits ? __ldcg(reinterpret_cast<const float4*>(base + s * kDim))
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        ml[j] = s < n_splits ? __ldcg(&prm.part_ml[hrow + s]) : make_float2(-INFINITY, 0.f);
+        v[j] = s < n_splits
+                   ? __ldcg(reinterpret_cast<const float4*>(prm.part_o + (hrow + s) * kDim + 4 * quad))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      float mnew = mrun;
+      #pragma unroll
+      for (int j = 0; j < 8; ++j) mnew = fmaxf(mnew, ml[j].x);
+      if (mnew == -INFINITY) continue;
+      const float a = fast_exp2(mrun - mnew);   // 0 while nothing was merged
+      lrun *= a;
+      o = make_float4(o.x * a, o.y * a, o.z * a, o.w * a);
       #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int s = s0 + 2 * j;
-        const float w = s < n_splits ? mg.w[hg][s] : 0.f;
+        const float w = fast_exp2(ml[j].x - mnew);   // 0 for an absent split
+        lrun += w * ml[j].y;
         o.x += w * v[j].x;
         o.y += w * v[j].y;
         o.z += w * v[j].z;
         o.w += w * v[j].w;
       }
+      mrun = mnew;
     }
-    o.x += __shfl_xor_sync(0xffffffffu, o.x, 16);
-    o.y += __shfl_xor_sync(0xffffffffu, o.y, 16);
-    o.z += __shfl_xor_sync(0xffffffffu, o.z, 16);
-    o.w += __shfl_xor_sync(0xffffffffu, o.w, 16);
+    // combine with the other half (lane ^ 16)
+    const float mo = __shfl_xor_sync(0xffffffffu, mrun, 16);
+    const float lo = __shfl_xor_sync(0xffffffffu, lrun, 16);
+    const float4 oo = make_float4(__shfl_xor_sync(0xffffffffu, o.x, 16),
+                                  __shfl_xor_sync(0xffffffffu, o.y, 16),
+                                  __shfl_xor_sync(0xffffffffu, o.z, 16),
+                                  __shfl_xor_sync(0xffffffffu, o.w, 16));
+    const float mx = fmaxf(mrun, mo);
+    const float wa = mrun == -INFINITY ? 0.f : fast_exp2(mrun - mx);
+    const float wb = mo == -INFINITY ? 0.f : fast_exp2(mo - mx);
+    const float LL = wa * lrun + wb * lo;
     if (half == 0) {
-      const float LL = mg.l[hg];
       const float inv = LL > 0.f ? 1.f / LL : 0.f;
       *reinterpret_cast<float4*>(prm.out + (static_cast<size_t>(b) * kHq + kvh * kGroup + hg) *
                                                kDim + 4 * quad) =
-          make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+          make_float4((wa * o.x + wb * oo.x) * inv, (wa * o.y + wb * oo.y) * inv,
+                      (wa * o.z + wb * oo.z) * inv, (wa * o.w + wb * oo.w) * inv);
     }
   }
   }  // ticket merge
@@ -868,21 +865,27 @@ pkv_status check_launch() {
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-// Pages per split when the caller leaves the choice to the library: the
-// fewest pages per block (at least one per warp) for which a batch of
-// full-length sequences still fits in one wave of resident blocks; past 16
-// pages a block's range would make long sequences the tail, so large
-// batches take 16 and run several waves.
+// Pages per block when the caller leaves the choice to the library and the
+// batch is too large for a cluster split: the largest of 128, 64, 32, 16
+// pages for which a batch of full-length sequences still yields at least
+// three (sequence, kv head, range) blocks per resident block slot. Fewer
+// blocks per slot leave SMs idle behind the longest sequences; more, smaller
+// ranges pay a partial merge for nothing (measured: 256 sequences run best
+// unsplit, 64 log-uniform ones with 32-page ranges).
 int auto_chunk_pages(const pkv_pool* pool, int batch) {
   const int max_pages = pool->cfg.max_seq_len / kPage;
   const int min_chunk = (max_pages + pool->cfg.max_splits - 1) / pool->cfg.max_splits;
   const long long resident = static_cast<long long>(pool->blocks_per_sm) * pool->num_sms;
-  for (int chunk = kTicketWarps > min_chunk ? kTicketWarps : min_chunk; chunk < 16; ++chunk) {
-    const long long blocks =
-        static_cast<long long>(batch) * kHkv * ((max_pages + chunk - 1) / chunk);
-    if (blocks <= resident) return chunk;
+  int chunk = 16;
+  for (int c = 128; c >= 16; c /= 2) {
+    const long long blocks = static_cast<long long>(batch) * kHkv * ((max_pages + c - 1) / c);
+    if (blocks >= 3 * resident) {
+      chunk = c;
+      break;
+    }
   }
-  return 16 > min_chunk ? 16 : min_chunk;
+  if (chunk > max_pages) chunk = max_pages;
+  return chunk < min_chunk ? min_chunk : chunk;
 }
 
 // Splits per sequence for a cluster merge when the library chooses: the
@@ -960,6 +963,11 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   }
   const int grid_splits = prm.num_splits > 0 ? prm.num_splits
                                              : (max_pages + prm.chunk_pages - 1) / prm.chunk_pages;
+  const long long blocks = static_cast<long long>(grid_splits) * kHkv * batch;
+  const long long resident =
+      static_cast<long long>(cluster ? pool->cluster_blocks_per_sm : pool->blocks_per_sm) *
+      pool->num_sms;
+  prm.early_trigger = blocks <= resident ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid_splits, kHkv, batch);
@@ -1076,6 +1084,7 @@ pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_
   prm.max_splits = num_splits;     // partial rows are (sequence, head) x num_splits
   prm.num_splits = num_splits;
   prm.chunk_pages = 0;
+  prm.early_trigger = 1;   // launched without programmatic dependent launch: no effect
   ticket_kernel<false><<<dim3(num_splits, kHkv, batch), block_threads(false), smem_bytes(false),
                          s>>>(prm);
   return check_launch();
