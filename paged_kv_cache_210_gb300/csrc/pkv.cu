@@ -291,6 +291,184 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t* __restrict_
   *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
 }
 
+// ---------------------------------------------------------------- page computation
+// Lane roles, fixed per lane. QK: a lane owns tokens tp and tp + 8 and the
+// 16-byte dim chunks qd and qd + 4 (read in a row-parity-dependent order so
+// the shared loads are bank-conflict-free); after the reduce-scatter it owns
+// head gh. PV: a lane owns dims 4 dq .. 4 dq + 3 of the tokens 2 i + tpar.
+struct LaneRoles {
+  int tp, qd, cA, cB, gh, dq, tpar;
+  __device__ explicit LaneRoles(int lane) {
+    tp = lane >> 2;
+    qd = lane & 3;
+    const int par = tp & 1;
+    cA = qd + 4 * par;
+    cB = qd + 4 * (1 - par);
+    gh = 2 * (qd & 1) + ((qd >> 1) & 1);
+    dq = lane & 15;
+    tpar = lane >> 4;
+  }
+};
+
+// Online-softmax state of one warp for the 4 heads of a kv head.
+struct WarpState {
+  float m_run;              // running max (base 2) of head gh
+  float l_run;              // this lane's share of the running sum of head gh
+  float2 acc[kGroup][2];    // PV accumulators: dims (4dq, 4dq+1), (4dq+2, 4dq+3)
+  __device__ void reset() {
+    m_run = -INFINITY;
+    l_run = 0.f;
+    #pragma unroll
+    for (int g = 0; g < kGroup; ++g) acc[g][0] = acc[g][1] = make_float2(0.f, 0.f);
+  }
+};
+
+// q of the 4 heads at qrow ([4][64] BF16) for this lane's chunks, scaled by
+// log2(e) / sqrt(64) so that scores come out in base 2.
+__device__ __forceinline__ void load_q(const uint16_t* qrow, const LaneRoles& r,
+                                       float2 (&qa)[kGroup][4], float2 (&qb)[kGroup][4],
+                                       bool from_shared) {
+  const float qscale = 1.4426950408889634f * 0.125f;
+  #pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+    const uint4* pa = reinterpret_cast<const uint4*>(qrow + g * kDim + r.cA * 8);
+    const uint4* pb = reinterpret_cast<const uint4*>(qrow + g * kDim + r.cB * 8);
+    const uint4 ra = from_shared ? *pa : __ldg(pa);
+    const uint4 rb = from_shared ? *pb : __ldg(pb);
+    const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
+    const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 fa = bf16x2_to_float2(wa[j]);
+      const float2 fb = bf16x2_to_float2(wb[j]);
+      qa[g][j] = make_float2(fa.x * qscale, fa.y * qscale);
+      qb[g][j] = make_float2(fb.x * qscale, fb.y * qscale);
+    }
+  }
+}
+
+// One page: K tile kt and V tile vt in shared memory, `live` valid tokens
+// (the rest are masked by select, so stale data never leaks). p and alpha
+// are the warp's shared slots for the probabilities and the rescale factors.
+__device__ __forceinline__ void attend_page(const uint8_t* kt, const uint8_t* vt, int live,
+                                            const float2 (&qa)[kGroup][4],
+                                            const float2 (&qb)[kGroup][4],
+                                            float2 (*p)[kGroup], float2* alpha_s,
+                                            const LaneRoles& r, WarpState& st) {
+  // scores for tokens tp and tp + 8, all 4 heads, this lane's 16 dims
+  float s[kGroup][2];
+  #pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint8_t* krow = kt + (r.tp + 8 * j) * kRowBytes;
+    const uint4 ka = *reinterpret_cast<const uint4*>(krow + r.cA * 16);
+    const uint4 kb = *reinterpret_cast<const uint4*>(krow + r.cB * 16);
+    const float2 fa[4] = {bf16x2_to_float2(ka.x), bf16x2_to_float2(ka.y),
+                          bf16x2_to_float2(ka.z), bf16x2_to_float2(ka.w)};
+    const float2 fb[4] = {bf16x2_to_float2(kb.x), bf16x2_to_float2(kb.y),
+                          bf16x2_to_float2(kb.z), bf16x2_to_float2(kb.w)};
+    #pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      float2 d = make_float2(0.f, 0.f);
+      #pragma unroll
+      for (int c = 0; c < 4; ++c) d = ffma2(qa[g][c], fa[c], d);
+      #pragma unroll
+      for (int c = 0; c < 4; ++c) d = ffma2(qb[g][c], fb[c], d);
+      s[g][j] = d.x + d.y;
+    }
+  }
+  // reduce-scatter over the 4 lanes of a token pair: the lane keeps head gh
+  float sc[2];
+  {
+    const bool hi1 = r.qd & 1;
+    const bool hi2 = r.qd & 2;
+    #pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float send0 = hi1 ? s[0][j] : s[2][j];
+      const float send1 = hi1 ? s[1][j] : s[3][j];
+      float keep0 = hi1 ? s[2][j] : s[0][j];
+      float keep1 = hi1 ? s[3][j] : s[1][j];
+      keep0 += __shfl_xor_sync(0xffffffffu, send0, 1);
+      keep1 += __shfl_xor_sync(0xffffffffu, send1, 1);
+      const float send = hi2 ? keep0 : keep1;
+      float kept = hi2 ? keep1 : keep0;
+      kept += __shfl_xor_sync(0xffffffffu, send, 2);
+      sc[j] = kept;
+    }
+  }
+  sc[0] = r.tp < live ? sc[0] : -INFINITY;
+  sc[1] = r.tp + 8 < live ? sc[1] : -INFINITY;
+
+  // online softmax, base 2, per head over the page's 16 tokens
+  float pm = fmaxf(sc[0], sc[1]);
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+  const float m_new = fmaxf(st.m_run, pm);
+  const float m_use = m_new == -INFINITY ? 0.f : m_new;
+  const float alpha = fast_exp2(st.m_run - m_use);
+  const float p0 = fast_exp2(sc[0] - m_use);
+  const float p1 = fast_exp2(sc[1] - m_use);
+  st.l_run = st.l_run * alpha + p0 + p1;
+  st.m_run = m_new;
+  p[r.tp][r.gh] = make_float2(p0, p0);
+  p[r.tp + 8][r.gh] = make_float2(p1, p1);
+  if (r.tp == 0) alpha_s[r.gh] = make_float2(alpha, alpha);
+  __syncwarp();
+
+  // PV: rescale, then accumulate this lane's tokens
+  {
+    const float4 a01 = *reinterpret_cast<const float4*>(&alpha_s[0]);
+    const float4 a23 = *reinterpret_cast<const float4*>(&alpha_s[2]);
+    const float2 al[kGroup] = {make_float2(a01.x, a01.y), make_float2(a01.z, a01.w),
+                               make_float2(a23.x, a23.y), make_float2(a23.z, a23.w)};
+    #pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      st.acc[g][0] = fmul2(st.acc[g][0], al[g]);
+      st.acc[g][1] = fmul2(st.acc[g][1], al[g]);
+    }
+  }
+  auto pv_token = [&](int t) {
+    const uint2 vv = *reinterpret_cast<const uint2*>(vt + t * kRowBytes + r.dq * 8);
+    const float2 v01 = bf16x2_to_float2(vv.x);
+    const float2 v23 = bf16x2_to_float2(vv.y);
+    const float4 pa = *reinterpret_cast<const float4*>(&p[t][0]);
+    const float4 pb = *reinterpret_cast<const float4*>(&p[t][2]);
+    const float2 pg[kGroup] = {make_float2(pa.x, pa.y), make_float2(pa.z, pa.w),
+                               make_float2(pb.x, pb.y), make_float2(pb.z, pb.w)};
+    #pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      st.acc[g][0] = ffma2(pg[g], v01, st.acc[g][0]);
+      st.acc[g][1] = ffma2(pg[g], v23, st.acc[g][1]);
+    }
+  };
+  if (live == kPage) {
+    #pragma unroll
+    for (int t2 = 0; t2 < kPage / 2; ++t2) pv_token(2 * t2 + r.tpar);
+  } else {
+    #pragma unroll
+    for (int t2 = 0; t2 < kPage / 2; ++t2) {
+      if (2 * t2 + r.tpar < live) pv_token(2 * t2 + r.tpar);
+    }
+  }
+  __syncwarp();
+}
+
+// End of a warp's pages: the running sum over the 8 token-pair lanes of each
+// head, the accumulators over the two token-parity halves.
+__device__ __forceinline__ void reduce_warp_state(WarpState& st) {
+  st.l_run += __shfl_xor_sync(0xffffffffu, st.l_run, 4);
+  st.l_run += __shfl_xor_sync(0xffffffffu, st.l_run, 8);
+  st.l_run += __shfl_xor_sync(0xffffffffu, st.l_run, 16);
+  #pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+    #pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      st.acc[g][h].x += __shfl_xor_sync(0xffffffffu, st.acc[g][h].x, 16);
+      st.acc[g][h].y += __shfl_xor_sync(0xffffffffu, st.acc[g][h].y, 16);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- decode
 // kCluster: the splits of one (sequence, kv head) form one thread-block
 // cluster (gridDim.x == cluster size) and merge through distributed shared
@@ -422,42 +600,13 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
   int issued = n_prefetch;
   __syncwarp();   // the appended row written by lanes 0..15 is read by every lane
 
-  // ---- lane roles
-  const int tp = lane >> 2;            // QK: tokens tp and tp + 8
-  const int qd = lane & 3;             // QK: 16-byte chunks qd and qd + 4
-  const int par = tp & 1;
-  const int cA = qd + 4 * par;         // chunk read first (bank-conflict-free order)
-  const int cB = qd + 4 * (1 - par);
-  const int gh = 2 * (qd & 1) + ((qd >> 1) & 1);   // head owned after reduce-scatter
-  const int dq = lane & 15;            // PV: dims 4 dq .. 4 dq + 3
-  const int tpar = lane >> 4;          // PV: tokens 2 i + tpar
-
-  // q of the 4 heads for this lane's chunks, scaled by log2(e) / sqrt(64)
-  const float qscale = 1.4426950408889634f * 0.125f;
+  const LaneRoles rl(lane);
+  const int tp = rl.tp, gh = rl.gh, dq = rl.dq, tpar = rl.tpar;
   float2 qa[kGroup][4], qb[kGroup][4];
-  {
-    const uint16_t* qrow = prm.q + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim;
-    #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-      const uint4 ra = __ldg(reinterpret_cast<const uint4*>(qrow + g * kDim + cA * 8));
-      const uint4 rb = __ldg(reinterpret_cast<const uint4*>(qrow + g * kDim + cB * 8));
-      const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
-      const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
-      #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 fa = bf16x2_to_float2(wa[j]);
-        const float2 fb = bf16x2_to_float2(wb[j]);
-        qa[g][j] = make_float2(fa.x * qscale, fa.y * qscale);
-        qb[g][j] = make_float2(fb.x * qscale, fb.y * qscale);
-      }
-    }
-  }
+  load_q(prm.q + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim, rl, qa, qb, false);
 
-  float m_run = -INFINITY;   // running max (base 2) of head gh
-  float l_run = 0.f;         // this lane's share of the running sum of head gh
-  float2 acc[kGroup][2];     // PV accumulators: dims (4dq, 4dq+1), (4dq+2, 4dq+3)
-  #pragma unroll
-  for (int g = 0; g < kGroup; ++g) acc[g][0] = acc[g][1] = make_float2(0.f, 0.f);
+  WarpState st;
+  st.reset();
 
   bool timed_out = false;
   int consumed = 0;
@@ -473,107 +622,7 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
       break;
     }
     consumed = i + 1;
-    const int live = ok ? valid : 0;
-    const uint8_t* kt = ws.k[stage];
-    const uint8_t* vt = ws.v[stage];
-
-    // ---- scores for tokens tp and tp + 8, all 4 heads, this lane's 16 dims
-    float s[kGroup][2];
-    #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const uint8_t* krow = kt + (tp + 8 * j) * kRowBytes;
-      const uint4 ka = *reinterpret_cast<const uint4*>(krow + cA * 16);
-      const uint4 kb = *reinterpret_cast<const uint4*>(krow + cB * 16);
-      const float2 fa[4] = {bf16x2_to_float2(ka.x), bf16x2_to_float2(ka.y),
-                            bf16x2_to_float2(ka.z), bf16x2_to_float2(ka.w)};
-      const float2 fb[4] = {bf16x2_to_float2(kb.x), bf16x2_to_float2(kb.y),
-                            bf16x2_to_float2(kb.z), bf16x2_to_float2(kb.w)};
-      #pragma unroll
-      for (int g = 0; g < kGroup; ++g) {
-        float2 d = make_float2(0.f, 0.f);
-        #pragma unroll
-        for (int c = 0; c < 4; ++c) d = ffma2(qa[g][c], fa[c], d);
-        #pragma unroll
-        for (int c = 0; c < 4; ++c) d = ffma2(qb[g][c], fb[c], d);
-        s[g][j] = d.x + d.y;
-      }
-    }
-    // ---- reduce-scatter over the 4 lanes of a token pair: lane keeps head gh
-    float sc[2];
-    {
-      const bool hi1 = qd & 1;
-      const bool hi2 = qd & 2;
-      #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float send0 = hi1 ? s[0][j] : s[2][j];
-        const float send1 = hi1 ? s[1][j] : s[3][j];
-        float keep0 = hi1 ? s[2][j] : s[0][j];
-        float keep1 = hi1 ? s[3][j] : s[1][j];
-        keep0 += __shfl_xor_sync(0xffffffffu, send0, 1);
-        keep1 += __shfl_xor_sync(0xffffffffu, send1, 1);
-        const float send = hi2 ? keep0 : keep1;
-        float kept = hi2 ? keep1 : keep0;
-        kept += __shfl_xor_sync(0xffffffffu, send, 2);
-        sc[j] = kept;
-      }
-    }
-    // mask tokens past the sequence end (select, so stale or NaN data never leaks)
-    sc[0] = tp < live ? sc[0] : -INFINITY;
-    sc[1] = tp + 8 < live ? sc[1] : -INFINITY;
-
-    // ---- online softmax, base 2, per head over the page's 16 tokens
-    float pm = fmaxf(sc[0], sc[1]);
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-    const float m_new = fmaxf(m_run, pm);
-    const float m_use = m_new == -INFINITY ? 0.f : m_new;
-    const float alpha = fast_exp2(m_run - m_use);
-    const float p0 = fast_exp2(sc[0] - m_use);
-    const float p1 = fast_exp2(sc[1] - m_use);
-    l_run = l_run * alpha + p0 + p1;
-    m_run = m_new;
-    ws.p[tp][gh] = make_float2(p0, p0);
-    ws.p[tp + 8][gh] = make_float2(p1, p1);
-    if (tp == 0) ws.alpha[gh] = make_float2(alpha, alpha);
-    __syncwarp();
-
-    // ---- PV: rescale, then accumulate this lane's tokens
-    {
-      const float4 a01 = *reinterpret_cast<const float4*>(&ws.alpha[0]);
-      const float4 a23 = *reinterpret_cast<const float4*>(&ws.alpha[2]);
-      const float2 al[kGroup] = {make_float2(a01.x, a01.y), make_float2(a01.z, a01.w),
-                                 make_float2(a23.x, a23.y), make_float2(a23.z, a23.w)};
-      #pragma unroll
-      for (int g = 0; g < kGroup; ++g) {
-        acc[g][0] = fmul2(acc[g][0], al[g]);
-        acc[g][1] = fmul2(acc[g][1], al[g]);
-      }
-    }
-    auto pv_token = [&](int r) {
-      const uint2 vv = *reinterpret_cast<const uint2*>(vt + r * kRowBytes + dq * 8);
-      const float2 v01 = bf16x2_to_float2(vv.x);
-      const float2 v23 = bf16x2_to_float2(vv.y);
-      const float4 pa = *reinterpret_cast<const float4*>(&ws.p[r][0]);
-      const float4 pb = *reinterpret_cast<const float4*>(&ws.p[r][2]);
-      const float2 pg[kGroup] = {make_float2(pa.x, pa.y), make_float2(pa.z, pa.w),
-                                 make_float2(pb.x, pb.y), make_float2(pb.z, pb.w)};
-      #pragma unroll
-      for (int g = 0; g < kGroup; ++g) {
-        acc[g][0] = ffma2(pg[g], v01, acc[g][0]);
-        acc[g][1] = ffma2(pg[g], v23, acc[g][1]);
-      }
-    };
-    if (live == kPage) {
-      #pragma unroll
-      for (int r2 = 0; r2 < kPage / 2; ++r2) pv_token(2 * r2 + tpar);
-    } else {
-      #pragma unroll
-      for (int r2 = 0; r2 < kPage / 2; ++r2) {
-        if (2 * r2 + tpar < live) pv_token(2 * r2 + tpar);
-      }
-    }
-    __syncwarp();
+    attend_page(ws.k[stage], ws.v[stage], ok ? valid : 0, qa, qb, ws.p, ws.alpha, rl, st);
     if (i + kStages < mine) {
       const int next_phys = __shfl_sync(0xffffffffu, my_phys, i + kStages);
       issue_copy(i + kStages, stage, next_phys);
@@ -594,23 +643,16 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const 
 
   if (!prm.early_trigger) pdl_launch_dependents();
 
-  // ---- warp state -> shared memory
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 4);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 8);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
-  #pragma unroll
-  for (int g = 0; g < kGroup; ++g) {
-    #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      acc[g][h].x += __shfl_xor_sync(0xffffffffu, acc[g][h].x, 16);
-      acc[g][h].y += __shfl_xor_sync(0xffffffffu, acc[g][h].y, 16);
-    }
-  }
+  // ---- warp state
+  reduce_warp_state(st);
   if (timed_out) {
     if (lane == 0) set_error(prm.err, kErrTimeout);
-    m_run = -INFINITY;
-    l_run = 0.f;
+    st.m_run = -INFINITY;
+    st.l_run = 0.f;
   }
+  const float m_run = st.m_run;
+  const float l_run = st.l_run;
+  const float2 (&acc)[kGroup][2] = st.acc;
   if constexpr (kCluster) {
     if (n_splits > 1) {
       // ---- cluster merge: each warp stores its (m, l, o) for head g straight
@@ -864,6 +906,7 @@ bool set_kernel_attributes(Kernel kernel, bool cluster) {
 pkv_status check_launch() {
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
+
 
 // Pages per block when the caller leaves the choice to the library and the
 // batch is too large for a cluster split: the largest of 128, 64, 32, 16
@@ -1130,6 +1173,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
   ok = ok && cudaMalloc(&pool->tickets, 2 * static_cast<size_t>(c.max_batch) * kHkv * sizeof(int)) ==
                  cudaSuccess;
   ok = ok && cudaMalloc(&pool->err, sizeof(int)) == cudaSuccess;
+
   ok = ok && cudaMemset(pool->tickets, 0, 2 * static_cast<size_t>(c.max_batch) * kHkv * sizeof(int)) ==
                  cudaSuccess;
   ok = ok && cudaMemset(pool->err, 0, sizeof(int)) == cudaSuccess;
@@ -1137,6 +1181,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
   ok = ok && set_kernel_attributes(ticket_kernel<true>, false);
   ok = ok && set_kernel_attributes(cluster_kernel<false>, true);
   ok = ok && set_kernel_attributes(cluster_kernel<true>, true);
+
   ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                   &pool->blocks_per_sm, ticket_kernel<true>, block_threads(false),
                   smem_bytes(false)) == cudaSuccess;
@@ -1164,6 +1209,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
   }
   if (ok && pool->blocks_per_sm < 1) pool->blocks_per_sm = 1;
   if (ok && pool->cluster_blocks_per_sm < 1) pool->cluster_blocks_per_sm = 1;
+
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     pkv_pool_destroy(pool);

@@ -155,6 +155,51 @@ def test_programmatic_dependent_launch_chain_matches_oracle(fused, graph):
         assert_close(out.cpu().numpy(), ref, f"pdl fused={fused} graph={graph} S={splits}")
 
 
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("pdl", [False, True])
+def test_many_sequences_chain_matches_oracle(fused, pdl):
+    """A batch too large for a cluster split (the library then picks page
+    ranges merged by ticket): 42 ragged sequences (every edge length three
+    times) over a fragmented pool, 3 layers, launched back to back (inside a
+    CUDA graph with programmatic dependent launch)."""
+    wl = W.custom(EDGE_LENGTHS * 3, num_layers=3, seed=330, hole_every=3, name="many")
+    st = DeviceState(wl)
+    ref, ok, ov = oracle_step(wl, st.host_k, st.host_v, *_host_inputs(st))
+    pool = _pool(wl, flags=pkv.PKV_FLAG_PDL if pdl else 0)
+    out = torch.full_like(st.out, float("nan"))
+
+    def chain():
+        for layer in range(wl.num_layers):
+            if fused:
+                pkv.pkv_append_attend(pool, layer, st.q[layer], st.k_new[layer], st.v_new[layer],
+                                      st.k_pool, st.v_pool, st.table, st.lens, out[layer])
+            else:
+                pkv.pkv_append(pool, layer, st.k_new[layer], st.v_new[layer], st.k_pool,
+                               st.v_pool, st.table, st.positions)
+                pkv.pkv_decode_attention(pool, layer, st.q[layer], st.k_pool, st.v_pool,
+                                         st.table, st.lens, out[layer])
+
+    if pdl:
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            chain()
+        g.replay()
+        torch.cuda.synchronize()
+    else:
+        chain()
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    assert np.array_equal(bits(st.k_pool), ok) and np.array_equal(bits(st.v_pool), ov)
+    got = out.cpu().numpy()
+    assert_close(got, ref, f"many fused={fused} pdl={pdl}")
+    if pdl:   # a second replay: the tickets were reset by the first
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+        assert_close(out.cpu().numpy(), ref, "second replay")
+
+
 def test_output_independent_of_physical_pages():
     """The same logical cache under two page permutations gives bit-identical
     output for a fixed split plan."""
