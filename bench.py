@@ -447,8 +447,8 @@ def run_ours(args, world, rank, local):
     if not args.no_cpu_baseline:
         threads = min(cpu_threads(), L)
         probe_dt, _, probe_layers = time_oracle(wl, threads, 1, threads)
-        # about 10-20 s of CPU work in total
-        n_steps = max(1, int(15.0 / max(probe_dt * threads, 1e-6)))
+        # about 20 s of CPU work (core-seconds) in total
+        n_steps = max(1, int(20.0 / max(probe_dt * threads, 1e-6)))
         dt, cbytes, n_layers = time_oracle(wl, threads, n_steps, threads)
         line["cpu_baseline"] = {
             "value": round(cbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
