@@ -51,7 +51,8 @@ constexpr int kMaxPages = kMaxSeqLen / 16;
 constexpr int kRowBytes = kDim * 2;             // one token of one kv head: 128 B
 constexpr int kTileBytes = kPage * kRowBytes;   // one (page, kv head) tile: 2 KiB
 // Block shapes: 4 warps with 3 page stages per warp. The ticket-merge kernel
-// fits 4 blocks per SM; the cluster-merge kernel (plus its inbox) 3, which
+// fits 4 blocks per SM (128 registers); the cluster-merge kernel (plus its
+// inbox) 3, so it may use up to 168 registers, and 3 per SM
 // leaves room for the next launch's blocks to become resident and prefetch
 // while this one finishes (8-warp cluster blocks, 2 per SM, measured slower
 // for 2 sequences because the next layer could not start early).
@@ -474,7 +475,7 @@ __device__ __forceinline__ void reduce_warp_state(WarpState& st) {
 // cluster (gridDim.x == cluster size) and merge through distributed shared
 // memory; otherwise splits merge through global partials and a ticket.
 template <bool kFused, bool kCluster, int kWarps, int kStages>
-__global__ void __launch_bounds__(kWarps * 32, 16 / kWarps) decode_kernel(const DecodeParams prm) {
+__global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decode_kernel(const DecodeParams prm) {
   constexpr int kThreads = kWarps * 32;
   using Smem = BlockSmem<kWarps, kStages>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
