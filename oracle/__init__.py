@@ -55,9 +55,13 @@ class Oracle:
         lib.pkv_oracle_decode_attention_split.argtypes = [G, i, P, P, P, P, P, i, i,
                                                           P, P, P, P]
         lib.pkv_oracle_contiguous_attention.argtypes = [P, P, P, i, i, i, i, P]
+        lib.pkv_oracle_append_rope.argtypes = [G, i, P, P, P, P, P, P, i, P, P, i]
+        lib.pkv_oracle_rope_queries.argtypes = [P, i, i, i, P, P, P, i, P]
+        lib.pkv_oracle_decode_attention_q64.argtypes = [G, i, P, P, P, P, P, i, P]
         for name in ("pkv_oracle_append", "pkv_oracle_decode_attention",
                      "pkv_oracle_decode_attention_mt", "pkv_oracle_decode_attention_split",
-                     "pkv_oracle_contiguous_attention"):
+                     "pkv_oracle_contiguous_attention", "pkv_oracle_append_rope",
+                     "pkv_oracle_rope_queries", "pkv_oracle_decode_attention_q64"):
             getattr(lib, name).restype = ctypes.c_int
         self.lib = lib
         self.path = path
@@ -123,6 +127,47 @@ class Oracle:
                                                         B, S, _ptr(out), _ptr(po), _ptr(pm),
                                                         _ptr(pl))
         return st, out, po, pm, pl
+
+    def append_rope(self, g, layer, k_new, v_new, k_pool, v_pool, block_tables, positions,
+                    cos_t, sin_t):
+        """append() with each new key rotated to its position (FP32, then BF16)."""
+        for a in (k_new, v_new, k_pool, v_pool):
+            _check(a, np.uint16)
+        _check(block_tables, np.int32)
+        _check(positions, np.int32)
+        _check(cos_t, np.float32)
+        _check(sin_t, np.float32)
+        return self.lib.pkv_oracle_append_rope(ctypes.byref(g), layer, _ptr(k_new), _ptr(v_new),
+                                               _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                               _ptr(positions), int(positions.shape[0]),
+                                               _ptr(cos_t), _ptr(sin_t), int(cos_t.shape[0]))
+
+    def rope_queries(self, q, positions, cos_t, sin_t):
+        """q [B][Hq][D] BF16 patterns -> (status, q rotated to its position, float64)."""
+        _check(q, np.uint16)
+        _check(positions, np.int32)
+        _check(cos_t, np.float32)
+        _check(sin_t, np.float32)
+        B, Hq, D = q.shape
+        out = np.zeros((B, Hq, D), np.float64)
+        st = self.lib.pkv_oracle_rope_queries(_ptr(q), B, Hq, D, _ptr(positions), _ptr(cos_t),
+                                              _ptr(sin_t), int(cos_t.shape[0]), _ptr(out))
+        return st, out
+
+    def decode_attention_q64(self, g, layer, q64, k_pool, v_pool, block_tables, seq_lens):
+        """decode_attention() with float64 queries [B][Hq][D] -> (status, out)."""
+        _check(q64, np.float64)
+        for a in (k_pool, v_pool):
+            _check(a, np.uint16)
+        _check(block_tables, np.int32)
+        _check(seq_lens, np.int32)
+        B = int(seq_lens.shape[0])
+        out = np.zeros((B, g.num_q_heads, g.head_dim), np.float64)
+        st = self.lib.pkv_oracle_decode_attention_q64(ctypes.byref(g), layer, _ptr(q64),
+                                                      _ptr(k_pool), _ptr(v_pool),
+                                                      _ptr(block_tables), _ptr(seq_lens), B,
+                                                      _ptr(out))
+        return st, out
 
     def contiguous_attention(self, q, k, v):
         """q [Hq][D], k and v [len][Hkv][D] (uint16 BF16 patterns) -> (status, out [Hq][D])."""

@@ -1,8 +1,9 @@
 """Build step for the CPU oracle (test infrastructure only).
 
 Compiles ``pkv_oracle.cpp`` with the host C++ compiler into
-``oracle/_build/libpkv_oracle.so``. Plain ``-O2`` with no architecture flags,
-so the same source builds on x86_64 and aarch64 hosts.
+``oracle/_build/libpkv_oracle.so``. Plain ``-O2`` with no architecture flags
+and no floating-point contraction, so the same source builds and rounds the
+same way on x86_64 and aarch64 hosts.
 """
 
 import os
@@ -21,7 +22,8 @@ def build(force: bool = False) -> str:
         return LIBRARY
     os.makedirs(BUILD_DIR, exist_ok=True)
     tmp = LIBRARY + f".tmp{os.getpid()}"
-    cmd = ["g++", "-std=c++17", "-O2", "-fPIC", "-shared", "-pthread",
+    # no fused multiply-add contraction: the same results on x86 and Arm hosts
+    cmd = ["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
            "-o", tmp, SOURCE]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIBRARY)

@@ -40,6 +40,17 @@
 //    pools; block tables are [layer][max_batch][max_pages_per_seq] int32;
 //  * BF16 values arrive as their 16-bit patterns and are widened exactly.
 //
+// Rotary position embedding (the pages have the decode step write the new
+// token at its absolute rotary position but do not print the rotation). Reading: the
+// rotate-half convention of Llama implementations, pairing dim i with
+// i + D/2, with the angles supplied as FP32 tables cos_t[p][i], sin_t[p][i]
+// (i < D/2) because the pages fix neither the base nor Llama 3.2's scaling:
+//   x'[i] = x[i] cos - x[i + D/2] sin,   x'[i + D/2] = x[i + D/2] cos + x[i] sin.
+// The appended key is stored in BF16, so its rotation is stated in the
+// precision in which that rounding is decided: FP32 products and sum, each
+// rounded, no fused multiply-add, then round to nearest even. Queries are not
+// stored and are rotated in FP64.
+//
 // The split variant computes, per contiguous range of logical pages, the
 // unnormalised partial (o, m, l) and merges the partials with the
 // log-sum-exp rule; it exists so that the merge algebra can be checked in
@@ -155,7 +166,8 @@ void attend_row(const double* q, const double* k_rows, const double* v_rows, int
 // All query heads of one sequence.
 int attend_sequence(const pkv_oracle_geometry* g, int layer, const uint16_t* q,
                     const uint16_t* k_pool, const uint16_t* v_pool, const int32_t* block_tables,
-                    const int32_t* seq_lens, int b, double* out, double* lse, double* wsum) {
+                    const int32_t* seq_lens, int b, double* out, double* lse, double* wsum,
+                    const double* q64 = nullptr) {
   const int D = g->head_dim;
   const int group = g->num_q_heads / g->num_kv_heads;
   const int len = seq_lens[b];
@@ -166,12 +178,28 @@ int attend_sequence(const pkv_oracle_geometry* g, int layer, const uint16_t* q,
       return ORACLE_OUT_OF_RANGE;
     for (int h = kv * group; h < (kv + 1) * group; ++h) {
       size_t row = static_cast<size_t>(b) * g->num_q_heads + h;
-      for (int d = 0; d < D; ++d) q_row[d] = bf16_bits_to_double(q[row * D + d]);
+      for (int d = 0; d < D; ++d)
+        q_row[d] = q64 ? q64[row * D + d] : bf16_bits_to_double(q[row * D + d]);
       attend_row(q_row.data(), k_rows.data(), v_rows.data(), len, D, out + row * D,
                  lse ? lse + row : nullptr, wsum ? wsum + row : nullptr);
     }
   }
   return ORACLE_OK;
+}
+
+float bf16_bits_to_float(uint16_t bits) {
+  uint32_t word = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &word, sizeof f);
+  return f;
+}
+
+// FP32 -> BF16 bit pattern, round to nearest, ties to even (finite inputs).
+uint16_t float_to_bf16_rne(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
 }
 
 }  // namespace
@@ -371,6 +399,93 @@ int pkv_oracle_contiguous_attention(const uint16_t* q, const uint16_t* k, const 
     }
   }
   return ORACLE_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+// Decode-time append with the key rotated to its position first: as
+// pkv_oracle_append, with k_new[b][kv] rotated by the angles of position
+// positions[b] (tables cos_t, sin_t: FP32 [table_len][D/2]) in the FP32
+// statement above, then rounded to BF16. V is copied unchanged.
+int pkv_oracle_append_rope(const pkv_oracle_geometry* g, int layer, const uint16_t* k_new,
+                           const uint16_t* v_new, uint16_t* k_pool, uint16_t* v_pool,
+                           const int32_t* block_tables, const int32_t* positions, int batch,
+                           const float* cos_t, const float* sin_t, int table_len) {
+  if (!geometry_ok(g) || g->head_dim % 2 != 0 || !cos_t || !sin_t || batch < 0 ||
+      batch > g->max_batch)
+    return ORACLE_BAD_ARG;
+  const int D = g->head_dim;
+  const int half = D / 2;
+  std::vector<uint16_t> rotated(static_cast<size_t>(batch) * g->num_kv_heads * D);
+  for (int b = 0; b < batch; ++b) {
+    const int pos = positions[b];
+    for (int kv = 0; kv < g->num_kv_heads; ++kv) {
+      const size_t row = (static_cast<size_t>(b) * g->num_kv_heads + kv) * D;
+      for (int i = 0; i < D; ++i) rotated[row + i] = k_new[row + i];
+      if (pos < 0 || pos >= table_len) continue;   // the append reports the range error
+      for (int i = 0; i < half; ++i) {
+        const float c = cos_t[static_cast<size_t>(pos) * half + i];
+        const float s = sin_t[static_cast<size_t>(pos) * half + i];
+        const float x = bf16_bits_to_float(k_new[row + i]);
+        const float y = bf16_bits_to_float(k_new[row + i + half]);
+        const float xc = x * c, ys = y * s, yc = y * c, xs = x * s;
+        rotated[row + i] = float_to_bf16_rne(xc - ys);
+        rotated[row + i + half] = float_to_bf16_rne(yc + xs);
+      }
+    }
+  }
+  return pkv_oracle_append(g, layer, rotated.data(), v_new, k_pool, v_pool, block_tables,
+                           positions, batch);
+}
+
+// Queries rotated to their positions, in double: q [batch][Hq][D] BF16 bit
+// patterns -> q_out double [batch][Hq][D].
+int pkv_oracle_rope_queries(const uint16_t* q, int batch, int num_q_heads, int head_dim,
+                            const int32_t* positions, const float* cos_t, const float* sin_t,
+                            int table_len, double* q_out) {
+  if (!q || !q_out || !cos_t || !sin_t || head_dim % 2 != 0 || batch < 0) return ORACLE_BAD_ARG;
+  const int half = head_dim / 2;
+  int status = ORACLE_OK;
+  for (int b = 0; b < batch; ++b) {
+    const int pos = positions[b];
+    for (int h = 0; h < num_q_heads; ++h) {
+      const size_t row = (static_cast<size_t>(b) * num_q_heads + h) * head_dim;
+      for (int i = 0; i < head_dim; ++i) q_out[row + i] = bf16_bits_to_double(q[row + i]);
+      if (pos < 0 || pos >= table_len) {
+        status = ORACLE_OUT_OF_RANGE;
+        continue;
+      }
+      for (int i = 0; i < half; ++i) {
+        const double c = cos_t[static_cast<size_t>(pos) * half + i];
+        const double s = sin_t[static_cast<size_t>(pos) * half + i];
+        const double x = bf16_bits_to_double(q[row + i]);
+        const double y = bf16_bits_to_double(q[row + i + half]);
+        q_out[row + i] = x * c - y * s;
+        q_out[row + i + half] = y * c + x * s;
+      }
+    }
+  }
+  return status;
+}
+
+// pkv_oracle_decode_attention with the queries given in double (q64
+// [batch][Hq][D]), e.g. after the rotation above.
+int pkv_oracle_decode_attention_q64(const pkv_oracle_geometry* g, int layer, const double* q64,
+                                    const uint16_t* k_pool, const uint16_t* v_pool,
+                                    const int32_t* block_tables, const int32_t* seq_lens,
+                                    int batch, double* out) {
+  if (!geometry_ok(g) || layer < 0 || layer >= g->num_layers || batch < 0 ||
+      batch > g->max_batch || !out || !q64)
+    return ORACLE_BAD_ARG;
+  int status = ORACLE_OK;
+  for (int b = 0; b < batch; ++b) {
+    int r = attend_sequence(g, layer, nullptr, k_pool, v_pool, block_tables, seq_lens, b, out,
+                            nullptr, nullptr, q64);
+    if (r != ORACLE_OK) status = r;
+  }
+  return status;
 }
 
 }  // extern "C"

@@ -331,8 +331,76 @@ def pin_append_rejects_out_of_range(orc):
             assert np.array_equal(kp, before_k) and np.array_equal(vp, before_v)
 
 
+def _rope_case(seed, n_pos=40):
+    rng = np.random.default_rng(seed)
+    wl = W.custom([n_pos, 7, 33], num_layers=1, seed=seed)
+    kp, vp = (bits(p) for p in wl.pools("cpu", "zero"))
+    kn, vn = bits(wl.k_new()), bits(wl.v_new())
+    g = oracle_pkg.geometry(1, wl.num_pages, wl.batch)
+    return rng, wl, kp, vp, kn, vn, g
+
+
+def pin_rope_zero_angle_is_identity(orc):
+    rng, wl, kp, vp, kn, vn, g = _rope_case(501)
+    cos_t = np.ones((W.MAX_SEQ_LEN, D // 2), np.float32)
+    sin_t = np.zeros_like(cos_t)
+    a_k, a_v = kp.copy(), vp.copy()
+    assert orc.append(g, 0, kn[0].copy(), vn[0].copy(), a_k, a_v, wl.block_tables,
+                      wl.positions) == oracle_pkg.OK
+    assert orc.append_rope(g, 0, kn[0].copy(), vn[0].copy(), kp, vp, wl.block_tables,
+                           wl.positions, cos_t, sin_t) == oracle_pkg.OK
+    assert np.array_equal(kp, a_k) and np.array_equal(vp, a_v)
+    q = normal_bits(rng, (3, HQ, D))
+    st, q64 = orc.rope_queries(q, wl.positions, cos_t, sin_t)
+    assert st == oracle_pkg.OK and np.array_equal(q64, bits_to_f64(q))
+
+
+def pin_rope_quarter_turn_swaps_halves(orc):
+    """cos = 0, sin = 1: x'[i] = -x[i + D/2] and x'[i + D/2] = x[i], exactly."""
+    rng, wl, kp, vp, kn, vn, g = _rope_case(502)
+    cos_t = np.zeros((W.MAX_SEQ_LEN, D // 2), np.float32)
+    sin_t = np.ones_like(cos_t)
+    assert orc.append_rope(g, 0, kn[0].copy(), vn[0].copy(), kp, vp, wl.block_tables,
+                           wl.positions, cos_t, sin_t) == oracle_pkg.OK
+    half = D // 2
+    for b in range(wl.batch):
+        pos = int(wl.positions[b])
+        got = bits_to_f64(kp[wl.block_tables[0, b, pos // P], :, pos % P, :])
+        x = bits_to_f64(kn[0, b])
+        np.testing.assert_array_equal(got[:, :half], -x[:, half:])
+        np.testing.assert_array_equal(got[:, half:], x[:, :half])
+    q = normal_bits(rng, (3, HQ, D))
+    st, q64 = orc.rope_queries(q, wl.positions, cos_t, sin_t)
+    qf = bits_to_f64(q)
+    np.testing.assert_array_equal(q64[..., :half], -qf[..., half:])
+    np.testing.assert_array_equal(q64[..., half:], qf[..., :half])
+
+
+def pin_rope_keeps_pair_norms_and_relative_scores(orc):
+    """A rotation keeps |(x_i, x_{i+D/2})|, and q_p . k_t depends on p - t only."""
+    rng = np.random.default_rng(503)
+    cos_t, sin_t = W.rope_tables(base=10000.0)
+    half = D // 2
+    q = normal_bits(rng, (1, HQ, D))
+    k = normal_bits(rng, (1, HQ, D))
+    def rot(x, p):
+        st, r = orc.rope_queries(x, np.array([p], np.int32), cos_t, sin_t)
+        assert st == oracle_pkg.OK
+        return r[0]
+    qf = bits_to_f64(q)[0]
+    r = rot(q, 777)
+    np.testing.assert_allclose(r[:, :half] ** 2 + r[:, half:] ** 2,
+                               qf[:, :half] ** 2 + qf[:, half:] ** 2, rtol=1e-6, atol=1e-9)
+    d1 = np.sum(rot(q, 100) * rot(k, 40), axis=-1)
+    d2 = np.sum(rot(q, 1100) * rot(k, 1040), axis=-1)
+    d0 = np.sum(rot(q, 60) * bits_to_f64(k)[0], axis=-1)
+    np.testing.assert_allclose(d1, d2, rtol=0, atol=2e-4)
+    np.testing.assert_allclose(d1, d0, rtol=0, atol=2e-4)
+
+
 ALL_PINS = [pin_golden_closed_form, pin_pool_geometry_facts, pin_single_token_returns_v_row,
             pin_zero_query_gives_mean_of_v, pin_weights_sum_to_one, pin_dominant_key,
             pin_paged_equals_contiguous, pin_contiguous_matches_sdpa, pin_paged_matches_sdpa,
             pin_split_equals_unsplit, pin_mt_matches_single_thread, pin_append_closed_form,
-            pin_append_rejects_out_of_range]
+            pin_append_rejects_out_of_range, pin_rope_zero_angle_is_identity,
+            pin_rope_quarter_turn_swaps_halves, pin_rope_keeps_pair_norms_and_relative_scores]

@@ -54,6 +54,15 @@ MUTATIONS = [
      "size_t src = (static_cast<size_t>(kv) * len + t) * D + d;", 0),
     ("threaded variant skips sequences", "for (int b = w; b < batch; b += nthreads)",
      "for (int b = w + 1; b < batch; b += nthreads)", 0),
+    ("key rotation sign flipped", "rotated[row + i] = float_to_bf16_rne(xc - ys);",
+     "rotated[row + i] = float_to_bf16_rne(xc + ys);", 0),
+    ("key rotation pairs neighbours", "const float y = bf16_bits_to_float(k_new[row + i + half]);",
+     "const float y = bf16_bits_to_float(k_new[row + (i ^ 1)]);", 0),
+    ("query rotation swaps cos and sin", "q_out[row + i + half] = y * c + x * s;",
+     "q_out[row + i + half] = y * s + x * c;", 0),
+    ("query rotation uses the wrong position",
+     "const double c = cos_t[static_cast<size_t>(pos) * half + i];",
+     "const double c = cos_t[static_cast<size_t>(pos + 1) * half + i];", 0),
 ]
 
 
@@ -70,7 +79,8 @@ def _pins_failed_by(tmp_path, text):
     mutant_src = tmp_path / "mutant.cpp"
     mutant_src.write_text(text)
     lib = tmp_path / "libmutant.so"
-    subprocess.run(["g++", "-std=c++17", "-O1", "-fPIC", "-shared", "-pthread", "-o", str(lib),
+    subprocess.run(["g++", "-std=c++17", "-O1", "-ffp-contract=off", "-fPIC", "-shared",
+                    "-pthread", "-o", str(lib),
                     str(mutant_src)], check=True)
     # run the pins in a child process: a planted index mistake may read out
     # of bounds, and a crash counts as noticed too

@@ -55,6 +55,17 @@ def pages_for_pool_mib(mib: int) -> int:
     return (mib * MIB) // PAGE_BYTES_KV
 
 
+def rope_tables(max_seq_len=MAX_SEQ_LEN, head_dim=HEAD_DIM, base=500000.0):
+    """Rotary angles as FP32 tables (cos, sin) of shape [max_seq_len][head_dim / 2]:
+    angle(p, i) = p * base^(-2 i / head_dim), taken in float64 then rounded.
+    The base is an input (the pages give neither it nor Llama 3.2's frequency
+    scaling); 500000 is the Llama 3 base."""
+    half = head_dim // 2
+    inv = base ** (-2.0 * np.arange(half, dtype=np.float64) / head_dim)
+    ang = np.arange(max_seq_len, dtype=np.float64)[:, None] * inv[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
 def _rng(seed: int, stream: str) -> np.random.Generator:
     return np.random.default_rng([seed, _STREAMS[stream]])
 
