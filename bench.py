@@ -14,7 +14,10 @@ same step with events between the launches gives the per-launch durations of
 the kernel for the roofline. value = KV GB/s
 = algorithmic bytes per step / step time, with algorithmic bytes per
 (sequence, layer) = seq_len x 2048 (every cached K/V row read once) + 2048
-(the new row written) + 4096 (q) + 8192 (FP32 out).
+(the new row written) + 4096 (q) + 8192 (FP32 out). With --rope the
+launches also rotate the appended key and the queries to their position
+(pkv_append_attend_rope; angle tables for base 500000), adding 256 bytes (the
+position's cos and sin rows) per (sequence, layer).
 
 --impl reference times the CPU oracle (FP64 C++) on the host cores on a
 bounded sample of the same workload and prints the same line with
@@ -60,9 +63,12 @@ DESCRIPTIONS = {
 }
 
 
-def step_bytes(wl):
+ROPE_BASE = 500000.0
+
+
+def step_bytes(wl, rope=False):
     """Algorithmic bytes of one fused step over all layers."""
-    per_seq = wl.seq_lens.astype(np.int64) * 2048 + 2048 + 4096 + 8192
+    per_seq = wl.seq_lens.astype(np.int64) * 2048 + 2048 + 4096 + 8192 + (256 if rope else 0)
     return int(per_seq.sum()) * wl.num_layers
 
 
@@ -185,17 +191,27 @@ def oracle_inputs(wl):
     return bits(kp), bits(vp), bits(wl.q()), bits(wl.k_new()), bits(wl.v_new())
 
 
-def time_oracle(wl, layers_per_step, n_steps, threads):
-    """Runs the oracle (append + attention) on `layers_per_step` layers per
-    step, layers in parallel over host threads; returns (seconds, bytes)."""
+def time_oracle(wl, layers_per_step, n_steps, threads, rope=False):
+    """Runs the oracle (append + attention, rotated when `rope`) on
+    `layers_per_step` layers per step, layers in parallel over host threads;
+    returns (seconds, bytes)."""
     import oracle
     orc = oracle.load()
     kp, vp, q, kn, vn = oracle_inputs(wl)
     g = oracle.geometry(wl.num_layers, wl.num_pages, wl.batch)
     pos = wl.positions
-    bytes_per_layer = step_bytes(wl) // wl.num_layers
+    bytes_per_layer = step_bytes(wl, rope) // wl.num_layers
+    cos_t, sin_t = W.rope_tables(base=ROPE_BASE)
 
     def one_layer(layer):
+        if rope:
+            st = orc.append_rope(g, layer, kn[layer].copy(), vn[layer].copy(), kp, vp,
+                                 wl.block_tables, pos, cos_t, sin_t)
+            st1, q64 = orc.rope_queries(q[layer].copy(), pos, cos_t, sin_t)
+            st2, _ = orc.decode_attention_q64(g, layer, q64, kp, vp, wl.block_tables,
+                                              wl.seq_lens)
+            assert st == st1 == st2 == oracle.OK
+            return layer
         st = orc.append(g, layer, kn[layer].copy(), vn[layer].copy(), kp, vp, wl.block_tables,
                         pos)
         st2, _, _, _ = orc.decode_attention(g, layer, q[layer].copy(), kp, vp,
@@ -224,12 +240,12 @@ def run_reference(args, world, rank):
     wl = WORKLOADS[args.workload]()
     threads = min(cpu_threads(), wl.num_layers)
     # size a step so the whole run stays within about a minute and a half
-    probe_dt, _, probe_layers = time_oracle(wl, threads, 1, threads)
+    probe_dt, _, probe_layers = time_oracle(wl, threads, 1, threads, args.rope)
     per_layer = probe_dt / probe_layers * threads   # core-seconds per layer
     budget = 90.0 / max(1, args.steps + args.warmup)
     layers = max(1, min(wl.num_layers, int(budget * threads / max(per_layer, 1e-9))))
-    time_oracle(wl, layers, args.warmup, threads)
-    dt, nbytes, n_layers = time_oracle(wl, layers, args.steps, threads)
+    time_oracle(wl, layers, args.warmup, threads, args.rope)
+    dt, nbytes, n_layers = time_oracle(wl, layers, args.steps, threads, args.rope)
     value = nbytes / dt / 1e9
     sample = (f"{layers} of {wl.num_layers} layers per step (all {wl.batch} sequences), "
               f"layers in parallel on {threads} threads, {args.steps} steps")
@@ -239,7 +255,9 @@ def run_reference(args, world, rank):
         "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
-                   "layers_per_step": layers},
+                   "layers_per_step": layers,
+                   "rope": f"key and queries rotated, base {ROPE_BASE:g}" if args.rope
+                   else "none"},
         "seq_layer_steps_per_s": round(n_layers * wl.batch / dt, 2),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
@@ -276,6 +294,7 @@ def run_ours(args, world, rank, local):
     out = torch.zeros((L, B, W.NUM_Q_HEADS, W.HEAD_DIM), device=dev)
     pool = pkv.pkv_pool_create(L, wl.num_pages, B, flags=0 if args.no_pdl else pkv.PKV_FLAG_PDL)
     splits = args.splits
+    rope_cos, rope_sin = (torch.from_numpy(t).to(dev) for t in W.rope_tables(base=ROPE_BASE))
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -295,8 +314,14 @@ def run_ours(args, world, rank, local):
         if marks:
             marks[0].record(s)
         for layer in range(L):
-            pkv.pkv_append_attend(pool, layer, q[layer], k_new[layer], v_new[layer], k_pool,
-                                  v_pool, table, lens, out[layer], num_splits=splits, stream=s)
+            if args.rope:
+                pkv.pkv_append_attend_rope(pool, layer, q[layer], k_new[layer], v_new[layer],
+                                           k_pool, v_pool, table, lens, rope_cos, rope_sin,
+                                           out[layer], num_splits=splits, stream=s)
+            else:
+                pkv.pkv_append_attend(pool, layer, q[layer], k_new[layer], v_new[layer], k_pool,
+                                      v_pool, table, lens, out[layer], num_splits=splits,
+                                      stream=s)
             if marks and len(marks) > 2:
                 marks[layer + 1].record(s)
         if marks and len(marks) == 2:
@@ -390,7 +415,7 @@ def run_ours(args, world, rank, local):
     assert pkv.pkv_get_error(pool) == pkv.PKV_OK
     e2e_total = max_over_ranks(sum(e2e_ms), world)
 
-    nbytes = step_bytes(wl)
+    nbytes = step_bytes(wl, args.rope)
     ms_per_step = total_ms / args.steps
     value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
     e2e_value = world * nbytes * len(e2e_ms) / (e2e_total * 1e-3) / 1e9
@@ -403,7 +428,7 @@ def run_ours(args, world, rank, local):
     launch_source = "timed-region CUDA events (start/end of each step) / 16 launches"
     events_between = (round(statistics.mean(launch_ms), 6) if launch_ms else None)
     achieved = (nbytes / L) / (per_launch_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload + ("-rope" if args.rope else ""))
 
     if rank != 0:
         return
@@ -420,6 +445,8 @@ def run_ours(args, world, rank, local):
             "step": "16 x fused append+attend (one launch per layer), CUDA graph" +
                     ("" if args.no_pdl else ", programmatic dependent launch between layers"),
             "splits": chunk_note,
+            "rope": f"key and queries rotated in the launch, base {ROPE_BASE:g}" if args.rope
+                    else "none (keys arrive rotated)",
             "l2": "flushed before every step (read of a buffer twice the L2 size, outside the "
                   "timed events)",
             "bytes_per_step": nbytes,
@@ -446,10 +473,10 @@ def run_ours(args, world, rank, local):
     }
     if not args.no_cpu_baseline:
         threads = min(cpu_threads(), L)
-        probe_dt, _, probe_layers = time_oracle(wl, threads, 1, threads)
+        probe_dt, _, probe_layers = time_oracle(wl, threads, 1, threads, args.rope)
         # about 20 s of CPU work (core-seconds) in total
         n_steps = max(1, int(20.0 / max(probe_dt * threads, 1e-6)))
-        dt, cbytes, n_layers = time_oracle(wl, threads, n_steps, threads)
+        dt, cbytes, n_layers = time_oracle(wl, threads, n_steps, threads, args.rope)
         line["cpu_baseline"] = {
             "value": round(cbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
@@ -467,6 +494,8 @@ def main():
     ap.add_argument("--workload", choices=list(WORKLOADS), default="llama-b2-2048")
     ap.add_argument("--splits", type=int, default=0, help="0: the library chooses")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rope", action="store_true",
+                    help="rotate the appended key and the queries inside the launches")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch")
     args = ap.parse_args()

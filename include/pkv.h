@@ -88,12 +88,13 @@ typedef struct {
 
 /* Launch decode kernels with programmatic dependent launch: a launch may
  * start while the kernel before it in the stream is still running, and
- * before waiting for that kernel it reads block_tables, seq_lens and the
- * pool rows below position seq_lens[b] - 1 (the unfused decode defers the
- * page holding that position). q, k, v, out and the appended slot are read
- * or written only after the wait. Contract: the kernel immediately before a
- * decode launch in the stream must not write block_tables, seq_lens or those
- * pool rows. Off by default. */
+ * before waiting for that kernel it reads block_tables, seq_lens, the rotary
+ * tables (the _rope entry points) and the pool rows below position
+ * seq_lens[b] - 1 (the unfused decode defers the page holding that
+ * position). q, k, v, out and the appended slot are read or written only
+ * after the wait. Contract: the kernel immediately before a decode launch in
+ * the stream must not write block_tables, seq_lens, the rotary tables or
+ * those pool rows. Off by default. */
 #define PKV_FLAG_PDL 1
 
 typedef struct pkv_pool* pkv_pool_t;
@@ -153,6 +154,45 @@ pkv_status pkv_append_attend(pkv_pool_t pool, int layer, const void* q, const vo
                              const void* v, void* k_pool, void* v_pool,
                              const int32_t* block_tables, const int32_t* seq_lens, float* out,
                              int batch, int num_splits, void* stream);
+
+/* Rotary position embedding applied on the decode path. The pages have decode
+ * write the new token at its absolute rotary position [samir-vllm: Build LLM
+ * Inference From Scratch in C++ and CUDA, "Architecture walkthrough", KV
+ * cache paragraph; 6 Hours of YouTube and 85 handtyped pages of notes on LLM
+ * Inference - Start here, README feature list, shared BF16 KV page pool
+ * bullet] and the prefill stack applies RoPE to Q and K; they do not print the
+ * rotation, so it is the rotate-half form: dim i < 32 pairs with dim i + 32,
+ *   x'[i] = x[i] cos(a) - x[i+32] sin(a),  x'[i+32] = x[i+32] cos(a) + x[i] sin(a),
+ * a = angle (p, i) for position p.
+ *
+ * rope_cos, rope_sin: device FP32 tables [max_seq_len][32] (cos and sin of
+ * the angle of pair i at position p; row p at offset 32 p), 16-byte aligned,
+ * owned by the caller, read-only here; the base and any frequency scaling are
+ * the caller's choice. A null or misaligned table returns INVALID_ARG.
+ *
+ * Keys are rotated in FP32 with each product and the sum rounded separately
+ * (no fused multiply-add) and stored as BF16 rounded to nearest even, so the
+ * pool content is bit-defined. Queries are rotated in FP32 and never stored.
+ *
+ * pkv_append_rope: pkv_append with each key rotated to positions[b].
+ * pkv_decode_attention_rope: pkv_decode_attention with each query rotated to
+ *   position seq_lens[b] - 1 (the cached keys are expected to be rotated).
+ * pkv_append_attend_rope: pkv_append_attend with both: the same results as
+ *   pkv_append_rope then pkv_decode_attention_rope, in one launch. */
+pkv_status pkv_append_rope(pkv_pool_t pool, int layer, const void* k, const void* v,
+                           void* k_pool, void* v_pool, const int32_t* block_tables,
+                           const int32_t* positions, const float* rope_cos,
+                           const float* rope_sin, int batch, void* stream);
+pkv_status pkv_decode_attention_rope(pkv_pool_t pool, int layer, const void* q,
+                                     const void* k_pool, const void* v_pool,
+                                     const int32_t* block_tables, const int32_t* seq_lens,
+                                     const float* rope_cos, const float* rope_sin, float* out,
+                                     int batch, int num_splits, void* stream);
+pkv_status pkv_append_attend_rope(pkv_pool_t pool, int layer, const void* q, const void* k,
+                                  const void* v, void* k_pool, void* v_pool,
+                                  const int32_t* block_tables, const int32_t* seq_lens,
+                                  const float* rope_cos, const float* rope_sin, float* out,
+                                  int batch, int num_splits, void* stream);
 
 /* Synchronises `stream`, then returns and clears the sticky device error
  * flag: PKV_OK, PKV_ERR_OUT_OF_RANGE or PKV_ERR_DEVICE_TIMEOUT (or CUDA if

@@ -25,7 +25,8 @@ PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OUT_OF_RANGE, PKV_ERR_CUDA, PKV_ERR_UNSUPPO
     PKV_ERR_DEVICE_TIMEOUT, PKV_ERR_STATIC_LIMIT = range(7)
 
 EXPORTED = ("pkv_pool_create", "pkv_pool_destroy", "pkv_append", "pkv_decode_attention",
-            "pkv_append_attend", "pkv_get_error", "pkv_decode_attention_noalloc",
+            "pkv_append_attend", "pkv_append_rope", "pkv_decode_attention_rope",
+            "pkv_append_attend_rope", "pkv_get_error", "pkv_decode_attention_noalloc",
             "pkv_status_string")
 
 
@@ -66,6 +67,9 @@ def load(path: str = None):
     lib.pkv_append.argtypes = [P, i, P, P, P, P, P, P, i, P]
     lib.pkv_decode_attention.argtypes = [P, i, P, P, P, P, P, P, i, i, P]
     lib.pkv_append_attend.argtypes = [P, i, P, P, P, P, P, P, P, P, i, i, P]
+    lib.pkv_append_rope.argtypes = [P, i, P, P, P, P, P, P, P, P, i, P]
+    lib.pkv_decode_attention_rope.argtypes = [P, i, P, P, P, P, P, P, P, P, i, i, P]
+    lib.pkv_append_attend_rope.argtypes = [P, i, P, P, P, P, P, P, P, P, P, P, i, i, P]
     lib.pkv_get_error.argtypes = [P, P]
     lib.pkv_decode_attention_noalloc.argtypes = [i, P, P, P, P, P, P, i, i, i, i, i, i, P, P]
     lib.pkv_status_string.argtypes = [i]
@@ -165,6 +169,39 @@ def pkv_append_attend(pool: Pool, layer, q, k, v, k_pool, v_pool, block_tables, 
                                      _addr(seq_lens), _addr(out), _batch(seq_lens, batch),
                                      int(num_splits), _stream(stream))
     _check(st, "pkv_append_attend")
+
+
+def pkv_append_rope(pool: Pool, layer, k, v, k_pool, v_pool, block_tables, positions,
+                    rope_cos, rope_sin, batch=None, stream=None):
+    """pkv_append with each key rotated to its position; rope_cos/rope_sin:
+    fp32 [max_seq_len][32] on the device."""
+    st = pool._lib.pkv_append_rope(pool.handle, int(layer), _addr(k), _addr(v), _addr(k_pool),
+                                   _addr(v_pool), _addr(block_tables), _addr(positions),
+                                   _addr(rope_cos), _addr(rope_sin), _batch(positions, batch),
+                                   _stream(stream))
+    _check(st, "pkv_append_rope")
+
+
+def pkv_decode_attention_rope(pool: Pool, layer, q, k_pool, v_pool, block_tables, seq_lens,
+                              rope_cos, rope_sin, out, batch=None, num_splits=0, stream=None):
+    """pkv_decode_attention with each query rotated to position seq_lens - 1."""
+    st = pool._lib.pkv_decode_attention_rope(pool.handle, int(layer), _addr(q), _addr(k_pool),
+                                             _addr(v_pool), _addr(block_tables),
+                                             _addr(seq_lens), _addr(rope_cos), _addr(rope_sin),
+                                             _addr(out), _batch(seq_lens, batch),
+                                             int(num_splits), _stream(stream))
+    _check(st, "pkv_decode_attention_rope")
+
+
+def pkv_append_attend_rope(pool: Pool, layer, q, k, v, k_pool, v_pool, block_tables, seq_lens,
+                           rope_cos, rope_sin, out, batch=None, num_splits=0, stream=None):
+    """pkv_append_attend with the key and the queries rotated to seq_lens - 1."""
+    st = pool._lib.pkv_append_attend_rope(pool.handle, int(layer), _addr(q), _addr(k), _addr(v),
+                                          _addr(k_pool), _addr(v_pool), _addr(block_tables),
+                                          _addr(seq_lens), _addr(rope_cos), _addr(rope_sin),
+                                          _addr(out), _batch(seq_lens, batch),
+                                          int(num_splits), _stream(stream))
+    _check(st, "pkv_append_attend_rope")
 
 
 def pkv_get_error(pool: Pool, stream=None) -> int:

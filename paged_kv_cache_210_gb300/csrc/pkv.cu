@@ -129,6 +129,8 @@ struct DecodeParams {
   int num_splits;             // > 0: S ranges per sequence
   int chunk_pages;            // > 0: ranges of this many pages (used when num_splits == 0)
   int early_trigger;          // let the next launch start right after the prefetch (one wave)
+  const float* rope_cos;      // rotary angles [max_seq_len][32] FP32, or null: no rotation
+  const float* rope_sin;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -242,6 +244,51 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
+// Two FP32 values -> BF16 pair (element 0 in the low half), each rounded to
+// nearest, ties to even.
+__device__ __forceinline__ uint32_t float2_to_bf16x2(float e0, float e1) {
+  uint32_t w;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(e1), "f"(e0));
+  return w;
+}
+
+// cos (or sin) of the 8 rotary angles 8 c4 .. 8 c4 + 7 of one position row.
+__device__ __forceinline__ void load_angles(const float* row, int c4, float (&v)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(row + 8 * c4));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(row + 8 * c4 + 4));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// Rotary embedding of one 16-byte chunk (8 dims) of the appended key. Dim i of
+// the low half pairs with dim i + 32 (rotate-half): low' = low cos - high sin,
+// high' = high cos + low sin. `own` is chunk c (dims 8c .. 8c+7), `partner` the
+// chunk 4 away, `high` says own is in the upper half; cs/sn hold the angles of
+// pairs 8 (c mod 4) .. +7. Products and sum are each rounded in FP32 (no fused
+// multiply-add), then to BF16, so the stored key has one defined value.
+__device__ __forceinline__ uint4 rope_key_chunk(uint4 own, uint4 partner, bool high,
+                                               const float (&cs)[8], const float (&sn)[8]) {
+  const uint32_t a[4] = {own.x, own.y, own.z, own.w};
+  const uint32_t b[4] = {partner.x, partner.y, partner.z, partner.w};
+  uint32_t o[4];
+  #pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 fa = bf16x2_to_float2(a[j]);
+    const float2 fb = bf16x2_to_float2(b[j]);
+    const float ac0 = __fmul_rn(fa.x, cs[2 * j]), bs0 = __fmul_rn(fb.x, sn[2 * j]);
+    const float ac1 = __fmul_rn(fa.y, cs[2 * j + 1]), bs1 = __fmul_rn(fb.y, sn[2 * j + 1]);
+    const float e0 = high ? __fadd_rn(ac0, bs0) : __fsub_rn(ac0, bs0);
+    const float e1 = high ? __fadd_rn(ac1, bs1) : __fsub_rn(ac1, bs1);
+    o[j] = float2_to_bf16x2(e0, e1);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint4 shfl_xor_uint4(uint4 v, int m) {
+  return make_uint4(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m),
+                    __shfl_xor_sync(0xffffffffu, v.z, m), __shfl_xor_sync(0xffffffffu, v.w, m));
+}
+
 // 2^x by the SFU's approximate exponential (PTX ex2.approx.ftz.f32: relative
 // error about 2^-22; results below 2^-126, i.e. softmax weights that cannot
 // contribute, flush to zero; 2^-inf = 0).
@@ -262,6 +309,8 @@ __device__ __forceinline__ void set_error(int* err, int bits) { atomicOr(err, bi
 // ---------------------------------------------------------------- append
 // One block of 128 threads per sequence: thread t copies 16-byte chunk
 // (t % 64) % 8 of kv head (t % 64) / 8, of K for t < 64 and of V otherwise.
+// With rotary tables the key is rotated to its position on the way (the
+// partner chunk sits in lane t ^ 4 of the same warp).
 __global__ void __launch_bounds__(128) append_kernel(const uint16_t* __restrict__ k,
                                                      const uint16_t* __restrict__ v,
                                                      uint16_t* __restrict__ k_pool,
@@ -269,7 +318,9 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t* __restrict_
                                                      const int32_t* __restrict__ table,
                                                      const int32_t* __restrict__ positions,
                                                      int table_stride, int num_pages,
-                                                     int max_seq_len, int* err) {
+                                                     int max_seq_len, int* err,
+                                                     const float* __restrict__ rope_cos,
+                                                     const float* __restrict__ rope_sin) {
   const int b = blockIdx.x;
   const int t = threadIdx.x;
   const int pos = positions[b];
@@ -289,7 +340,17 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t* __restrict_
   const uint16_t* src = (t < 64 ? k : v) + (static_cast<size_t>(b) * kHkv + head) * kDim + chunk * 8;
   uint16_t* dst = (t < 64 ? k_pool : v_pool) +
                   ((static_cast<size_t>(page) * kHkv + head) * kPage + slot) * kDim + chunk * 8;
-  *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+  uint4 val = __ldg(reinterpret_cast<const uint4*>(src));
+  if (rope_cos) {   // the same for every thread of the block
+    const uint4 partner = shfl_xor_uint4(val, 4);
+    if (t < 64) {
+      float cs[8], sn[8];
+      load_angles(rope_cos + static_cast<size_t>(pos) * (kDim / 2), chunk & 3, cs);
+      load_angles(rope_sin + static_cast<size_t>(pos) * (kDim / 2), chunk & 3, sn);
+      val = rope_key_chunk(val, partner, chunk >= 4, cs, sn);
+    }
+  }
+  *reinterpret_cast<uint4*>(dst) = val;
 }
 
 // ---------------------------------------------------------------- page computation
@@ -325,25 +386,46 @@ struct WarpState {
 };
 
 // q of the 4 heads at qrow ([4][64] BF16) for this lane's chunks, scaled by
-// log2(e) / sqrt(64) so that scores come out in base 2.
+// log2(e) / sqrt(64) so that scores come out in base 2. kRope: q is first
+// rotated in FP32 by the angles cs, sn of pairs 8 qd .. 8 qd + 7 at the
+// query's position; the lane's chunks qd and qd + 4 are exactly the two
+// halves of those pairs. With the scale folded into the angles and the sign
+// of the rotation folded into sin (chunk A is the low half when cA < 4):
+//   A' = A c' + B s_A,  B' = B c' - A s_A,  c' = c scale, s_A = -/+ s scale.
+template <bool kRope>
 __device__ __forceinline__ void load_q(const uint16_t* qrow, const LaneRoles& r,
                                        float2 (&qa)[kGroup][4], float2 (&qb)[kGroup][4],
-                                       bool from_shared) {
+                                       const float (&cs)[8], const float (&sn)[8]) {
   const float qscale = 1.4426950408889634f * 0.125f;
+  float2 cq[4], sa[4], sb[4];
+  if (kRope) {
+    const float sgn = r.cA < 4 ? -qscale : qscale;
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      cq[j] = make_float2(cs[2 * j] * qscale, cs[2 * j + 1] * qscale);
+      sa[j] = make_float2(sn[2 * j] * sgn, sn[2 * j + 1] * sgn);
+      sb[j] = make_float2(-sa[j].x, -sa[j].y);
+    }
+  }
   #pragma unroll
   for (int g = 0; g < kGroup; ++g) {
     const uint4* pa = reinterpret_cast<const uint4*>(qrow + g * kDim + r.cA * 8);
     const uint4* pb = reinterpret_cast<const uint4*>(qrow + g * kDim + r.cB * 8);
-    const uint4 ra = from_shared ? *pa : __ldg(pa);
-    const uint4 rb = from_shared ? *pb : __ldg(pb);
+    const uint4 ra = __ldg(pa);
+    const uint4 rb = __ldg(pb);
     const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
     const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
     #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 fa = bf16x2_to_float2(wa[j]);
       const float2 fb = bf16x2_to_float2(wb[j]);
-      qa[g][j] = make_float2(fa.x * qscale, fa.y * qscale);
-      qb[g][j] = make_float2(fb.x * qscale, fb.y * qscale);
+      if (kRope) {
+        qa[g][j] = ffma2(fb, sa[j], fmul2(fa, cq[j]));
+        qb[g][j] = ffma2(fa, sb[j], fmul2(fb, cq[j]));
+      } else {
+        qa[g][j] = make_float2(fa.x * qscale, fa.y * qscale);
+        qb[g][j] = make_float2(fb.x * qscale, fb.y * qscale);
+      }
     }
   }
 }
@@ -474,7 +556,7 @@ __device__ __forceinline__ void reduce_warp_state(WarpState& st) {
 // kCluster: the splits of one (sequence, kv head) form one thread-block
 // cluster (gridDim.x == cluster size) and merge through distributed shared
 // memory; otherwise splits merge through global partials and a ticket.
-template <bool kFused, bool kCluster, int kWarps, int kStages>
+template <bool kFused, bool kCluster, int kWarps, int kStages, bool kRope>
 __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decode_kernel(const DecodeParams prm) {
   constexpr int kThreads = kWarps * 32;
   using Smem = BlockSmem<kWarps, kStages>;
@@ -550,17 +632,59 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
       mbar_arrive(&ws.bar[stage]);
     }
   };
-  // Fused step: lanes 0..15 write the appended token's K/V row to the pool and
-  // to the stage tile (only after the wait: k/v may come from the previous kernel).
-  auto place_new_row = [&](int i, int stage, int phys) {
-    const int lp = page_begin + warp + kWarps * i;
-    if (!kFused || lp != last_page || lane >= 16) return;
+  // Rotary angles of the position len - 1 for pairs 8 (lane & 3) .. + 7: the
+  // query rotation uses them, and so does the key rotation in lanes 0..7
+  // (chunk c = lane, c & 3 == lane & 3). The tables are constant inputs, read
+  // ahead of the wait for the previous launch.
+  float rcs[8], rsn[8];
+  if (kRope) {
+    load_angles(prm.rope_cos + static_cast<size_t>(len - 1) * (kDim / 2), lane & 3, rcs);
+    load_angles(prm.rope_sin + static_cast<size_t>(len - 1) * (kDim / 2), lane & 3, rsn);
+  }
+
+  // Fused step: the warp whose i_new-th page is the sequence's last page
+  // writes the appended token's K/V row to the pool and to the stage tile.
+  // Lanes 0..15 load one 16-byte chunk each (K for lanes 0..7, V for 8..15),
+  // only after the wait: k/v may come from the previous kernel.
+  const int new_off = last_page - page_begin - warp;
+  const int i_new = kFused && new_off >= 0 && new_off % kWarps == 0 && new_off / kWarps < mine
+                        ? new_off / kWarps
+                        : -1;
+  auto load_new_row = [&]() {
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (lane < 16) {
+      const uint16_t* src = (lane >= 8 ? prm.v_new : prm.k_new) +
+                            (static_cast<size_t>(b) * kHkv + kvh) * kDim + (lane & 7) * 8;
+      val = __ldg(reinterpret_cast<const uint4*>(src));
+    }
+    return val;
+  };
+  // Stores the loaded chunk `val` (page i_new, in stage `stage`). With rotary
+  // tables lanes 0..7 rotate the key first, the partner chunk coming from
+  // lane ^ 4, with the angles above (`preloaded`) or loaded again (in the
+  // page loop, where rcs/rsn are no longer kept). Called by the whole warp.
+  auto place_new_row = [&](int stage, int phys, bool preloaded, uint4 val) {
     if (phys < 0 || phys >= prm.num_pages) return;
     const bool is_v = lane >= 8;
     const int c = lane & 7;
-    const uint16_t* src = (is_v ? prm.v_new : prm.k_new) +
-                          (static_cast<size_t>(b) * kHkv + kvh) * kDim + c * 8;
-    const uint4 val = __ldg(reinterpret_cast<const uint4*>(src));
+    if (kRope) {
+      const uint4 partner = shfl_xor_uint4(val, 4);
+      if (lane < 8) {
+        float cs[8], sn[8];
+        if (preloaded) {
+          #pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            cs[e] = rcs[e];
+            sn[e] = rsn[e];
+          }
+        } else {
+          load_angles(prm.rope_cos + static_cast<size_t>(len - 1) * (kDim / 2), c & 3, cs);
+          load_angles(prm.rope_sin + static_cast<size_t>(len - 1) * (kDim / 2), c & 3, sn);
+        }
+        val = rope_key_chunk(val, partner, c >= 4, cs, sn);
+      }
+    }
+    if (lane >= 16) return;
     uint16_t* pool = is_v ? prm.v_pool : prm.k_pool;
     *reinterpret_cast<uint4*>(pool + ((static_cast<size_t>(phys) * kHkv + kvh) * kPage +
                                       new_slot) * kDim + c * 8) = val;
@@ -596,15 +720,20 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
   // launch do not take slots this launch's later blocks need.
   if (prm.early_trigger) pdl_launch_dependents();
   pdl_wait();
+  // the new row's load goes out before q's, so the two latencies overlap
+  const bool new_in_prologue = i_new >= 0 && i_new < n_prefetch;
+  uint4 new_val = make_uint4(0u, 0u, 0u, 0u);
+  if (new_in_prologue) new_val = load_new_row();
   if (deferred >= 0) issue_copy(deferred, deferred, __shfl_sync(0xffffffffu, my_phys, deferred));
-  for (int i = 0; i < n_prefetch; ++i) place_new_row(i, i, __shfl_sync(0xffffffffu, my_phys, i));
   int issued = n_prefetch;
-  __syncwarp();   // the appended row written by lanes 0..15 is read by every lane
 
   const LaneRoles rl(lane);
   const int tp = rl.tp, gh = rl.gh, dq = rl.dq, tpar = rl.tpar;
   float2 qa[kGroup][4], qb[kGroup][4];
-  load_q(prm.q + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim, rl, qa, qb, false);
+  load_q<kRope>(prm.q + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim, rl, qa, qb, rcs,
+                rsn);
+  if (new_in_prologue) place_new_row(i_new, __shfl_sync(0xffffffffu, my_phys, i_new), true, new_val);
+  __syncwarp();   // the appended row written by lanes 0..15 is read by every lane
 
   WarpState st;
   st.reset();
@@ -627,7 +756,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
     if (i + kStages < mine) {
       const int next_phys = __shfl_sync(0xffffffffu, my_phys, i + kStages);
       issue_copy(i + kStages, stage, next_phys);
-      place_new_row(i + kStages, stage, next_phys);
+      if (i + kStages == i_new) place_new_row(stage, next_phys, false, load_new_row());
       __syncwarp();
       issued = i + kStages + 1;
     }
@@ -880,10 +1009,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // The two kernel shapes: ticket merge (4 warps, 3 stages) and cluster merge
 // (8 warps, 2 stages, plus the leader's inbox).
-template <bool kFused>
-constexpr auto ticket_kernel = decode_kernel<kFused, false, kTicketWarps, kTicketStages>;
-template <bool kFused>
-constexpr auto cluster_kernel = decode_kernel<kFused, true, kClusterWarps, kClusterStages>;
+template <bool kFused, bool kRope = false>
+constexpr auto ticket_kernel = decode_kernel<kFused, false, kTicketWarps, kTicketStages, kRope>;
+template <bool kFused, bool kRope = false>
+constexpr auto cluster_kernel = decode_kernel<kFused, true, kClusterWarps, kClusterStages, kRope>;
 
 size_t smem_bytes(bool cluster) {
   return cluster ? sizeof(BlockSmem<kClusterWarps, kClusterStages>) + sizeof(ClusterInbox)
@@ -949,7 +1078,9 @@ template <bool kFused>
 pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* k,
                          const void* v, const void* k_pool, const void* v_pool,
                          const int32_t* block_tables, const int32_t* seq_lens, float* out,
-                         int batch, int num_splits, void* stream) {
+                         int batch, int num_splits, void* stream,
+                         const float* rope_cos = nullptr, const float* rope_sin = nullptr,
+                         bool rope = false) {
   if (!pool) return PKV_ERR_INVALID_ARG;
   const pkv_pool_config& c = pool->cfg;
   if (layer < 0 || layer >= c.num_layers || batch < 0 || batch > c.max_batch)
@@ -962,6 +1093,8 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
       !aligned16(seq_lens) || !aligned16(out))
     return PKV_ERR_INVALID_ARG;
   if (kFused && (!aligned16(k) || !aligned16(v))) return PKV_ERR_INVALID_ARG;
+  if (rope && (!rope_cos || !rope_sin || !aligned16(rope_cos) || !aligned16(rope_sin)))
+    return PKV_ERR_INVALID_ARG;
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_ERR_INVALID_ARG;
@@ -985,6 +1118,8 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   prm.table_stride = max_pages;
   prm.max_seq_len = c.max_seq_len;
   prm.max_splits = c.max_splits;
+  prm.rope_cos = rope ? rope_cos : nullptr;
+  prm.rope_sin = rope ? rope_sin : nullptr;
 
   // Plan: S splits per sequence merged in a cluster when 2 <= S <= the
   // largest cluster this device schedules; otherwise (S = 1, S larger, or a
@@ -1034,8 +1169,14 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   }
   cfg.attrs = attrs;
   cfg.numAttrs = n_attrs;
-  cudaError_t e = cluster ? cudaLaunchKernelEx(&cfg, cluster_kernel<kFused>, prm)
-                          : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused>, prm);
+  cudaError_t e;
+  if (rope) {
+    e = cluster ? cudaLaunchKernelEx(&cfg, cluster_kernel<kFused, true>, prm)
+                : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused, true>, prm);
+  } else {
+    e = cluster ? cudaLaunchKernelEx(&cfg, cluster_kernel<kFused>, prm)
+                : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused>, prm);
+  }
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return check_launch();
 }
@@ -1129,6 +1270,8 @@ pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_
   prm.num_splits = num_splits;
   prm.chunk_pages = 0;
   prm.early_trigger = 1;   // launched without programmatic dependent launch: no effect
+  prm.rope_cos = nullptr;
+  prm.rope_sin = nullptr;
   ticket_kernel<false><<<dim3(num_splits, kHkv, batch), block_threads(false), smem_bytes(false),
                          s>>>(prm);
   return check_launch();
@@ -1182,6 +1325,10 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
   ok = ok && set_kernel_attributes(ticket_kernel<true>, false);
   ok = ok && set_kernel_attributes(cluster_kernel<false>, true);
   ok = ok && set_kernel_attributes(cluster_kernel<true>, true);
+  ok = ok && set_kernel_attributes(ticket_kernel<false, true>, false);
+  ok = ok && set_kernel_attributes(ticket_kernel<true, true>, false);
+  ok = ok && set_kernel_attributes(cluster_kernel<false, true>, true);
+  ok = ok && set_kernel_attributes(cluster_kernel<true, true>, true);
 
   ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                   &pool->blocks_per_sm, ticket_kernel<true>, block_threads(false),
@@ -1231,9 +1378,14 @@ pkv_status pkv_pool_destroy(pkv_pool_t pool) {
   return st;
 }
 
-pkv_status pkv_append(pkv_pool_t pool, int layer, const void* k, const void* v, void* k_pool,
-                      void* v_pool, const int32_t* block_tables, const int32_t* positions,
-                      int batch, void* stream) {
+}  // extern "C"
+
+namespace {
+
+pkv_status launch_append(pkv_pool_t pool, int layer, const void* k, const void* v, void* k_pool,
+                         void* v_pool, const int32_t* block_tables, const int32_t* positions,
+                         const float* rope_cos, const float* rope_sin, bool rope, int batch,
+                         void* stream) {
   if (!pool) return PKV_ERR_INVALID_ARG;
   const pkv_pool_config& c = pool->cfg;
   if (layer < 0 || layer >= c.num_layers || batch < 0 || batch > c.max_batch)
@@ -1243,6 +1395,8 @@ pkv_status pkv_append(pkv_pool_t pool, int layer, const void* k, const void* v, 
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool) ||
       !aligned16(block_tables) || !aligned16(positions))
     return PKV_ERR_INVALID_ARG;
+  if (rope && (!rope_cos || !rope_sin || !aligned16(rope_cos) || !aligned16(rope_sin)))
+    return PKV_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_ERR_INVALID_ARG;
   const int max_pages = c.max_seq_len / kPage;
@@ -1250,8 +1404,28 @@ pkv_status pkv_append(pkv_pool_t pool, int layer, const void* k, const void* v, 
       static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v),
       static_cast<uint16_t*>(k_pool), static_cast<uint16_t*>(v_pool),
       block_tables + static_cast<size_t>(layer) * c.max_batch * max_pages, positions, max_pages,
-      c.num_pages, c.max_seq_len, pool->err);
+      c.num_pages, c.max_seq_len, pool->err, rope ? rope_cos : nullptr,
+      rope ? rope_sin : nullptr);
   return check_launch();
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_append(pkv_pool_t pool, int layer, const void* k, const void* v, void* k_pool,
+                      void* v_pool, const int32_t* block_tables, const int32_t* positions,
+                      int batch, void* stream) {
+  return launch_append(pool, layer, k, v, k_pool, v_pool, block_tables, positions, nullptr,
+                       nullptr, false, batch, stream);
+}
+
+pkv_status pkv_append_rope(pkv_pool_t pool, int layer, const void* k, const void* v,
+                           void* k_pool, void* v_pool, const int32_t* block_tables,
+                           const int32_t* positions, const float* rope_cos,
+                           const float* rope_sin, int batch, void* stream) {
+  return launch_append(pool, layer, k, v, k_pool, v_pool, block_tables, positions, rope_cos,
+                       rope_sin, true, batch, stream);
 }
 
 pkv_status pkv_decode_attention(pkv_pool_t pool, int layer, const void* q, const void* k_pool,
@@ -1268,6 +1442,24 @@ pkv_status pkv_append_attend(pkv_pool_t pool, int layer, const void* q, const vo
                              int batch, int num_splits, void* stream) {
   return launch_decode<true>(pool, layer, q, k, v, k_pool, v_pool, block_tables, seq_lens, out,
                              batch, num_splits, stream);
+}
+
+pkv_status pkv_decode_attention_rope(pkv_pool_t pool, int layer, const void* q,
+                                     const void* k_pool, const void* v_pool,
+                                     const int32_t* block_tables, const int32_t* seq_lens,
+                                     const float* rope_cos, const float* rope_sin, float* out,
+                                     int batch, int num_splits, void* stream) {
+  return launch_decode<false>(pool, layer, q, nullptr, nullptr, k_pool, v_pool, block_tables,
+                              seq_lens, out, batch, num_splits, stream, rope_cos, rope_sin, true);
+}
+
+pkv_status pkv_append_attend_rope(pkv_pool_t pool, int layer, const void* q, const void* k,
+                                  const void* v, void* k_pool, void* v_pool,
+                                  const int32_t* block_tables, const int32_t* seq_lens,
+                                  const float* rope_cos, const float* rope_sin, float* out,
+                                  int batch, int num_splits, void* stream) {
+  return launch_decode<true>(pool, layer, q, k, v, k_pool, v_pool, block_tables, seq_lens, out,
+                             batch, num_splits, stream, rope_cos, rope_sin, true);
 }
 
 pkv_status pkv_get_error(pkv_pool_t pool, void* stream) {

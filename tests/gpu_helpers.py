@@ -53,9 +53,11 @@ class DeviceState:
 
 
 def oracle_step(wl, host_k, host_v, q_bits, kn_bits, vn_bits, layers=None, threads=8,
-                table=None, lens=None):
+                table=None, lens=None, rope=None):
     """Oracle append then attention for each layer, on (copies of) host pools.
-    Returns (out [len(layers)][B][32][64], pool_k, pool_v after the appends)."""
+    rope = (cos, sin) FP32 tables: the key and the queries are rotated to
+    their position first. Returns (out [len(layers)][B][32][64], pool_k,
+    pool_v after the appends)."""
     orc = oracle.load()
     table = wl.block_tables if table is None else table
     lens = wl.seq_lens if lens is None else lens
@@ -66,11 +68,19 @@ def oracle_step(wl, host_k, host_v, q_bits, kn_bits, vn_bits, layers=None, threa
     outs = []
     positions = (lens - 1).astype(np.int32)
     for layer in layers:
-        st = orc.append(g, layer, kn_bits[layer].copy(), vn_bits[layer].copy(), kp, vp, table,
-                        positions)
-        assert st == oracle.OK, st
-        st, out = orc.decode_attention_mt(g, layer, q_bits[layer].copy(), kp, vp, table, lens,
-                                          threads)
+        if rope is None:
+            st = orc.append(g, layer, kn_bits[layer].copy(), vn_bits[layer].copy(), kp, vp,
+                            table, positions)
+            assert st == oracle.OK, st
+            st, out = orc.decode_attention_mt(g, layer, q_bits[layer].copy(), kp, vp, table,
+                                              lens, threads)
+        else:
+            st = orc.append_rope(g, layer, kn_bits[layer].copy(), vn_bits[layer].copy(), kp, vp,
+                                 table, positions, rope[0], rope[1])
+            assert st == oracle.OK, st
+            st, q64 = orc.rope_queries(q_bits[layer].copy(), positions, rope[0], rope[1])
+            assert st == oracle.OK, st
+            st, out = orc.decode_attention_q64(g, layer, q64, kp, vp, table, lens)
         assert st == oracle.OK, st
         outs.append(out)
     return np.stack(outs), kp, vp
