@@ -485,6 +485,108 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- admission scheduler (host)
+def scheduler_trace(n_steps, seed=W.BASE_SEED + 20):
+    """A continuous-batching trace at the 4 GiB pool: requests with prompts
+    log-uniform in [16, 1024] and allowances log-uniform in [16, 1024],
+    submitted two per step, some ending early; returns per-step actions."""
+    rng = np.random.default_rng(seed)
+    lo, hi = np.log(16), np.log(1024)
+    steps = []
+    for _ in range(n_steps):
+        subs = [(int(np.exp(rng.uniform(lo, hi))), int(np.exp(rng.uniform(lo, hi))))
+                for _ in range(2)]
+        steps.append((subs, float(rng.random())))
+    return steps
+
+
+def drive_scheduler(api, pool_pages, trace, max_batch=256):
+    """Runs the trace through a scheduler API (native or oracle); returns
+    (seconds of scheduler calls on the decode path, steps, batch sizes)."""
+    s = api["create"](pool_pages)
+    length, prefix = {}, {}
+    t_decode = 0.0
+    batches = []
+    for subs, early in trace:
+        for p, n in subs:
+            rid = api["submit"](s, p, n)
+            if rid is not None:
+                prefix[rid] = p + min(n, 2048 - p) - 1
+                length[rid] = p
+        admitted = api["admit"](s)
+        t0 = time.perf_counter()
+        batch = api["batch"](s)[:max_batch]
+        api["extend"](s, batch, [length[r] for r in batch])
+        api["tables"](s, batch, max_batch)
+        t_decode += time.perf_counter() - t0
+        batches.append(len(batch))
+        for i, rid in enumerate(batch):
+            if length[rid] >= prefix[rid] or (i == 0 and early < 0.05):
+                api["finish"](s, rid)
+                del length[rid]
+            else:
+                length[rid] += 1
+        del admitted
+    return t_decode, len(trace), batches
+
+
+def run_scheduler_bench(args):
+    import paged_kv_cache_210_gb300 as pkv
+    from paged_kv_cache_210_gb300 import build as lib_build
+    lib_build.build()
+    pkv.load()
+    pool_pages = W.pages_for_pool_mib(4096)
+
+    def native_submit(s, p, n):
+        try:
+            return pkv.pkv_sched_submit(s, p, n)
+        except pkv.PkvError:
+            return None
+    tables = {}
+
+    def native_tables(s, batch, max_batch):
+        out = tables.get(max_batch)
+        if out is None:
+            out = tables[max_batch] = np.empty((16, max_batch, 128), np.int32)
+        return pkv.pkv_sched_block_tables(s, batch, max_batch, 128, out, clear_tail=False)
+    native = {"create": lambda n: pkv.pkv_sched_create(n), "submit": native_submit,
+              "admit": pkv.pkv_sched_admit, "batch": pkv.pkv_sched_decode_batch,
+              "extend": pkv.pkv_sched_extend_batch, "finish": pkv.pkv_sched_finish,
+              "tables": native_tables}
+    trace = scheduler_trace(args.warmup + args.steps)
+    drive_scheduler(native, pool_pages, trace[:args.warmup])
+    t, n, batches = drive_scheduler(native, pool_pages, trace)
+    us = t / n * 1e6
+    line = {
+        "metric": "admission scheduler host time per decode step (batch, page growth, block "
+                  "tables)", "value": round(us, 3), "unit": "us/step", "n_gpus": 0,
+        "steps": n, "warmup": args.warmup, "higher_is_better": False, "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": "continuous batching at the 4 GiB pool (131072 pages), 16 layers, "
+                               "prompts and allowances log-uniform in [16, 1024], 2 submissions "
+                               "per step, decode batch capped at 256",
+                   "mean_batch": round(float(np.mean(batches)), 1),
+                   "max_batch": int(np.max(batches)),
+                   "tables_bytes_per_step": 16 * 256 * 128 * 4},
+    }
+    if not args.no_cpu_baseline:
+        from oracle import admission as A
+
+        def o_submit(s, p, n):
+            st, rid = s.submit(p, n)
+            return rid
+        orc = {"create": lambda n: A.AdmissionScheduler(n), "submit": o_submit,
+               "admit": lambda s: s.admit(), "batch": lambda s: s.decode_batch(),
+               "extend": lambda s, rs, ls: [s.extend(r, l) for r, l in zip(rs, ls)],
+               "finish": lambda s, r: s.finish(r),
+               "tables": lambda s, b, mb: s.block_tables(b, 128)}
+        sample = min(len(trace), 400)
+        to, no, _ = drive_scheduler(orc, pool_pages, trace[:sample])
+        line["cpu_baseline"] = {"value": round(to / no * 1e6, 3), "unit": "us/step", "cores": 1,
+                                "kind": "oracle", "sample": f"first {sample} steps of the trace"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -498,9 +600,14 @@ def main():
                     help="rotate the appended key and the queries inside the launches")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch")
+    ap.add_argument("--component", choices=["decode", "scheduler"], default="decode",
+                    help="scheduler: time the host admission scheduler instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.component == "scheduler":
+        run_scheduler_bench(args)
+        return
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -61,7 +61,8 @@ typedef enum {
   PKV_ERR_CUDA = 3,           /* a CUDA runtime call failed */
   PKV_ERR_UNSUPPORTED = 4,    /* geometry this library is not built for */
   PKV_ERR_DEVICE_TIMEOUT = 5, /* a bounded in-kernel wait gave up */
-  PKV_ERR_STATIC_LIMIT = 6    /* request larger than pkv_decode_attention_noalloc's scratch */
+  PKV_ERR_STATIC_LIMIT = 6,   /* request larger than pkv_decode_attention_noalloc's scratch */
+  PKV_ERR_REJECTED = 7        /* admission: a request's budget exceeds the whole pool */
 } pkv_status;
 
 /* Pool geometry. page_size, num_q_heads, num_kv_heads and head_dim must be

@@ -20,20 +20,36 @@ HEAD_DIM = 64
 MAX_SEQ_LEN = 2048
 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_OUT_OF_RANGE", 3: "PKV_ERR_CUDA",
-          4: "PKV_ERR_UNSUPPORTED", 5: "PKV_ERR_DEVICE_TIMEOUT", 6: "PKV_ERR_STATIC_LIMIT"}
+          4: "PKV_ERR_UNSUPPORTED", 5: "PKV_ERR_DEVICE_TIMEOUT", 6: "PKV_ERR_STATIC_LIMIT",
+          7: "PKV_ERR_REJECTED"}
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OUT_OF_RANGE, PKV_ERR_CUDA, PKV_ERR_UNSUPPORTED, \
-    PKV_ERR_DEVICE_TIMEOUT, PKV_ERR_STATIC_LIMIT = range(7)
+    PKV_ERR_DEVICE_TIMEOUT, PKV_ERR_STATIC_LIMIT, PKV_ERR_REJECTED = range(8)
 
 EXPORTED = ("pkv_pool_create", "pkv_pool_destroy", "pkv_append", "pkv_decode_attention",
             "pkv_append_attend", "pkv_append_rope", "pkv_decode_attention_rope",
             "pkv_append_attend_rope", "pkv_get_error", "pkv_decode_attention_noalloc",
-            "pkv_status_string")
+            "pkv_sched_budget", "pkv_sched_create", "pkv_sched_destroy", "pkv_sched_submit",
+            "pkv_sched_admit", "pkv_sched_extend", "pkv_sched_extend_batch", "pkv_sched_finish",
+            "pkv_sched_decode_batch",
+            "pkv_sched_block_tables", "pkv_sched_get_stats", "pkv_status_string")
 
 
 class PkvError(RuntimeError):
     def __init__(self, status, call):
         self.status = status
         super().__init__(f"{call}: {STATUS.get(status, status)}")
+
+
+class SchedConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "num_layers", "num_pages", "page_size", "max_seq_len", "static_batching")]
+
+
+class SchedStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "pool_pages", "submitted", "rejected", "admitted", "finished", "peak_active",
+        "largest_decode_batch", "peak_assigned_pages", "admission_waits", "free_pages",
+        "free_credits", "active", "waiting")]
 
 
 class PoolConfig(ctypes.Structure):
@@ -72,6 +88,18 @@ def load(path: str = None):
     lib.pkv_append_attend_rope.argtypes = [P, i, P, P, P, P, P, P, P, P, P, P, i, i, P]
     lib.pkv_get_error.argtypes = [P, P]
     lib.pkv_decode_attention_noalloc.argtypes = [i, P, P, P, P, P, P, i, i, i, i, i, i, P, P]
+    SC, SP = ctypes.POINTER(SchedConfig), ctypes.POINTER(ctypes.c_int)
+    lib.pkv_sched_budget.argtypes = [SC, i, i, SP, SP, ctypes.POINTER(ctypes.c_int64)]
+    lib.pkv_sched_create.argtypes = [SC, ctypes.POINTER(ctypes.c_void_p)]
+    lib.pkv_sched_destroy.argtypes = [P]
+    lib.pkv_sched_submit.argtypes = [P, i, i, SP]
+    lib.pkv_sched_admit.argtypes = [P, P, i, SP]
+    lib.pkv_sched_extend.argtypes = [P, i, i]
+    lib.pkv_sched_finish.argtypes = [P, i]
+    lib.pkv_sched_decode_batch.argtypes = [P, P, i, SP]
+    lib.pkv_sched_extend_batch.argtypes = [P, P, P, i]
+    lib.pkv_sched_block_tables.argtypes = [P, P, i, P, i, i, i]
+    lib.pkv_sched_get_stats.argtypes = [P, ctypes.POINTER(SchedStats)]
     lib.pkv_status_string.argtypes = [i]
     lib.pkv_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -223,3 +251,134 @@ def pkv_decode_attention_noalloc(layer, q, k_pool, v_pool, block_tables, seq_len
                                           int(max_seq_len), _batch(seq_lens, batch),
                                           int(num_splits), _addr(error_bits), _stream(stream))
     _check(st, "pkv_decode_attention_noalloc")
+
+
+# ---------------------------------------------------------------- admission scheduler (host)
+class Scheduler:
+    """Owns a pkv_sched_t: admission credits and lazy page assignment for the
+    shared pool (host only; see include/pkv_sched.h)."""
+
+    def __init__(self, handle, config, lib):
+        self.handle = handle
+        self.config = config
+        self._lib = lib
+
+    def close(self):
+        if self.handle:
+            _check(self._lib.pkv_sched_destroy(self.handle), "pkv_sched_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _sched_config(num_pages, num_layers, page_size, max_seq_len, static_batching):
+    return SchedConfig(int(num_layers), int(num_pages), int(page_size), int(max_seq_len),
+                       1 if static_batching else 0)
+
+
+def pkv_sched_budget(prompt_tokens, max_new_tokens, num_layers=16, page_size=PAGE_SIZE,
+                     max_seq_len=MAX_SEQ_LEN, lib=None):
+    """(allowed new tokens, largest processed prefix, budget in pages)."""
+    lib = lib or load()
+    cfg = _sched_config(1, num_layers, page_size, max_seq_len, False)
+    allowed, prefix, budget = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    _check(lib.pkv_sched_budget(ctypes.byref(cfg), int(prompt_tokens), int(max_new_tokens),
+                                ctypes.byref(allowed), ctypes.byref(prefix),
+                                ctypes.byref(budget)), "pkv_sched_budget")
+    return allowed.value, prefix.value, budget.value
+
+
+def pkv_sched_create(num_pages, num_layers=16, page_size=PAGE_SIZE, max_seq_len=MAX_SEQ_LEN,
+                     static_batching=False, lib=None) -> Scheduler:
+    lib = lib or load()
+    cfg = _sched_config(num_pages, num_layers, page_size, max_seq_len, static_batching)
+    handle = ctypes.c_void_p()
+    _check(lib.pkv_sched_create(ctypes.byref(cfg), ctypes.byref(handle)), "pkv_sched_create")
+    return Scheduler(handle.value, cfg, lib)
+
+
+def pkv_sched_destroy(sched: Scheduler):
+    sched.close()
+
+
+def pkv_sched_submit(sched: Scheduler, prompt_tokens, max_new_tokens) -> int:
+    """Queues a request and returns its id; PkvError(PKV_ERR_REJECTED) when
+    its budget exceeds the pool."""
+    rid = ctypes.c_int(-1)
+    _check(sched._lib.pkv_sched_submit(sched.handle, int(prompt_tokens), int(max_new_tokens),
+                                       ctypes.byref(rid)), "pkv_sched_submit")
+    return rid.value
+
+
+def pkv_sched_get_stats(sched: Scheduler) -> dict:
+    st = SchedStats()
+    _check(sched._lib.pkv_sched_get_stats(sched.handle, ctypes.byref(st)), "pkv_sched_get_stats")
+    return {name: getattr(st, name) for name, _ in SchedStats._fields_}
+
+
+def _id_buffer(n):
+    return (ctypes.c_int * max(1, n))()
+
+
+def pkv_sched_admit(sched: Scheduler) -> list:
+    """One admission pass; the admitted ids in order."""
+    cap = pkv_sched_get_stats(sched)["waiting"]
+    buf, count = _id_buffer(cap), ctypes.c_int()
+    _check(sched._lib.pkv_sched_admit(sched.handle, buf, int(cap), ctypes.byref(count)),
+           "pkv_sched_admit")
+    return list(buf[:count.value])
+
+
+def pkv_sched_extend(sched: Scheduler, request_id, length):
+    _check(sched._lib.pkv_sched_extend(sched.handle, int(request_id), int(length)),
+           "pkv_sched_extend")
+
+
+def pkv_sched_extend_batch(sched: Scheduler, ids, lengths):
+    """pkv_sched_extend for every (id, length) pair, in one call."""
+    import numpy as np
+    id_buf = np.ascontiguousarray(ids, dtype=np.intc)
+    len_buf = np.ascontiguousarray(lengths, dtype=np.intc)
+    if id_buf.shape != len_buf.shape or id_buf.ndim != 1:
+        raise ValueError("ids and lengths must be 1-D and of one length")
+    _check(sched._lib.pkv_sched_extend_batch(sched.handle, id_buf.ctypes.data, len_buf.ctypes.data,
+                                             int(id_buf.shape[0])), "pkv_sched_extend_batch")
+
+
+def pkv_sched_finish(sched: Scheduler, request_id):
+    _check(sched._lib.pkv_sched_finish(sched.handle, int(request_id)), "pkv_sched_finish")
+
+
+def pkv_sched_decode_batch(sched: Scheduler) -> list:
+    """The active requests in admission order (one decode step's batch)."""
+    cap = pkv_sched_get_stats(sched)["active"]
+    buf, count = _id_buffer(cap), ctypes.c_int()
+    _check(sched._lib.pkv_sched_decode_batch(sched.handle, buf, int(cap), ctypes.byref(count)),
+           "pkv_sched_decode_batch")
+    return list(buf[:count.value])
+
+
+def pkv_sched_block_tables(sched: Scheduler, ids, max_batch=None, max_pages=None, out=None,
+                           clear_tail=True):
+    """Host block tables int32 [num_layers][max_batch][max_pages] for the batch
+    `ids` (numpy array; `out` may supply a C-contiguous one to fill; with
+    clear_tail False, entries past each row's pages are left as they were)."""
+    import numpy as np
+    ids = np.ascontiguousarray(ids, dtype=np.intc).reshape(-1)
+    max_batch = len(ids) if max_batch is None else int(max_batch)
+    max_pages = sched.config.max_seq_len // sched.config.page_size if max_pages is None \
+        else int(max_pages)
+    shape = (sched.config.num_layers, max_batch, max_pages)
+    if out is None:
+        out = np.empty(shape, np.int32)
+    elif out.shape != shape or out.dtype != np.int32 or not out.flags.c_contiguous:
+        raise ValueError(f"out must be a C-contiguous int32 array of shape {shape}")
+    _check(sched._lib.pkv_sched_block_tables(sched.handle, ids.ctypes.data, len(ids),
+                                             out.ctypes.data_as(ctypes.c_void_p), max_batch,
+                                             max_pages, 1 if clear_tail else 0),
+           "pkv_sched_block_tables")
+    return out

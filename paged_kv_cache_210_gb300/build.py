@@ -1,9 +1,10 @@
 """Build step: compile the CUDA library for sm_103a into ``_build/libpkv.so``.
 
-One translation unit, compiled with nvcc for ``compute_103a``/``sm_103a``
-only, position-independent, with the CUDA runtime linked statically so the
-library loads beside any PyTorch build. Rebuilds when a source or the public
-header is newer than the library.
+The CUDA sources (``csrc/*.cu``, compiled for ``compute_103a``/``sm_103a``
+only) and the host-only C++ sources (``csrc/*.cpp``: the admission
+scheduler) go into one position-independent library with the CUDA runtime
+linked statically, so it loads beside any PyTorch build. Rebuilds when a
+source or a public header is newer than the library.
 """
 
 import glob
@@ -19,7 +20,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
 def sources():
-    return sorted(glob.glob(os.path.join(HERE, "csrc", "*.cu")))
+    return sorted(glob.glob(os.path.join(HERE, "csrc", "*.cu")) +
+                  glob.glob(os.path.join(HERE, "csrc", "*.cpp")))
 
 
 def _stale():
