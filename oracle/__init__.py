@@ -58,10 +58,13 @@ class Oracle:
         lib.pkv_oracle_append_rope.argtypes = [G, i, P, P, P, P, P, P, i, P, P, i]
         lib.pkv_oracle_rope_queries.argtypes = [P, i, i, i, P, P, P, i, P]
         lib.pkv_oracle_decode_attention_q64.argtypes = [G, i, P, P, P, P, P, i, P]
+        lib.pkv_oracle_prefill_fill.argtypes = [G, i, P, P, P, P, P, P, P, i]
+        lib.pkv_oracle_prefill_attention.argtypes = [G, i, P, P, P, P, P, P, i, P, i]
         for name in ("pkv_oracle_append", "pkv_oracle_decode_attention",
                      "pkv_oracle_decode_attention_mt", "pkv_oracle_decode_attention_split",
                      "pkv_oracle_contiguous_attention", "pkv_oracle_append_rope",
-                     "pkv_oracle_rope_queries", "pkv_oracle_decode_attention_q64"):
+                     "pkv_oracle_rope_queries", "pkv_oracle_decode_attention_q64",
+                     "pkv_oracle_prefill_fill", "pkv_oracle_prefill_attention"):
             getattr(lib, name).restype = ctypes.c_int
         self.lib = lib
         self.path = path
@@ -167,6 +170,34 @@ class Oracle:
                                                       _ptr(k_pool), _ptr(v_pool),
                                                       _ptr(block_tables), _ptr(seq_lens), B,
                                                       _ptr(out))
+        return st, out
+
+    def prefill_fill(self, g, layer, k, v, k_pool, v_pool, block_tables, cu_tokens, start_pos):
+        """Writes chunk tokens' K/V (k, v: [total][Hkv][D] BF16 patterns) into the pools."""
+        for a in (k, v, k_pool, v_pool):
+            _check(a, np.uint16)
+        for a in (block_tables, cu_tokens, start_pos):
+            _check(a, np.int32)
+        return self.lib.pkv_oracle_prefill_fill(ctypes.byref(g), layer, _ptr(k), _ptr(v),
+                                                _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                                _ptr(cu_tokens), _ptr(start_pos),
+                                                int(start_pos.shape[0]))
+
+    def prefill_attention(self, g, layer, q, k_pool, v_pool, block_tables, cu_tokens, start_pos,
+                          threads=8):
+        """Causal attention over the pages for every chunk token -> (status, out
+        [total][Hq][D] float64)."""
+        _check(q, np.uint16)
+        for a in (k_pool, v_pool):
+            _check(a, np.uint16)
+        for a in (block_tables, cu_tokens, start_pos):
+            _check(a, np.int32)
+        out = np.zeros((q.shape[0], g.num_q_heads, g.head_dim), np.float64)
+        st = self.lib.pkv_oracle_prefill_attention(ctypes.byref(g), layer, _ptr(q), _ptr(k_pool),
+                                                   _ptr(v_pool), _ptr(block_tables),
+                                                   _ptr(cu_tokens), _ptr(start_pos),
+                                                   int(start_pos.shape[0]), _ptr(out),
+                                                   int(threads))
         return st, out
 
     def contiguous_attention(self, q, k, v):

@@ -489,3 +489,103 @@ int pkv_oracle_decode_attention_q64(const pkv_oracle_geometry* g, int layer, con
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- prefill
+// Prefill over pages [samir-vllm: Build LLM Inference From Scratch in C++ and
+// CUDA, "Architecture walkthrough", Prefill and KV cache paragraphs; 6 Hours
+// of YouTube and 85 handtyped pages of notes on LLM Inference - Start here,
+// README feature list, dense causal prefill and shared BF16 KV page pool
+// bullets]: prefill fills the prompt's pages with its K/V, and each prompt
+// token attends causally to every token up to and including itself.
+//
+// Readings: a call carries, for each sequence b, a chunk of n_b tokens packed
+// at rows cu_tokens[b] .. cu_tokens[b+1] - 1 of q/k/v, at absolute positions
+// start_pos[b] .. start_pos[b] + n_b - 1 (start_pos > 0 continues a prompt
+// whose earlier tokens are already in the pages: chunked prefill); the fill
+// is the decode append applied to every token of the chunk; token i of the
+// chunk attends to keys 0 .. start_pos[b] + i, read through the block table
+// (so the fill of the same chunk comes first).
+extern "C" {
+
+int pkv_oracle_prefill_fill(const pkv_oracle_geometry* g, int layer, const uint16_t* k,
+                            const uint16_t* v, uint16_t* k_pool, uint16_t* v_pool,
+                            const int32_t* block_tables, const int32_t* cu_tokens,
+                            const int32_t* start_pos, int batch) {
+  if (!geometry_ok(g) || layer < 0 || layer >= g->num_layers || batch < 0 ||
+      batch > g->max_batch || !k || !v || !k_pool || !v_pool || !cu_tokens || !start_pos)
+    return ORACLE_BAD_ARG;
+  const int D = g->head_dim;
+  int status = ORACLE_OK;
+  for (int b = 0; b < batch; ++b) {
+    for (int row = cu_tokens[b]; row < cu_tokens[b + 1]; ++row) {
+      const int pos = start_pos[b] + (row - cu_tokens[b]);
+      const long page = pos < 0 ? -1 : physical_page(g, block_tables, layer, b, pos);
+      if (page < 0) {
+        status = ORACLE_OUT_OF_RANGE;
+        continue;
+      }
+      for (int h = 0; h < g->num_kv_heads; ++h)
+        for (int d = 0; d < D; ++d) {
+          const size_t src = (static_cast<size_t>(row) * g->num_kv_heads + h) * D + d;
+          k_pool[pool_index(g, page, h, pos % g->page_size, d)] = k[src];
+          v_pool[pool_index(g, page, h, pos % g->page_size, d)] = v[src];
+        }
+    }
+  }
+  return status;
+}
+
+// Causal attention of every chunk token over the pages: out [total][Hq][D]
+// (double), total = cu_tokens[batch]. (sequence, kv head) pairs are spread
+// over `nthreads` host threads; each output row is computed the same way
+// whatever the thread count.
+int pkv_oracle_prefill_attention(const pkv_oracle_geometry* g, int layer, const uint16_t* q,
+                                 const uint16_t* k_pool, const uint16_t* v_pool,
+                                 const int32_t* block_tables, const int32_t* cu_tokens,
+                                 const int32_t* start_pos, int batch, double* out,
+                                 int nthreads) {
+  if (!geometry_ok(g) || layer < 0 || layer >= g->num_layers || batch < 0 ||
+      batch > g->max_batch || !q || !k_pool || !v_pool || !cu_tokens || !start_pos || !out)
+    return ORACLE_BAD_ARG;
+  const int D = g->head_dim;
+  const int Hq = g->num_q_heads;
+  const int group = Hq / g->num_kv_heads;
+  const int units = batch * g->num_kv_heads;
+  if (nthreads < 1) nthreads = 1;
+  std::vector<int> status(static_cast<size_t>(nthreads), ORACLE_OK);
+  auto work = [&](int w) {
+    std::vector<double> k_rows, v_rows, q_row(D);
+    for (int u = w; u < units; u += nthreads) {
+      const int b = u / g->num_kv_heads;
+      const int kv = u % g->num_kv_heads;
+      const int n = cu_tokens[b + 1] - cu_tokens[b];
+      if (n == 0) continue;
+      const int len = start_pos[b] + n;          // keys the last token sees
+      if (start_pos[b] < 0 ||
+          !gather_head(g, k_pool, v_pool, block_tables, layer, b, kv, len, k_rows, v_rows)) {
+        status[w] = ORACLE_OUT_OF_RANGE;
+        continue;
+      }
+      for (int i = 0; i < n; ++i) {
+        const size_t row = static_cast<size_t>(cu_tokens[b] + i);
+        for (int h = kv * group; h < (kv + 1) * group; ++h) {
+          for (int d = 0; d < D; ++d) q_row[d] = bf16_bits_to_double(q[(row * Hq + h) * D + d]);
+          attend_row(q_row.data(), k_rows.data(), v_rows.data(), start_pos[b] + i + 1, D,
+                     out + (row * Hq + h) * D, nullptr, nullptr);
+        }
+      }
+    }
+  };
+  if (nthreads == 1) {
+    work(0);
+  } else {
+    std::vector<std::thread> pool;
+    for (int w = 0; w < nthreads; ++w) pool.emplace_back(work, w);
+    for (auto& t : pool) t.join();
+  }
+  for (int s : status)
+    if (s != ORACLE_OK) return s;
+  return ORACLE_OK;
+}
+
+}  // extern "C"

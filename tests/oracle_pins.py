@@ -398,9 +398,110 @@ def pin_rope_keeps_pair_norms_and_relative_scores(orc):
     np.testing.assert_allclose(d1, d0, rtol=0, atol=2e-4)
 
 
+# ---------------------------------------------------------------- prefill
+def _prefill_state(chunk_lens, start_pos, seed):
+    wl = W.prefill(chunk_lens, start_pos, num_layers=1, seed=seed)
+    kp, vp = (bits(t) for t in wl.pools("cpu", "nan"))
+    return wl, kp, vp, bits(wl.q()[0]), bits(wl.k()[0]), bits(wl.v()[0])
+
+
+def _prefill_run(orc, wl, kp, vp, q, k, v):
+    g = oracle_pkg.geometry(1, wl.num_pages, wl.batch)
+    assert orc.prefill_fill(g, 0, k, v, kp, vp, wl.block_tables, wl.cu_tokens,
+                            wl.start_pos) == oracle_pkg.OK
+    st, out = orc.prefill_attention(g, 0, q, kp, vp, wl.block_tables, wl.cu_tokens,
+                                    wl.start_pos, threads=3)
+    assert st == oracle_pkg.OK
+    return out
+
+
+def pin_prefill_matches_causal_sdpa(orc):
+    """Against torch float64 scaled_dot_product_attention with a causal mask
+    offset by the chunk's start, on K/V gathered by the test's own reading of
+    the layout (GQA expanded); chunks starting at 0 and mid-prompt."""
+    chunk, start = [20, 37, 9], [0, 5, 30]
+    wl, kp, vp, q, k, v = _prefill_state(chunk, start, 601)
+    before_k = kp.copy()
+    out = _prefill_run(orc, wl, kp, vp, q, k, v)
+    cu = wl.cu_tokens
+    for b in range(wl.batch):
+        n, s0 = int(chunk[b]), int(start[b])
+        L = s0 + n
+        rows = wl.block_tables[0, b]
+        t = np.arange(L)
+        kk = bits_to_f64(kp[rows[t // P], :, t % P, :])      # [L][Hkv][D]
+        vv = bits_to_f64(vp[rows[t // P], :, t % P, :])
+        # the chunk's rows come from k/v, the earlier ones were already cached
+        np.testing.assert_array_equal(kp[rows[t[s0:] // P], :, t[s0:] % P, :],
+                                      k[cu[b]:cu[b + 1]])
+        np.testing.assert_array_equal(kp[rows[t[:s0] // P], :, t[:s0] % P, :],
+                                      before_k[rows[t[:s0] // P], :, t[:s0] % P, :])
+        qq = torch.from_numpy(bits_to_f64(q[cu[b]:cu[b + 1]])).permute(1, 0, 2)   # [Hq][n][D]
+        kt = torch.from_numpy(kk).permute(1, 0, 2).repeat_interleave(HQ // HKV, dim=0)
+        vt = torch.from_numpy(vv).permute(1, 0, 2).repeat_interleave(HQ // HKV, dim=0)
+        mask = torch.arange(L)[None, :] <= (s0 + torch.arange(n))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qq, kt, vt, attn_mask=mask)
+        np.testing.assert_allclose(out[cu[b]:cu[b + 1]], ref.permute(1, 0, 2).numpy(),
+                                   rtol=0, atol=1e-12)
+
+
+def pin_prefill_first_token_returns_its_v_row(orc):
+    wl, kp, vp, q, k, v = _prefill_state([16, 1], [0, 0], 602)
+    out = _prefill_run(orc, wl, kp, vp, q, k, v)
+    for b, row in ((0, 0), (1, 16)):
+        for h in range(HQ):
+            np.testing.assert_array_equal(out[row, h], bits_to_f64(v[row, h // (HQ // HKV)]))
+
+
+def pin_prefill_chunks_compose(orc):
+    """Prefilling [0, a) then [a, n) gives the rows of a single [0, n) call,
+    bit for bit, and the last token equals decode attention at length n."""
+    n, a = 45, 17
+    whole, kp, vp, q, k, v = _prefill_state([n], [0], 603)
+    out_whole = _prefill_run(orc, whole, kp.copy(), vp.copy(), q, k, v)
+    parts = []
+    kp2, vp2 = kp.copy(), vp.copy()
+    for s0, s1 in ((0, a), (a, n)):
+        wl = W.PrefillWorkload("part", 1, whole.num_pages, np.array([s0], np.int32),
+                               np.array([s1 - s0], np.int32), whole.block_tables, whole.seed)
+        parts.append(_prefill_run(orc, wl, kp2, vp2, q[s0:s1].copy(), k[s0:s1].copy(),
+                                  v[s0:s1].copy()))
+    np.testing.assert_array_equal(np.concatenate(parts), out_whole)
+    g = oracle_pkg.geometry(1, whole.num_pages, 1)
+    st, dec, _, _ = orc.decode_attention(g, 0, q[n - 1:n].copy(), kp2, vp2, whole.block_tables,
+                                         np.array([n], np.int32))
+    assert st == oracle_pkg.OK
+    np.testing.assert_array_equal(dec[0], out_whole[n - 1])
+
+
+def pin_prefill_fill_closed_form(orc):
+    """Every chunk row lands at page table[(s + i) // 16], slot (s + i) % 16,
+    and nothing else changes; a position past the table is reported."""
+    wl, kp, vp, q, k, v = _prefill_state([33, 4], [3, 60], 604)
+    kp0, vp0 = kp.copy(), vp.copy()
+    g = oracle_pkg.geometry(1, wl.num_pages, wl.batch)
+    assert orc.prefill_fill(g, 0, k, v, kp, vp, wl.block_tables, wl.cu_tokens,
+                            wl.start_pos) == oracle_pkg.OK
+    ek, ev = kp0.copy(), vp0.copy()
+    for b in range(wl.batch):
+        for i in range(int(wl.chunk_lens[b])):
+            pos = int(wl.start_pos[b]) + i
+            row = int(wl.cu_tokens[b]) + i
+            page = wl.block_tables[0, b, pos // P]
+            ek[page, :, pos % P] = k[row]
+            ev[page, :, pos % P] = v[row]
+    assert np.array_equal(kp, ek) and np.array_equal(vp, ev)
+    bad = wl.start_pos.copy()
+    bad[1] = 2048 - 2                      # runs past the 128-page table
+    assert orc.prefill_fill(g, 0, k, v, kp, vp, wl.block_tables, wl.cu_tokens,
+                            bad) == oracle_pkg.OUT_OF_RANGE
+
+
 ALL_PINS = [pin_golden_closed_form, pin_pool_geometry_facts, pin_single_token_returns_v_row,
             pin_zero_query_gives_mean_of_v, pin_weights_sum_to_one, pin_dominant_key,
             pin_paged_equals_contiguous, pin_contiguous_matches_sdpa, pin_paged_matches_sdpa,
             pin_split_equals_unsplit, pin_mt_matches_single_thread, pin_append_closed_form,
             pin_append_rejects_out_of_range, pin_rope_zero_angle_is_identity,
-            pin_rope_quarter_turn_swaps_halves, pin_rope_keeps_pair_norms_and_relative_scores]
+            pin_rope_quarter_turn_swaps_halves, pin_rope_keeps_pair_norms_and_relative_scores,
+            pin_prefill_matches_causal_sdpa, pin_prefill_first_token_returns_its_v_row,
+            pin_prefill_chunks_compose, pin_prefill_fill_closed_form]

@@ -54,6 +54,16 @@ MUTATIONS = [
      "size_t src = (static_cast<size_t>(kv) * len + t) * D + d;", 0),
     ("threaded variant skips sequences", "for (int b = w; b < batch; b += nthreads)",
      "for (int b = w + 1; b < batch; b += nthreads)", 0),
+    ("prefill token does not attend itself", "start_pos[b] + i + 1, D,", "start_pos[b] + i, D,",
+     0),
+    ("prefill fill ignores the chunk start",
+     "const int pos = start_pos[b] + (row - cu_tokens[b]);",
+     "const int pos = row - cu_tokens[b];", 0),
+    ("prefill reads the next sequence's queries",
+     "const size_t row = static_cast<size_t>(cu_tokens[b] + i);",
+     "const size_t row = static_cast<size_t>(cu_tokens[b] + i + (b + 1 < batch ? 1 : 0));", 0),
+    ("prefill gathers one key too few", "const int len = start_pos[b] + n;          // keys",
+     "const int len = start_pos[b] + n - 1;      // keys", 0),
     ("key rotation sign flipped", "rotated[row + i] = float_to_bf16_rne(xc - ys);",
      "rotated[row + i] = float_to_bf16_rne(xc + ys);", 0),
     ("key rotation pairs neighbours", "const float y = bf16_bits_to_float(k_new[row + i + half]);",

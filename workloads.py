@@ -27,6 +27,12 @@ Workloads (seed 210 + index, one sub-stream per quantity):
   4 ragged    16 layers, batch 256, lengths uniform in [1, 2048] with
               {1, 16, 32, 2048, 17, 1024} forced first, pool sized to fit, K x 4
   5 long      16 layers, batch 1 or 4 at 2,048, 1 GiB pool, scattered pages
+
+Prefill chunks (PrefillWorkload): for each sequence, a chunk of n_b prompt
+tokens at positions start_b .. start_b + n_b - 1, packed token-major into
+q [L][T][32][64] and k/v [L][T][8][64] (T = sum n_b, rows cu_tokens[b] ..
+cu_tokens[b+1] - 1); positions < start_b are already cached (earlier chunks);
+the chunk's own slots hold the fill value until the prefill writes them.
 """
 
 from dataclasses import dataclass, field
@@ -246,3 +252,81 @@ def custom(seq_lens, num_layers=1, num_pages=None, seed=BASE_SEED + 9, k_scale=1
         num_pages = max(1, num_pages)
     table = assign_pages(lens, num_layers, num_pages, _rng(seed, "pages"), hole_every)
     return Workload(name, num_layers, num_pages, lens, table, seed, k_scale=k_scale)
+
+
+@dataclass
+class PrefillWorkload:
+    name: str
+    num_layers: int
+    num_pages: int
+    start_pos: np.ndarray         # int32 [B]: position of each chunk's first token
+    chunk_lens: np.ndarray        # int32 [B]: tokens in each chunk
+    block_tables: np.ndarray      # int32 [L][B][128], covering start + n tokens
+    seed: int
+    note: str = ""
+
+    @property
+    def batch(self) -> int:
+        return int(self.chunk_lens.shape[0])
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.chunk_lens.sum())
+
+    @property
+    def cu_tokens(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.chunk_lens)]).astype(np.int32)
+
+    @property
+    def seq_lens(self) -> np.ndarray:
+        """Length of each sequence once the chunk is in the cache."""
+        return (self.start_pos + self.chunk_lens).astype(np.int32)
+
+    def _normal(self, shape, stream, device):
+        gen = torch.Generator(device=device)
+        gen.manual_seed(self.seed * 1000 + _STREAMS[stream])
+        return _bf16(torch.randn(shape, generator=gen, device=device, dtype=torch.float32))
+
+    def q(self, device="cpu") -> torch.Tensor:
+        """bf16 [L][T][32][64]."""
+        return self._normal((self.num_layers, self.total_tokens, NUM_Q_HEADS, HEAD_DIM), "q",
+                            device)
+
+    def k(self, device="cpu") -> torch.Tensor:
+        """bf16 [L][T][8][64]: the chunk tokens' keys."""
+        return self._normal((self.num_layers, self.total_tokens, NUM_KV_HEADS, HEAD_DIM),
+                            "k_new", device)
+
+    def v(self, device="cpu") -> torch.Tensor:
+        return self._normal((self.num_layers, self.total_tokens, NUM_KV_HEADS, HEAD_DIM),
+                            "v_new", device)
+
+    def pools(self, device="cpu", fill="nan"):
+        """Pools holding positions < start_pos (the earlier chunks); every
+        other slot holds `fill`."""
+        lens = self.start_pos.astype(np.int32) + 1   # a Workload caches seq_len - 1 tokens
+        base = Workload(self.name, self.num_layers, self.num_pages, lens, self.block_tables,
+                        self.seed)
+        return base.pools(device, fill)
+
+
+def prefill(chunk_lens, start_pos=None, num_layers=1, num_pages=None, seed=BASE_SEED + 30,
+            hole_every=0, name="prefill") -> PrefillWorkload:
+    """Chunks of the given lengths; the pool defaults to exactly the pages the
+    sequences need once their chunks are in."""
+    n = np.asarray(chunk_lens, np.int32)
+    start = np.zeros_like(n) if start_pos is None else np.asarray(start_pos, np.int32)
+    total = (start + n).astype(np.int64)
+    need = int(((total + PAGE_SIZE - 1) // PAGE_SIZE).sum()) * num_layers
+    if num_pages is None:
+        num_pages = need if not hole_every else -(-need * hole_every // (hole_every - 1)) + 1
+        num_pages = max(1, num_pages)
+    table = assign_pages(total, num_layers, num_pages, _rng(seed, "pages"), hole_every)
+    return PrefillWorkload(name, num_layers, num_pages, start, n, table, seed)
+
+
+def prefill_prompt(prompt_len=2048, num_layers=16) -> PrefillWorkload:
+    """One prompt prefilled at once, the pages' engine's way (one prompt at a
+    time between decode iterations): 16 layers, 2,048 tokens, 128 MiB pool."""
+    return prefill([prompt_len], num_layers=num_layers, num_pages=pages_for_pool_mib(128),
+                   seed=BASE_SEED + 6, name=f"prefill-{prompt_len}")
