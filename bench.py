@@ -82,7 +82,8 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for rel in ("paged_kv_cache_210_gb300/csrc/pkv.cu", "include/pkv.h"):
+    for rel in ("paged_kv_cache_210_gb300/csrc/pkv.cu", "paged_kv_cache_210_gb300/csrc/pool_internal.h",
+                "include/pkv.h"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

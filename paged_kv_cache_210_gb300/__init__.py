@@ -31,7 +31,8 @@ EXPORTED = ("pkv_pool_create", "pkv_pool_destroy", "pkv_append", "pkv_decode_att
             "pkv_sched_budget", "pkv_sched_create", "pkv_sched_destroy", "pkv_sched_submit",
             "pkv_sched_admit", "pkv_sched_extend", "pkv_sched_extend_batch", "pkv_sched_finish",
             "pkv_sched_decode_batch",
-            "pkv_sched_block_tables", "pkv_sched_get_stats", "pkv_status_string")
+            "pkv_sched_block_tables", "pkv_sched_get_stats", "pkv_prefill_fill",
+            "pkv_prefill_attention", "pkv_prefill", "pkv_status_string")
 
 
 class PkvError(RuntimeError):
@@ -100,6 +101,9 @@ def load(path: str = None):
     lib.pkv_sched_extend_batch.argtypes = [P, P, P, i]
     lib.pkv_sched_block_tables.argtypes = [P, P, i, P, i, i, i]
     lib.pkv_sched_get_stats.argtypes = [P, ctypes.POINTER(SchedStats)]
+    lib.pkv_prefill_fill.argtypes = [P, i, P, P, P, P, P, P, P, i, i, i, P]
+    lib.pkv_prefill_attention.argtypes = [P, i, P, P, P, P, P, P, P, i, i, i, P]
+    lib.pkv_prefill.argtypes = [P, i, P, P, P, P, P, P, P, P, P, i, i, i, P]
     lib.pkv_status_string.argtypes = [i]
     lib.pkv_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -251,6 +255,43 @@ def pkv_decode_attention_noalloc(layer, q, k_pool, v_pool, block_tables, seq_len
                                           int(max_seq_len), _batch(seq_lens, batch),
                                           int(num_splits), _addr(error_bits), _stream(stream))
     _check(st, "pkv_decode_attention_noalloc")
+
+
+# ---------------------------------------------------------------- prefill
+def pkv_prefill_fill(pool: Pool, layer, k, v, k_pool, v_pool, block_tables, cu_tokens, start_pos,
+                     max_chunk_tokens, batch=None, total_tokens=None, stream=None):
+    """Writes chunk tokens' K/V (bf16 [T][8][64]) into their pages."""
+    batch = int(start_pos.shape[0]) if batch is None else int(batch)
+    total = int(k.shape[0]) if total_tokens is None else int(total_tokens)
+    st = pool._lib.pkv_prefill_fill(pool.handle, int(layer), _addr(k), _addr(v), _addr(k_pool),
+                                    _addr(v_pool), _addr(block_tables), _addr(cu_tokens),
+                                    _addr(start_pos), batch, total, int(max_chunk_tokens),
+                                    _stream(stream))
+    _check(st, "pkv_prefill_fill")
+
+
+def pkv_prefill_attention(pool: Pool, layer, q, k_pool, v_pool, block_tables, cu_tokens, start_pos,
+                          out, max_chunk_tokens, batch=None, total_tokens=None, stream=None):
+    """Causal attention of chunk tokens (q bf16 [T][32][64]) over the pages; out fp32."""
+    batch = int(start_pos.shape[0]) if batch is None else int(batch)
+    total = int(q.shape[0]) if total_tokens is None else int(total_tokens)
+    st = pool._lib.pkv_prefill_attention(pool.handle, int(layer), _addr(q), _addr(k_pool),
+                                         _addr(v_pool), _addr(block_tables), _addr(cu_tokens),
+                                         _addr(start_pos), _addr(out), batch, total,
+                                         int(max_chunk_tokens), _stream(stream))
+    _check(st, "pkv_prefill_attention")
+
+
+def pkv_prefill(pool: Pool, layer, q, k, v, k_pool, v_pool, block_tables, cu_tokens, start_pos,
+                out, max_chunk_tokens, batch=None, total_tokens=None, stream=None):
+    """pkv_prefill_fill then pkv_prefill_attention."""
+    batch = int(start_pos.shape[0]) if batch is None else int(batch)
+    total = int(q.shape[0]) if total_tokens is None else int(total_tokens)
+    st = pool._lib.pkv_prefill(pool.handle, int(layer), _addr(q), _addr(k), _addr(v),
+                               _addr(k_pool), _addr(v_pool), _addr(block_tables),
+                               _addr(cu_tokens), _addr(start_pos), _addr(out), batch, total,
+                               int(max_chunk_tokens), _stream(stream))
+    _check(st, "pkv_prefill")
 
 
 # ---------------------------------------------------------------- admission scheduler (host)

@@ -28,7 +28,8 @@ def _stale():
     if not os.path.exists(LIBRARY):
         return True
     newest = max(os.path.getmtime(p) for p in sources() + glob.glob(os.path.join(INCLUDE, "*.h"))
-                 + glob.glob(os.path.join(HERE, "csrc", "*.cuh")))
+                 + glob.glob(os.path.join(HERE, "csrc", "*.cuh"))
+                 + glob.glob(os.path.join(HERE, "csrc", "*.h")))
     return os.path.getmtime(LIBRARY) < newest
 
 

@@ -38,6 +38,7 @@
 #include <mutex>
 
 #include "pkv.h"
+#include "pool_internal.h"
 
 namespace {
 
@@ -66,10 +67,10 @@ constexpr int kMaxSplitsLimit = 128;
 constexpr int kMaxClusterSize = 16;                // non-portable cluster size limit
 
 // device error flag bits
-constexpr int kErrPage = 1;
-constexpr int kErrPosition = 2;
-constexpr int kErrSeqLen = 4;
-constexpr int kErrTimeout = 8;
+constexpr int kErrPage = PKV_DEV_ERR_PAGE;
+constexpr int kErrPosition = PKV_DEV_ERR_POSITION;
+constexpr int kErrSeqLen = PKV_DEV_ERR_SEQ_LEN;
+constexpr int kErrTimeout = PKV_DEV_ERR_TIMEOUT;
 
 // about two seconds at the maximum SM clock
 constexpr long long kWaitCycles = 4000000000LL;
@@ -990,25 +991,12 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
 
 // ================================================================= host side
 
-struct pkv_pool {
-  pkv_pool_config cfg;
-  int device;
-  int num_sms;
-  int blocks_per_sm;           // resident decode blocks per SM (occupancy API)
-  int cluster_blocks_per_sm;   // the same for the cluster-merge kernel
-  int max_cluster;     // largest cluster size (power of two <= 16) the device schedules
-  float* part_o;     // [2][max_batch][32][max_splits][64]
-  float2* part_ml;   // [2][max_batch][32][max_splits]
-  int* tickets;      // [2][max_batch][8]
-  int* err;          // sticky error bits
-};
-
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The two kernel shapes: ticket merge (4 warps, 3 stages) and cluster merge
-// (8 warps, 2 stages, plus the leader's inbox).
+// The two kernel shapes: ticket merge and cluster merge (4 warps, 3 stages
+// each; the cluster kernel adds the leader's inbox).
 template <bool kFused, bool kRope = false>
 constexpr auto ticket_kernel = decode_kernel<kFused, false, kTicketWarps, kTicketStages, kRope>;
 template <bool kFused, bool kRope = false>

@@ -1,0 +1,32 @@
+// Internal to libpkv: the pool handle behind pkv_pool_t and the device error
+// bits, shared by the decode (pkv.cu) and prefill (prefill.cu) sources.
+#ifndef PKV_POOL_INTERNAL_H
+#define PKV_POOL_INTERNAL_H
+
+#include <cuda_runtime.h>
+
+#include "pkv.h"
+
+struct pkv_pool {
+  pkv_pool_config cfg;
+  int device;
+  int num_sms;
+  int blocks_per_sm;           // resident decode blocks per SM (occupancy API)
+  int cluster_blocks_per_sm;   // the same for the cluster-merge kernel
+  int max_cluster;     // largest cluster size (power of two <= 16) the device schedules
+  float* part_o;     // [2][max_batch][32][max_splits][64]
+  float2* part_ml;   // [2][max_batch][32][max_splits]
+  int* tickets;      // [2][max_batch][8]
+  int* err;          // sticky error bits (PKV_DEV_ERR_*)
+};
+
+// Sticky device error bits; pkv_get_error maps TIMEOUT to
+// PKV_ERR_DEVICE_TIMEOUT and the others to PKV_ERR_OUT_OF_RANGE.
+enum : int {
+  PKV_DEV_ERR_PAGE = 1,       // a page id outside [0, num_pages)
+  PKV_DEV_ERR_POSITION = 2,   // a position outside [0, max_seq_len)
+  PKV_DEV_ERR_SEQ_LEN = 4,    // a length outside [1, max_seq_len]
+  PKV_DEV_ERR_TIMEOUT = 8,    // a bounded wait gave up
+};
+
+#endif  // PKV_POOL_INTERNAL_H
