@@ -588,6 +588,153 @@ def run_scheduler_bench(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- prefill over pages
+def prefill_flops(wl):
+    """Algorithmic FLOPs of one prefill attention launch: for every chunk
+    token at position p and each of the 32 query heads, (p + 1) keys of
+    64-dim dot products and (p + 1) value rows of 64: 4 * 64 * (p + 1)."""
+    total = 0
+    for s0, n in zip(wl.start_pos.tolist(), wl.chunk_lens.tolist()):
+        keys = n * s0 + n * (n + 1) // 2
+        total += keys
+    return total * W.NUM_Q_HEADS * W.HEAD_DIM * 4
+
+
+def run_prefill_bench(args):
+    import paged_kv_cache_210_gb300 as pkv
+    from paged_kv_cache_210_gb300 import build as lib_build
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib_build.build()
+    pkv.load()
+    wl = W.prefill_prompt(args.prompt_len)
+    L, T = wl.num_layers, wl.total_tokens
+    k_pool, v_pool = wl.pools(dev, "zero")
+    q, k, v = wl.q(dev), wl.k(dev), wl.v(dev)
+    table = torch.from_numpy(wl.block_tables).to(dev)
+    cu = torch.from_numpy(wl.cu_tokens).to(dev)
+    start = torch.from_numpy(wl.start_pos).to(dev)
+    out = torch.zeros((L, T, W.NUM_Q_HEADS, W.HEAD_DIM), device=dev)
+    pool = pkv.pkv_pool_create(L, wl.num_pages, wl.batch)
+    max_chunk = int(wl.chunk_lens.max())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    made = [make_event() for _ in range(2 * L + 3)]
+    external = all(e[1] for e in made)
+    marks = [e[0] for e in made[:2 * L + 1]]
+    t0, t1 = made[2 * L + 1][0], made[2 * L + 2][0]
+
+    def step(events=None):
+        s = torch.cuda.current_stream()
+        if events:
+            events[0].record(s)
+        for layer in range(L):
+            pkv.pkv_prefill_fill(pool, layer, k[layer], v[layer], k_pool, v_pool, table, cu, start,
+                                 max_chunk, stream=s)
+            if events and len(events) > 2:
+                events[2 * layer + 1].record(s)
+            pkv.pkv_prefill_attention(pool, layer, q[layer], k_pool, v_pool, table, cu, start,
+                                      out[layer], max_chunk, stream=s)
+            if events and len(events) > 2:
+                events[2 * layer + 2].record(s)
+        if events and len(events) == 2:
+            events[1].record(s)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    graph, per_launch = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step([t0, t1] if external else None)
+    with torch.cuda.graph(per_launch, stream=stream):
+        step(marks if external else None)
+
+    def replay(g, a, b):
+        with torch.cuda.stream(stream):
+            flush_buf.sum()
+            if external:
+                g.replay()
+            else:
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+
+    for _ in range(args.warmup):
+        replay(graph, t0, t1)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev)
+    time.sleep(0.3)
+    step_ms = []
+    for _ in range(args.steps):
+        replay(graph, t0, t1)
+        stream.synchronize()
+        step_ms.append(t0.elapsed_time(t1))
+    clocks = sampler.stop()
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    fill_ms, attn_ms = [], []
+    if external:
+        for _ in range(max(3, min(args.steps, 100))):
+            replay(per_launch, marks[0], marks[-1])
+            stream.synchronize()
+            for layer in range(L):
+                fill_ms.append(marks[2 * layer].elapsed_time(marks[2 * layer + 1]))
+                attn_ms.append(marks[2 * layer + 1].elapsed_time(marks[2 * layer + 2]))
+    ms = float(np.mean(step_ms))
+    flops = prefill_flops(wl)
+    peaks, kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    attn_launch_ms = float(np.mean(attn_ms)) if attn_ms else ms / L
+    achieved = flops / (attn_launch_ms * 1e-3) / 1e12
+    line = {
+        "metric": "prefill over pages: causal attention TFLOP/s (algorithmic) and prompt "
+                  "tokens/s", "value": round(flops * L / (ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 operands, f32 accumulate", "data": "synthetic",
+        "config": {"workload": f"prefill-{args.prompt_len}: one {args.prompt_len}-token prompt, "
+                               "16 layers, 32q/8kv heads, head_dim 64, 128 MiB pool, shuffled "
+                               "pages; per layer the page fill then causal attention over the "
+                               "pages",
+                   "l2": "flushed before every step (read of a buffer twice the L2 size)",
+                   "flops_per_layer": flops},
+        "prompt_tokens_per_s": round(T / (ms * 1e-3), 1),
+        "step_ms_p10_p50_p90": [round(float(np.percentile(step_ms, p)), 4) for p in (10, 50, 90)],
+        "clocks": clocks,
+        "gpu_launches": 2 * L * args.steps,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{kind} cuBLAS bf16 burst (MEASURED_PEAKS bf16_tflops)",
+                     "traffic": None, "kernel": "prefill_attention_kernel",
+                     "per_launch_ms": round(attn_launch_ms, 5),
+                     "fill_per_launch_ms": round(float(np.mean(fill_ms)), 5) if fill_ms else None},
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        orc = oracle.load()
+        g = oracle.geometry(L, wl.num_pages, wl.batch)
+        kp, vp = (t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+                  for t in wl.pools("cpu", "zero"))
+
+        def b16(t):
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+        qc, kc, vc = b16(wl.q()[0]), b16(wl.k()[0]), b16(wl.v()[0])
+        threads = cpu_threads()
+        tt = time.perf_counter()
+        assert orc.prefill_fill(g, 0, kc, vc, kp, vp, wl.block_tables, wl.cu_tokens,
+                                wl.start_pos) == oracle.OK
+        st, _ = orc.prefill_attention(g, 0, qc, kp, vp, wl.block_tables, wl.cu_tokens,
+                                      wl.start_pos, threads=threads)
+        dt = time.perf_counter() - tt
+        assert st == oracle.OK
+        line["cpu_baseline"] = {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s",
+                                "cores": min(threads, wl.batch * W.NUM_KV_HEADS),
+                                "kind": "oracle",
+                                "sample": f"1 of {L} layers (fill + attention), {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -601,13 +748,17 @@ def main():
                     help="rotate the appended key and the queries inside the launches")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch")
-    ap.add_argument("--component", choices=["decode", "scheduler"], default="decode",
-                    help="scheduler: time the host admission scheduler instead")
+    ap.add_argument("--component", choices=["decode", "scheduler", "prefill"], default="decode",
+                    help="scheduler: the host admission scheduler; prefill: prefill over pages")
+    ap.add_argument("--prompt-len", type=int, default=2048, help="prefill prompt length")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.component == "scheduler":
         run_scheduler_bench(args)
+        return
+    if args.component == "prefill":
+        run_prefill_bench(args)
         return
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
