@@ -12,25 +12,38 @@
 // attention; here it reads keys through the block table, so a chunk can
 // continue a prompt whose earlier pages are already cached.
 //
-// Attention kernel, one CTA of 4 warps per (sequence, kv head, 32-token
-// query tile):
+// Attention kernel, one CTA per (sequence, kv head, 32-token query tile),
+// warp-specialised:
 //  * the 128 rows of the MMA are the tile's 32 tokens x the 4 query heads
 //    of the kv head (row = token * 4 + head), so every K/V page tile is
 //    shared by the group, as in decode;
-//  * Q (16 KiB) and per step 4 pages of K and of V (64 keys, 8 KiB each)
-//    arrive by TMA tensor copies (cp.async.bulk.tensor) with the 128-byte
-//    swizzle, K/V double-buffered; a page's tile is addressed by its id in
-//    the block table, so nothing is gathered into a contiguous buffer;
-//  * S = Q K^T (M 128, N 64, K 64) and the value product O_step = P V
-//    (M 128, N 64, K 64) run as tcgen05.mma kind::f16 with FP32
-//    accumulators in tensor memory, issued by one thread and completed on
-//    mbarriers through tcgen05.commit;
-//  * each thread owns one row: it reads its S row from tensor memory,
-//    keeps the running max and sum (online softmax in base 2), writes the
-//    probabilities to shared memory as a BF16 high part and a BF16 low
-//    part (two MMAs, so P carries ~16 significant bits), and accumulates
-//    O_step into 64 FP32 registers with the rescale factor;
+//  * a loader warp brings Q (16 KiB) and per step 4 pages of K and of V
+//    (64 keys, 8 KiB each) by TMA tensor copies (cp.async.bulk.tensor) with
+//    the 128-byte swizzle, one page per lane, K in a 4-stage and V in a
+//    3-stage ring, so loads run two to three steps ahead; a page's tile is
+//    addressed by its id in the block table, nothing is gathered into a
+//    contiguous buffer;
+//  * an MMA warp (one thread) issues S = Q K^T (M 128, N 64, K 64) one step
+//    ahead into a double-buffered tensor-memory tile and O += P V (M 128,
+//    N 64, K 64) into an FP32 accumulator that stays in tensor memory, as
+//    tcgen05.mma kind::f16 completed on mbarriers through tcgen05.commit,
+//    which also tell the loader when a stage is free;
+//  * eight softmax warps, two per tensor-memory lane quarter: each thread
+//    reads its row's 64 scores (so both halves agree on the row max) and
+//    handles 32 of them: online softmax in base 2, where the max used for
+//    the exponentials moves only when the row max grows by more than 2^8
+//    (O is then rescaled in tensor memory, by the warps whose rows need
+//    it); the probabilities go to shared memory as a BF16 high part
+//    (truncated) and a BF16 low part (two MMAs, ~16 significant bits for
+//    P); an mbarrier with one arrival per softmax thread hands P to the
+//    producer, so no block-wide barrier sits in the step loop;
 //  * tiles run heaviest first (the last tile of a prompt sees the most keys).
+//
+// What bounds it (measured): per step a softmax thread spends ~1,100 cycles
+// on its 32 exponentials and the surrounding arithmetic (the SFU pipe is
+// shared by the four softmax warps of each scheduler) and ~600 waiting for
+// the previous value product, so the step, not the tensor cores, sets the
+// pace; 128-row x 64-key steps keep every product small (M 128, N 64).
 //
 // Every mbarrier wait is bounded (about two seconds of SM clock); a timeout
 // sets the error flag, the CTA waits (bounded) for its own copies and
@@ -61,18 +74,29 @@ constexpr int kTileTokens = 32;                      // query tokens per CTA
 constexpr int kRows = kTileTokens * kGroup;          // 128: the MMA's M
 constexpr int kStepKeys = 64;                        // keys per step: the S MMA's N
 constexpr int kStepPages = kStepKeys / kPage;        // 4
-constexpr int kThreads = 128;
-constexpr uint32_t kTmemCols = 128;                  // S: columns 0..63, O_step: 64..127
+constexpr int kSoftmaxWarps = 8;                     // two per tensor-memory lane quarter
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kLoadWarp = kSoftmaxWarps;             // TMA copies
+constexpr int kMmaWarp = kSoftmaxWarps + 1;          // tensor-core products
+constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kKStages = 4;                          // K ring
+constexpr int kVStages = 3;                          // V ring
+constexpr uint32_t kTmemCols = 256;                  // S: 0..63 and 64..127, O: 128..191
+constexpr uint32_t kTmemO = 128;
+constexpr float kRescaleLog2 = 8.f;                  // lazy max: p <= 2^8
 constexpr long long kWaitCycles = 4000000000LL;      // about two seconds
 
 struct PrefillSmem {                                 // every tile 1024-byte aligned
   uint8_t q[kRows * kRowBytes];                      // 16 KiB
-  uint8_t k[2][kStepKeys * kRowBytes];               // 2 x 8 KiB
-  uint8_t v[2][kStepKeys * kRowBytes];               // 2 x 8 KiB
+  uint8_t k[kKStages][kStepKeys * kRowBytes];        // 4 x 8 KiB
+  uint8_t v[kVStages][kStepKeys * kRowBytes];        // 3 x 8 KiB
   uint8_t p_hi[kRows * kRowBytes];                   // 16 KiB
   uint8_t p_lo[kRows * kRowBytes];                   // 16 KiB
-  unsigned long long bar_q, bar_kv[2], bar_s, bar_o;
+  unsigned long long bar_q, bar_k[kKStages], bar_v[kVStages], bar_s[2], bar_p, bar_o;
+  unsigned long long k_free[kKStages], v_free[kVStages];   // stage read by its product
   uint32_t tmem_base;
+  int abort_flag;
+  float lsum[2][kRows];                              // the two halves' row sums
   int pages[kMaxPages];                              // block-table row, -1 = not loadable
 };
 static_assert(offsetof(PrefillSmem, k) % 1024 == 0 && offsetof(PrefillSmem, v) % 1024 == 0 &&
@@ -89,7 +113,7 @@ struct PrefillParams {
   int num_pages;
   int table_stride;
   int max_seq_len;
-  int tiles_max;              // gridDim.x: tiles per sequence the launch covers
+  int tiles_max;              // gridDim.y: tiles per sequence the launch covers
   int total_tokens;           // rows of q and out
 };
 
@@ -100,6 +124,8 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ void set_error(int* err, int bits) { atomicOr(err, bits); }
 
+__device__ __forceinline__ int lane_of(int tid) { return tid & 31; }
+
 __device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                : "memory");
@@ -109,6 +135,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, u
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
@@ -204,14 +234,27 @@ __device__ __forceinline__ void mma_commit(unsigned long long* bar) {
                : "memory");
 }
 
-// 64 consecutive FP32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Barrier among the softmax warps only (named barrier 1).
+__device__ __forceinline__ void softmax_warps_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
@@ -241,10 +284,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return w;
 }
 
-__device__ __forceinline__ float bf16_lo_to_float(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi_to_float(uint32_t w) {
-  return __uint_as_float(w & 0xffff0000u);
-}
 
 // ---------------------------------------------------------------- fill
 // One block of 128 threads per chunk token (blockIdx.x = token of the chunk,
@@ -288,15 +327,17 @@ __global__ void __launch_bounds__(128) prefill_fill_kernel(
 }
 
 // ---------------------------------------------------------------- attention
-__global__ void __launch_bounds__(kThreads, 1) prefill_attention_kernel(
+__global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v, const PrefillParams prm) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(smem_raw + pad);
 
-  const int tile = prm.tiles_max - 1 - static_cast<int>(blockIdx.x);   // heaviest first
-  const int g = blockIdx.y;
+  // CTAs are dispatched in linear block order (x fastest): the kv head in x
+  // and the tile, counted from the last, in y make that order heaviest first
+  const int tile = prm.tiles_max - 1 - static_cast<int>(blockIdx.y);
+  const int g = blockIdx.x;
   const int b = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -305,10 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attention_kernel(
   const int n = prm.cu_tokens[b + 1] - row0;
   const int start = prm.start_pos[b];
   if (row0 < 0 || n < 0 || row0 + n > prm.total_tokens) {   // rows outside the caller's buffers
-    if (blockIdx.x == 0 && g == 0 && tid == 0) set_error(prm.err, PKV_DEV_ERR_SEQ_LEN);
+    if (blockIdx.y == 0 && g == 0 && tid == 0) set_error(prm.err, PKV_DEV_ERR_SEQ_LEN);
     return;
   }
-  if (blockIdx.x == 0 && g == 0 && tid == 0 && n > prm.tiles_max * kTileTokens)
+  if (blockIdx.y == 0 && g == 0 && tid == 0 && n > prm.tiles_max * kTileTokens)
     set_error(prm.err, PKV_DEV_ERR_SEQ_LEN);
   if (tile * kTileTokens >= n) return;                 // the whole CTA, before any allocation
   if (start < 0 || start + n > prm.max_seq_len) {
@@ -334,10 +375,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attention_kernel(
 
   if (tid == 0) {
     mbar_init(&sm.bar_q, 1);
-    mbar_init(&sm.bar_kv[0], 1);
-    mbar_init(&sm.bar_kv[1], 1);
-    mbar_init(&sm.bar_s, 1);
+    for (int i = 0; i < kKStages; ++i) mbar_init(&sm.bar_k[i], 1);
+    for (int i = 0; i < kVStages; ++i) mbar_init(&sm.bar_v[i], 1);
+    mbar_init(&sm.bar_s[0], 1);
+    mbar_init(&sm.bar_s[1], 1);
+    mbar_init(&sm.bar_p, kSoftmaxThreads);
     mbar_init(&sm.bar_o, 1);
+    for (int i = 0; i < kKStages; ++i) mbar_init(&sm.k_free[i], 1);
+    for (int i = 0; i < kVStages; ++i) mbar_init(&sm.v_free[i], 1);
+    sm.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -345,180 +391,285 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attention_kernel(
   const bool any_bad_page = __syncthreads_or(bad_page);   // also publishes sm.pages
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
 
-  // K/V of step j (pages 4j .. 4j+3) into stage j & 1: thread 0 issues
-  auto issue_kv = [&](int j) {
-    const int stage = j & 1;
-    int valid = 0;
-    for (int q = 0; q < kStepPages; ++q) {
-      const int lp = j * kStepPages + q;
-      valid += (lp < n_pages && sm.pages[lp] >= 0) ? 1 : 0;
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ copy engine
+    // Lanes 0..3 each copy one page of a step; lane 0 waits for the stage to
+    // be free (its product committed) and sets the expected bytes first.
+    const int lane = lane_of(tid);
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+      mbar_arrive_expect_tx(&sm.bar_q, kRows * kRowBytes);
+      tma_load_3d(sm.q, &tmap_q, 0, g * kGroup, row0 + tile * kTileTokens, &sm.bar_q);
     }
-    mbar_arrive_expect_tx(&sm.bar_kv[stage], static_cast<uint32_t>(valid) * 2 * kPage * kRowBytes);
-    for (int q = 0; q < kStepPages; ++q) {
-      const int lp = j * kStepPages + q;
-      if (lp < n_pages && sm.pages[lp] >= 0) {
-        tma_load_4d(sm.k[stage] + q * kPage * kRowBytes, &tmap_k, 0, 0, g, sm.pages[lp],
-                    &sm.bar_kv[stage]);
-        tma_load_4d(sm.v[stage] + q * kPage * kRowBytes, &tmap_v, 0, 0, g, sm.pages[lp],
-                    &sm.bar_kv[stage]);
+    int k_issued = 0, v_issued = 0;
+    auto issue_tile = [&](uint8_t* dst, const CUtensorMap* map, unsigned long long* bar,
+                          unsigned long long* free_bar, int j, int stages) -> bool {
+      bool ok = true;
+      if (lane == 0) {
+        if (j >= stages) ok = mbar_wait(free_bar, ((j - stages) / stages) & 1);
+        if (ok) {
+          int valid = 0;
+          for (int q = 0; q < kStepPages; ++q) {
+            const int lp = j * kStepPages + q;
+            valid += (lp < n_pages && sm.pages[lp] >= 0) ? 1 : 0;
+          }
+          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(valid) * kPage * kRowBytes);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (ok && lane < kStepPages) {
+        const int lp = j * kStepPages + lane;
+        const int page = lp < n_pages ? sm.pages[lp] : -1;
+        if (page >= 0) tma_load_4d(dst + lane * kPage * kRowBytes, map, 0, 0, g, page, bar);
+      }
+      __syncwarp();
+      return ok;
+    };
+    bool ok = true;
+    for (int j = 0; ok && j < n_steps; ++j) {
+      if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) {   // one view per warp
+        ok = false;
+        break;
+      }
+      ok = issue_tile(sm.k[j % kKStages], &tmap_k, &sm.bar_k[j % kKStages],
+                      &sm.k_free[j % kKStages], j, kKStages);
+      if (!ok) break;
+      ++k_issued;
+      ok = issue_tile(sm.v[j % kVStages], &tmap_v, &sm.bar_v[j % kVStages],
+                      &sm.v_free[j % kVStages], j, kVStages);
+      if (!ok) break;
+      ++v_issued;
+    }
+    if (lane == 0) {
+      if (!ok) {
+        *abort_flag = 1;
+        set_error(prm.err, PKV_DEV_ERR_TIMEOUT);
+      }
+      // every copy issued lands before the CTA frees its memory (last phase
+      // of each barrier; every wait bounded)
+      mbar_wait(&sm.bar_q, 0);
+      for (int st = 0; st < kKStages; ++st) {
+        const int uses = (k_issued - st + kKStages - 1) / kKStages;
+        if (uses > 0) mbar_wait(&sm.bar_k[st], (uses - 1) & 1);
+      }
+      for (int st = 0; st < kVStages; ++st) {
+        const int uses = (v_issued - st + kVStages - 1) / kVStages;
+        if (uses > 0) mbar_wait(&sm.bar_v[st], (uses - 1) & 1);
       }
     }
-  };
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&sm.bar_q, kRows * kRowBytes);
-    tma_load_3d(sm.q, &tmap_q, 0, g * kGroup, row0 + tile * kTileTokens, &sm.bar_q);
-    issue_kv(0);
-    if (n_steps > 1) issue_kv(1);
-  }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ tensor cores
+    if (lane_of(tid) == 0) {
+      const uint32_t idesc_s = instr_desc(kRows, kStepKeys, false);
+      const uint32_t idesc_o = instr_desc(kRows, kDim, true);
+      const uint64_t q_desc = smem_desc_sw128(smem_u32(sm.q), 16, 1024);
+      const uint64_t phi_desc = smem_desc_sw128(smem_u32(sm.p_hi), 16, 1024);
+      const uint64_t plo_desc = smem_desc_sw128(smem_u32(sm.p_lo), 16, 1024);
+      int s_issued = 0, o_issued = 0;
+      // the descriptor's start address counts 16-byte units: + bytes >> 4
+      auto issue_s = [&](int j) -> bool {          // S(j) = Q K(j)^T, buffer j & 1
+        if (!mbar_wait(&sm.bar_k[j % kKStages], (j / kKStages) & 1)) return false;
+        tc_fence_after();
+        const uint64_t k_desc = smem_desc_sw128(smem_u32(sm.k[j % kKStages]), 16, 1024);
+        #pragma unroll
+        for (int kk = 0; kk < kDim / 16; ++kk)
+          mma_bf16(tmem + (j & 1) * kStepKeys, q_desc + kk * 2, k_desc + kk * 2, idesc_s, kk > 0);
+        mma_commit(&sm.bar_s[j & 1]);
+        mma_commit(&sm.k_free[j % kKStages]);
+        ++s_issued;
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {         // O += P(j) V(j)
+        if (!mbar_wait(&sm.bar_p, j & 1) ||
+            !mbar_wait(&sm.bar_v[j % kVStages], (j / kVStages) & 1))
+          return false;
+        tc_fence_after();
+        const uint64_t v_desc = smem_desc_sw128(smem_u32(sm.v[j % kVStages]), 8192, 1024);
+        #pragma unroll
+        for (int kk = 0; kk < kStepKeys / 16; ++kk)
+          mma_bf16(tmem + kTmemO, phi_desc + kk * 2, v_desc + kk * (16 * kRowBytes >> 4), idesc_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        #pragma unroll
+        for (int kk = 0; kk < kStepKeys / 16; ++kk)
+          mma_bf16(tmem + kTmemO, plo_desc + kk * 2, v_desc + kk * (16 * kRowBytes >> 4), idesc_o,
+                   1u);
+        mma_commit(&sm.bar_o);
+        mma_commit(&sm.v_free[j % kVStages]);
+        ++o_issued;
+        return true;
+      };
+      bool ok = mbar_wait(&sm.bar_q, 0);
+      // S one step ahead of the value product: S(j), then P(j - 1) V(j - 1)
+      for (int j = 0; ok && j <= n_steps; ++j) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        if (j < n_steps && !issue_s(j)) {
+          ok = false;
+          break;
+        }
+        if (j > 0 && !issue_pv(j - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_error(prm.err, PKV_DEV_ERR_TIMEOUT);
+      }
+      // every product issued completes before the CTA frees its memory
+      for (int b2 = 0; b2 < 2; ++b2) {
+        const int uses = (s_issued - b2 + 1) / 2;
+        if (uses > 0) mbar_wait(&sm.bar_s[b2], (uses - 1) & 1);
+      }
+      if (o_issued > 0) mbar_wait(&sm.bar_o, (o_issued - 1) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int half = warp >> 2;                         // key columns 32*half .. +31
+    const int r = (warp & 3) * 32 + (tid & 31);         // the MMA row = tensor-memory lane
+    const int tok = r >> 2;                             // token of the tile, head r & 3
+    const int pos = p_first + min(tok, t_valid - 1);    // rows past the chunk mirror its last token
+    const float c = 1.4426950408889634f * 0.125f;       // log2(e) / sqrt(64)
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    float m_run = -INFINITY, l_half = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_steps; ++j) {
+      if (*abort_flag || !mbar_wait(&sm.bar_s[j & 1], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sa[32], sb[32];                           // keys 0..31 and 32..63 of the step
+      tmem_ld32(tmem + lane_addr + (j & 1) * kStepKeys, sa);
+      tmem_ld32(tmem + lane_addr + (j & 1) * kStepKeys + 32, sb);
 
-  // this thread's row: token tok of the tile, head (tid & 3) of the group
-  const int tok = tid >> 2;
-  const int pos = p_first + min(tok, t_valid - 1);     // rows past the chunk mirror its last token
-  const float c = 1.4426950408889634f * 0.125f;        // log2(e) / sqrt(64)
-  const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t idesc_s = instr_desc(kRows, kStepKeys, false);
-  const uint32_t idesc_o = instr_desc(kRows, kDim, true);
-  const uint32_t q_addr = smem_u32(sm.q);
-  const uint32_t phi_addr = smem_u32(sm.p_hi);
-  const uint32_t plo_addr = smem_u32(sm.p_lo);
+      // row max over all 64 keys (raw scores; the scale is positive)
+      const int key0 = j * kStepKeys;
+      if (key0 + kStepKeys - 1 > p_first) {             // some key hidden from some row
+        #pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (key0 + i > pos) sa[i] = __float_as_uint(-INFINITY);
+          if (key0 + 32 + i > pos) sb[i] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mx8[8];
+      #pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(__uint_as_float(sa[e]), __uint_as_float(sb[e]));
+      #pragma unroll
+      for (int i = 8; i < 32; ++i)
+        mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(__uint_as_float(sa[i]), __uint_as_float(sb[i])));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_step = mx * c;
+      float alpha = 1.f;
+      const bool grow = m_step > m_run + kRescaleLog2;
+      if (grow) {
+        alpha = fast_exp2(m_run - m_step);
+        m_run = m_step;
+        l_half *= alpha;
+      }
+      // this half's 32 probabilities, their sum, BF16 high / low parts
+      uint32_t hi[16], lo[16];
+      auto probabilities = [&](const uint32_t (&v)[32]) {
+        const float2 c2 = make_float2(c, c);
+        const float2 nm2 = make_float2(-m_run, -m_run);
+        const float2 neg1 = make_float2(-1.f, -1.f);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        #pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                      c2, nm2);
+          const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          acc[(i >> 1) & 3] = __fadd2_rn(acc[(i >> 1) & 3], pp);
+          const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
+          hi[i / 2] = __byte_perm(b0, b1, 0x7632);
+          const float2 h = make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                       __uint_as_float(b1 & 0xffff0000u));
+          const float2 rest = __ffma2_rn(h, neg1, pp);
+          lo[i / 2] = pack_bf16x2(rest.x, rest.y);
+        }
+        const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        l_half += a.x + a.y;
+      };
+      if (half == 0) {
+        probabilities(sa);
+      } else {
+        probabilities(sb);
+      }
 
-  float o[kDim];
-  #pragma unroll
-  for (int d = 0; d < kDim; ++d) o[d] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
-
-  bool failed = !mbar_wait(&sm.bar_q, 0);
-  int kv_waited = 0;          // steps whose K/V this CTA has waited for
-  int kv_issued = min(n_steps, 2);
-  bool s_pending = false, o_pending = false;
-  int j = 0;
-  for (; j < n_steps; ++j) {
-    const int stage = j & 1;
-    bool ok = mbar_wait(&sm.bar_kv[stage], (j >> 1) & 1);
-    if (ok) kv_waited = j + 1;
-    // V rows the product must not see: keys past the tile's last token and
-    // pages not loaded (zero, so that p = 0 times them stays 0)
-    if (ok && (any_bad_page || (j + 1) * kStepKeys > n_keys)) {
-      for (int idx = tid; idx < kStepKeys * 8; idx += kThreads) {
-        const int key_row = idx >> 3;
-        const int key = j * kStepKeys + key_row;
-        const int lp = key / kPage;
-        if (key >= n_keys || lp >= n_pages || sm.pages[lp] < 0)
-          *reinterpret_cast<uint4*>(sm.v[stage] + key_row * kRowBytes + (idx & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+      // the previous product must be done before P and O are touched
+      if (j > 0) {
+        if (!mbar_wait(&sm.bar_o, (j - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grow)) {             // rescale this half of O
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_addr + kTmemO + half * 32, ov);
+          #pragma unroll
+          for (int d = 0; d < 32; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
+          tmem_st32(tmem + lane_addr + kTmemO + half * 32, ov);
+        }
+      }
+      // V rows the product must not see: keys past the tile's last token and
+      // pages not loaded (zero, so that p = 0 times them stays 0)
+      if (any_bad_page || (j + 1) * kStepKeys > n_keys) {
+        if (!mbar_wait(&sm.bar_v[j % kVStages], (j / kVStages) & 1)) {
+          ok = false;
+          break;
+        }
+        for (int idx = tid; idx < kStepKeys * 8; idx += kSoftmaxThreads) {
+          const int key_row = idx >> 3;
+          const int key = key0 + key_row;
+          const int lp = key / kPage;
+          if (key >= n_keys || lp >= n_pages || sm.pages[lp] < 0)
+            *reinterpret_cast<uint4*>(sm.v[j % kVStages] + key_row * kRowBytes + (idx & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      #pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const int chunk = half * 4 + ch;
+        const uint32_t off = static_cast<uint32_t>(r * kRowBytes + ((chunk ^ (r & 7)) << 4));
+        *reinterpret_cast<uint4*>(sm.p_hi + off) =
+            make_uint4(hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
+        *reinterpret_cast<uint4*>(sm.p_lo + off) =
+            make_uint4(lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
       }
       fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm.bar_p);
     }
-    if (__syncthreads_or(failed || !ok)) {
-      failed = true;
-      break;
+    if (!ok) {
+      *abort_flag = 1;
+      if (tid == 0) set_error(prm.err, PKV_DEV_ERR_TIMEOUT);
     }
-
-    // S = Q K^T
-    if (tid == 0) {
+    // the two halves' sums of each row meet in shared memory
+    sm.lsum[half][r] = l_half;
+    softmax_warps_sync();
+    if (ok && !*abort_flag && mbar_wait(&sm.bar_o, (n_steps - 1) & 1)) {
       tc_fence_after();
-      const uint32_t k_addr = smem_u32(sm.k[stage]);
-      #pragma unroll
-      for (int kk = 0; kk < kDim / 16; ++kk)
-        mma_bf16(tmem, smem_desc_sw128(q_addr + kk * 32, 16, 1024),
-                 smem_desc_sw128(k_addr + kk * 32, 16, 1024), idesc_s, kk > 0);
-      mma_commit(&sm.bar_s);
-    }
-    s_pending = true;
-    ok = mbar_wait(&sm.bar_s, j & 1);
-    s_pending = !ok;
-    tc_fence_after();
-    uint32_t sraw[kStepKeys];
-    tmem_ld64(tmem + lane_addr, sraw);
-
-    // online softmax over this step's keys (base 2)
-    const int key0 = j * kStepKeys;
-    float m_step = -INFINITY;
-    #pragma unroll
-    for (int i = 0; i < kStepKeys; ++i) {
-      const float s = key0 + i <= pos ? __uint_as_float(sraw[i]) * c : -INFINITY;
-      sraw[i] = __float_as_uint(s);
-      m_step = fmaxf(m_step, s);
-    }
-    const float m_new = fmaxf(m_run, m_step);
-    const float alpha = fast_exp2(m_run - m_new);
-    float sum = 0.f;
-    #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      uint32_t hi[4], lo[4];
-      #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p0 = fast_exp2(__uint_as_float(sraw[ch * 8 + 2 * e]) - m_new);
-        const float p1 = fast_exp2(__uint_as_float(sraw[ch * 8 + 2 * e + 1]) - m_new);
-        sum += p0 + p1;
-        hi[e] = pack_bf16x2(p0, p1);
-        lo[e] = pack_bf16x2(p0 - bf16_lo_to_float(hi[e]), p1 - bf16_hi_to_float(hi[e]));
+      uint32_t ov[32];
+      tmem_ld32(tmem + lane_addr + kTmemO + half * 32, ov);
+      if (tok < t_valid) {
+        const float inv = 1.f / (sm.lsum[0][r] + sm.lsum[1][r]);
+        float* dst = prm.out + ((static_cast<size_t>(row0) + tile * kTileTokens + tok) * kHq +
+                                g * kGroup + (r & 3)) * kDim + half * 32;
+        #pragma unroll
+        for (int d = 0; d < 32; d += 4)
+          *reinterpret_cast<float4*>(dst + d) =
+              make_float4(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv,
+                          __uint_as_float(ov[d + 2]) * inv, __uint_as_float(ov[d + 3]) * inv);
       }
-      const uint32_t off = static_cast<uint32_t>(tid * kRowBytes + ((ch ^ (tid & 7)) << 4));
-      *reinterpret_cast<uint4*>(sm.p_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(sm.p_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    l_run = l_run * alpha + sum;
-    m_run = m_new;
-    #pragma unroll
-    for (int d = 0; d < kDim; ++d) o[d] *= alpha;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-
-    // O_step = P_hi V + P_lo V
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t v_addr = smem_u32(sm.v[stage]);
-      #pragma unroll
-      for (int kk = 0; kk < kStepKeys / 16; ++kk)
-        mma_bf16(tmem + kDim, smem_desc_sw128(phi_addr + kk * 32, 16, 1024),
-                 smem_desc_sw128(v_addr + kk * 16 * kRowBytes, 8192, 1024), idesc_o, kk > 0);
-      #pragma unroll
-      for (int kk = 0; kk < kStepKeys / 16; ++kk)
-        mma_bf16(tmem + kDim, smem_desc_sw128(plo_addr + kk * 32, 16, 1024),
-                 smem_desc_sw128(v_addr + kk * 16 * kRowBytes, 8192, 1024), idesc_o, 1);
-      mma_commit(&sm.bar_o);
-    }
-    o_pending = true;
-    ok = mbar_wait(&sm.bar_o, j & 1);
-    o_pending = !ok;
-    tc_fence_after();
-    uint32_t oraw[kDim];
-    tmem_ld64(tmem + lane_addr + kDim, oraw);
-    #pragma unroll
-    for (int d = 0; d < kDim; ++d) o[d] += __uint_as_float(oraw[d]);
-
-    // both products of this step are done: its K/V stage can be refilled
-    if (ok && tid == 0 && j + 2 < n_steps) {
-      issue_kv(j + 2);
-      kv_issued = j + 3;
-    }
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-  }
-
-  if (failed) {
-    if (tid == 0) set_error(prm.err, PKV_DEV_ERR_TIMEOUT);
-    // let this CTA's copies and products in flight land (each wait bounded)
-    for (int w = kv_waited; w < kv_issued; ++w) mbar_wait(&sm.bar_kv[w & 1], (w >> 1) & 1);
-    if (s_pending) mbar_wait(&sm.bar_s, j & 1);
-    if (o_pending) mbar_wait(&sm.bar_o, j & 1);
-  } else if (tok < t_valid) {
-    const float inv = 1.f / l_run;
-    float* dst = prm.out + ((static_cast<size_t>(row0) + tile * kTileTokens + tok) * kHq +
-                            g * kGroup + (tid & 3)) * kDim;
-    #pragma unroll
-    for (int d = 0; d < kDim; d += 4)
-      *reinterpret_cast<float4*>(dst + d) =
-          make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
   }
   tc_fence_before();
   __syncthreads();
@@ -654,7 +805,7 @@ pkv_status launch_attention(pkv_pool_t pool, int layer, const void* q, const voi
   prm.max_seq_len = c.max_seq_len;
   prm.tiles_max = (max_chunk_tokens + kTileTokens - 1) / kTileTokens;
   prm.total_tokens = total_tokens;
-  prefill_attention_kernel<<<dim3(prm.tiles_max, kHkv, batch), kThreads, kSmemBytes,
+  prefill_attention_kernel<<<dim3(kHkv, prm.tiles_max, batch), kThreads, kSmemBytes,
                              static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
