@@ -156,14 +156,20 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend=None):
+    """One process per GPU (torchrun sets RANK/LOCAL_RANK/WORLD_SIZE/MASTER_*);
+    NCCL on GPUs, gloo where there is none (the CPU tests of this path)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return world, rank, local
 
 
@@ -174,12 +180,20 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The slowest rank's figure (the whole job ends with it)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_gbs(world, bytes_per_step, steps, total_ms_max):
+    """Replicas: every rank moves bytes_per_step per step; the job takes as
+    long as its slowest rank. GB/s over all ranks."""
+    return world * bytes_per_step * steps / (total_ms_max * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -418,8 +432,8 @@ def run_ours(args, world, rank, local):
 
     nbytes = step_bytes(wl, args.rope)
     ms_per_step = total_ms / args.steps
-    value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
-    e2e_value = world * nbytes * len(e2e_ms) / (e2e_total * 1e-3) / 1e9
+    value = whole_job_gbs(world, nbytes, args.steps, total_ms)
+    e2e_value = whole_job_gbs(world, nbytes, len(e2e_ms), e2e_total)
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
 
