@@ -29,21 +29,24 @@
 //    tcgen05.mma kind::f16 completed on mbarriers through tcgen05.commit,
 //    which also tell the loader when a stage is free;
 //  * eight softmax warps, two per tensor-memory lane quarter: each thread
-//    reads its row's 64 scores (so both halves agree on the row max) and
-//    handles 32 of them: online softmax in base 2, where the max used for
-//    the exponentials moves only when the row max grows by more than 2^8
-//    (O is then rescaled in tensor memory, by the warps whose rows need
-//    it); the probabilities go to shared memory as a BF16 high part
-//    (truncated) and a BF16 low part (two MMAs, ~16 significant bits for
-//    P); an mbarrier with one arrival per softmax thread hands P to the
-//    producer, so no block-wide barrier sits in the step loop;
+//    reads its half (32 keys) of its row's scores; online softmax in base 2
+//    whose max moves only when a row's max grows by more than 2^8 (then the
+//    two halves agree on it through shared memory, and O is rescaled in
+//    tensor memory by the warps whose rows grew); the probabilities go back
+//    into tensor memory over the scores they came from, as a BF16 high part
+//    (truncated) and a BF16 low part, and the value product reads them from
+//    there (A operand in tensor memory; ~16 significant bits for P from two
+//    MMAs). The score tiles are double-buffered, so P is too: the softmax
+//    warps never wait for the previous value product, except to rescale O.
+//    An mbarrier with one arrival per softmax thread hands P over; the
+//    only block-level syncs in the step loop are two votes among the
+//    softmax warps;
 //  * tiles run heaviest first (the last tile of a prompt sees the most keys).
 //
-// What bounds it (measured): per step a softmax thread spends ~1,100 cycles
-// on its 32 exponentials and the surrounding arithmetic (the SFU pipe is
-// shared by the four softmax warps of each scheduler) and ~600 waiting for
-// the previous value product, so the step, not the tensor cores, sets the
-// pace; 128-row x 64-key steps keep every product small (M 128, N 64).
+// What bounds it (measured on an earlier version): per step a softmax
+// thread spent ~1,100 cycles on its 32 exponentials and the surrounding
+// arithmetic, so the step, not the tensor cores, sets the pace; 128-row x
+// 64-key steps keep every product small (M 128, N 64).
 //
 // Every mbarrier wait is bounded (about two seconds of SM clock); a timeout
 // sets the error flag, the CTA waits (bounded) for its own copies and
@@ -90,17 +93,16 @@ struct PrefillSmem {                                 // every tile 1024-byte ali
   uint8_t q[kRows * kRowBytes];                      // 16 KiB
   uint8_t k[kKStages][kStepKeys * kRowBytes];        // 4 x 8 KiB
   uint8_t v[kVStages][kStepKeys * kRowBytes];        // 3 x 8 KiB
-  uint8_t p_hi[kRows * kRowBytes];                   // 16 KiB
-  uint8_t p_lo[kRows * kRowBytes];                   // 16 KiB
   unsigned long long bar_q, bar_k[kKStages], bar_v[kVStages], bar_s[2], bar_p, bar_o;
+  unsigned long long p_free[2];                      // tile (S, then P) read by its value product
   unsigned long long k_free[kKStages], v_free[kVStages];   // stage read by its product
   uint32_t tmem_base;
   int abort_flag;
   float lsum[2][kRows];                              // the two halves' row sums
+  float pmax[2][kRows];                              // the two halves' step maxima
   int pages[kMaxPages];                              // block-table row, -1 = not loadable
 };
-static_assert(offsetof(PrefillSmem, k) % 1024 == 0 && offsetof(PrefillSmem, v) % 1024 == 0 &&
-                  offsetof(PrefillSmem, p_hi) % 1024 == 0 && offsetof(PrefillSmem, p_lo) % 1024 == 0,
+static_assert(offsetof(PrefillSmem, k) % 1024 == 0 && offsetof(PrefillSmem, v) % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
 constexpr size_t kSmemBytes = sizeof(PrefillSmem) + 1024;   // + room to align the base
 
@@ -227,6 +229,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T: A's 128 rows are the tensor-memory lanes,
+// its K elements packed two BF16 per 32-bit column (element 2c in the low half).
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // One arrive on `bar` once every MMA this thread issued before has completed.
 __device__ __forceinline__ void mma_commit(unsigned long long* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -250,6 +264,33 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "tcgen05.wait::st.sync.aligned;"
       ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane, written
+// (completion awaited separately with tmem_wait_st).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Barrier among the softmax warps that also ORs a flag over them.
+__device__ __forceinline__ bool softmax_warps_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "n"(kSoftmaxThreads)
+      : "memory");
+  return r != 0;
 }
 
 // Barrier among the softmax warps only (named barrier 1).
@@ -381,6 +422,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
     mbar_init(&sm.bar_s[1], 1);
     mbar_init(&sm.bar_p, kSoftmaxThreads);
     mbar_init(&sm.bar_o, 1);
+    mbar_init(&sm.p_free[0], 1);
+    mbar_init(&sm.p_free[1], 1);
     for (int i = 0; i < kKStages; ++i) mbar_init(&sm.k_free[i], 1);
     for (int i = 0; i < kVStages; ++i) mbar_init(&sm.v_free[i], 1);
     sm.abort_flag = 0;
@@ -467,12 +510,14 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
       const uint32_t idesc_s = instr_desc(kRows, kStepKeys, false);
       const uint32_t idesc_o = instr_desc(kRows, kDim, true);
       const uint64_t q_desc = smem_desc_sw128(smem_u32(sm.q), 16, 1024);
-      const uint64_t phi_desc = smem_desc_sw128(smem_u32(sm.p_hi), 16, 1024);
-      const uint64_t plo_desc = smem_desc_sw128(smem_u32(sm.p_lo), 16, 1024);
       int s_issued = 0, o_issued = 0;
       // the descriptor's start address counts 16-byte units: + bytes >> 4
-      auto issue_s = [&](int j) -> bool {          // S(j) = Q K(j)^T, buffer j & 1
+      // S(j) = Q K(j)^T into tile j & 1, once K(j) landed and the value
+      // product of P(j - 2), which the softmax warps wrote over S(j - 2) in
+      // that tile, is done
+      auto issue_s = [&](int j) -> bool {
         if (!mbar_wait(&sm.bar_k[j % kKStages], (j / kKStages) & 1)) return false;
+        if (j >= 2 && !mbar_wait(&sm.p_free[j & 1], ((j - 2) >> 1) & 1)) return false;
         tc_fence_after();
         const uint64_t k_desc = smem_desc_sw128(smem_u32(sm.k[j % kKStages]), 16, 1024);
         #pragma unroll
@@ -483,22 +528,26 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
         ++s_issued;
         return true;
       };
-      auto issue_pv = [&](int j) -> bool {         // O += P(j) V(j)
+      // O += P(j) V(j): P from tensor memory (tile j & 1: high part in
+      // columns 0..31, low part in 32..63, 16 keys per 8 columns)
+      auto issue_pv = [&](int j) -> bool {
         if (!mbar_wait(&sm.bar_p, j & 1) ||
             !mbar_wait(&sm.bar_v[j % kVStages], (j / kVStages) & 1))
           return false;
         tc_fence_after();
         const uint64_t v_desc = smem_desc_sw128(smem_u32(sm.v[j % kVStages]), 8192, 1024);
+        const uint32_t p_tile = tmem + (j & 1) * kStepKeys;
         #pragma unroll
         for (int kk = 0; kk < kStepKeys / 16; ++kk)
-          mma_bf16(tmem + kTmemO, phi_desc + kk * 2, v_desc + kk * (16 * kRowBytes >> 4), idesc_o,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_tmem_a(tmem + kTmemO, p_tile + kk * 8, v_desc + kk * (16 * kRowBytes >> 4),
+                          idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         #pragma unroll
         for (int kk = 0; kk < kStepKeys / 16; ++kk)
-          mma_bf16(tmem + kTmemO, plo_desc + kk * 2, v_desc + kk * (16 * kRowBytes >> 4), idesc_o,
-                   1u);
+          mma_bf16_tmem_a(tmem + kTmemO, p_tile + 32 + kk * 8, v_desc + kk * (16 * kRowBytes >> 4),
+                          idesc_o, 1u);
         mma_commit(&sm.bar_o);
         mma_commit(&sm.v_free[j % kVStages]);
+        mma_commit(&sm.p_free[j & 1]);
         ++o_issued;
         return true;
       };
@@ -540,43 +589,45 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
     float m_run = -INFINITY, l_half = 0.f;
     bool ok = true;
     for (int j = 0; j < n_steps; ++j) {
-      if (*abort_flag || !mbar_wait(&sm.bar_s[j & 1], (j >> 1) & 1)) {
-        ok = false;
-        break;
-      }
+      // (a failed wait is voted on with the other softmax threads below, so
+      // that every one of them leaves the loop at the same step)
+      bool failed = *abort_flag != 0 || !mbar_wait(&sm.bar_s[j & 1], (j >> 1) & 1);
       tc_fence_after();
-      uint32_t sa[32], sb[32];                           // keys 0..31 and 32..63 of the step
-      tmem_ld32(tmem + lane_addr + (j & 1) * kStepKeys, sa);
-      tmem_ld32(tmem + lane_addr + (j & 1) * kStepKeys + 32, sb);
+      uint32_t sv[32];                                   // this half's 32 keys of the step
+      tmem_ld32(tmem + lane_addr + (j & 1) * kStepKeys + half * 32, sv);
 
-      // row max over all 64 keys (raw scores; the scale is positive)
-      const int key0 = j * kStepKeys;
-      if (key0 + kStepKeys - 1 > p_first) {             // some key hidden from some row
+      const int key0 = j * kStepKeys + half * 32;
+      if (key0 + 31 > p_first) {                         // some key hidden from some row
         #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (key0 + i > pos) sa[i] = __float_as_uint(-INFINITY);
-          if (key0 + 32 + i > pos) sb[i] = __float_as_uint(-INFINITY);
-        }
+        for (int i = 0; i < 32; ++i)
+          if (key0 + i > pos) sv[i] = __float_as_uint(-INFINITY);
       }
       float mx8[8];
       #pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(__uint_as_float(sa[e]), __uint_as_float(sb[e]));
+      for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(sv[e]);
       #pragma unroll
-      for (int i = 8; i < 32; ++i)
-        mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(__uint_as_float(sa[i]), __uint_as_float(sb[i])));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_step = mx * c;
+      for (int i = 8; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
+      const float half_max = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // The max used for the exponentials moves only when a row's max grows
+      // by more than 2^8. Usually no row's does; when one does, the two
+      // halves of every row agree on the step's row max through shared memory.
       float alpha = 1.f;
-      const bool grow = m_step > m_run + kRescaleLog2;
-      if (grow) {
-        alpha = fast_exp2(m_run - m_step);
-        m_run = m_step;
-        l_half *= alpha;
+      bool grow = false;
+      if (softmax_warps_any(half_max * c > m_run + kRescaleLog2)) {
+        sm.pmax[half][r] = half_max;
+        softmax_warps_sync();
+        const float m_step = fmaxf(sm.pmax[0][r], sm.pmax[1][r]) * c;
+        grow = m_step > m_run + kRescaleLog2;
+        if (grow) {
+          alpha = fast_exp2(m_run - m_step);
+          m_run = m_step;
+          l_half *= alpha;
+        }
       }
       // this half's 32 probabilities, their sum, BF16 high / low parts
       uint32_t hi[16], lo[16];
-      auto probabilities = [&](const uint32_t (&v)[32]) {
+      {
         const float2 c2 = make_float2(c, c);
         const float2 nm2 = make_float2(-m_run, -m_run);
         const float2 neg1 = make_float2(-1.f, -1.f);
@@ -584,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
                          make_float2(0.f, 0.f)};
         #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
                                       c2, nm2);
           const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
           acc[(i >> 1) & 3] = __fadd2_rn(acc[(i >> 1) & 3], pp);
@@ -597,21 +648,14 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
         }
         const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
         l_half += a.x + a.y;
-      };
-      if (half == 0) {
-        probabilities(sa);
-      } else {
-        probabilities(sb);
       }
 
-      // the previous product must be done before P and O are touched
-      if (j > 0) {
-        if (!mbar_wait(&sm.bar_o, (j - 1) & 1)) {
-          ok = false;
-          break;
-        }
+      // a row that grew its max rescales O, once P(j - 1) V(j - 1) is done
+      // (P(j) V(j) cannot start before this thread hands over P(j))
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        failed |= !mbar_wait(&sm.bar_o, (j - 1) & 1);
         tc_fence_after();
-        if (__any_sync(0xffffffffu, grow)) {             // rescale this half of O
+        if (!failed) {
           uint32_t ov[32];
           tmem_ld32(tmem + lane_addr + kTmemO + half * 32, ov);
           #pragma unroll
@@ -622,29 +666,31 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
       // V rows the product must not see: keys past the tile's last token and
       // pages not loaded (zero, so that p = 0 times them stays 0)
       if (any_bad_page || (j + 1) * kStepKeys > n_keys) {
-        if (!mbar_wait(&sm.bar_v[j % kVStages], (j / kVStages) & 1)) {
-          ok = false;
-          break;
-        }
-        for (int idx = tid; idx < kStepKeys * 8; idx += kSoftmaxThreads) {
-          const int key_row = idx >> 3;
-          const int key = key0 + key_row;
-          const int lp = key / kPage;
-          if (key >= n_keys || lp >= n_pages || sm.pages[lp] < 0)
-            *reinterpret_cast<uint4*>(sm.v[j % kVStages] + key_row * kRowBytes + (idx & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+        if (mbar_wait(&sm.bar_v[j % kVStages], (j / kVStages) & 1)) {
+          for (int idx = tid; idx < kStepKeys * 8; idx += kSoftmaxThreads) {
+            const int key_row = idx >> 3;
+            const int key = j * kStepKeys + key_row;
+            const int lp = key / kPage;
+            if (key >= n_keys || lp >= n_pages || sm.pages[lp] < 0)
+              *reinterpret_cast<uint4*>(sm.v[j % kVStages] + key_row * kRowBytes + (idx & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        } else {
+          failed = true;
         }
       }
-      #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const int chunk = half * 4 + ch;
-        const uint32_t off = static_cast<uint32_t>(r * kRowBytes + ((chunk ^ (r & 7)) << 4));
-        *reinterpret_cast<uint4*>(sm.p_hi + off) =
-            make_uint4(hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
-        *reinterpret_cast<uint4*>(sm.p_lo + off) =
-            make_uint4(lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
+      // both halves of every row have read S(j): P(j) may overwrite it
+      tc_fence_before();
+      if (softmax_warps_any(failed)) {
+        ok = false;
+        break;
       }
-      fence_proxy_async_smem();
+      tc_fence_after();
+      const uint32_t p_tile = tmem + lane_addr + (j & 1) * kStepKeys;
+      tmem_st16(p_tile + half * 16, hi);
+      tmem_st16(p_tile + 32 + half * 16, lo);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&sm.bar_p);
     }
