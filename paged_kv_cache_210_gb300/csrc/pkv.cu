@@ -99,7 +99,14 @@ struct alignas(16) BlockSmem {
   WarpSmem<kStages> warp[kWarps];
   float m[kWarps][kGroup];
   float l[kWarps][kGroup];
-  float acc[kWarps][kGroup][kDim];
+  union {
+    float acc[kWarps][kGroup][kDim];   // the warps' partial outputs (block merge)
+    struct {                           // longest-first order (prologue only)
+      int hist[kMaxPages + 1];
+      int wsum[kWarps];
+      int pick[3];
+    } order;
+  };
   int pages[kMaxPages];      // this sequence's block-table row
   int last;
 };
@@ -130,6 +137,7 @@ struct DecodeParams {
   int num_splits;             // > 0: S ranges per sequence
   int chunk_pages;            // > 0: ranges of this many pages (used when num_splits == 0)
   int early_trigger;          // let the next launch start right after the prefetch (one wave)
+  int longest_first;          // blockIdx.z is a rank by length, not a sequence index
   const float* rope_cos;      // rotary angles [max_seq_len][32] FP32, or null: no rotation
   const float* rope_sin;
 };
@@ -553,6 +561,105 @@ __device__ __forceinline__ void reduce_warp_state(WarpState& st) {
   }
 }
 
+// ---------------------------------------------------------------- dispatch order
+// Blocks start in linear block order (x fastest, z slowest). With mixed
+// lengths, handing out the longest sequences first shortens the launch's
+// tail (the longest-processing-time-first rule), so a ticket-mode launch
+// reads blockIdx.z as a rank: rank z is the z-th sequence by page count,
+// most pages first, ties by index. Each block finds its own sequence with a
+// counting sort of the page counts in shared memory: O(batch / threads +
+// 128) work and four block barriers, reading only seq_lens (which may be
+// read before the wait for the previous launch).
+__device__ __forceinline__ int page_count(int len) {
+  return min(max((len + kPage - 1) / kPage, 0), kMaxPages);
+}
+
+// Returns -1 without the second pass when `useful(pages)` says a block of
+// that rank has no work (split slots past the sequence's last range).
+template <int kWarps, int kStages, class Useful>
+__device__ int longest_first_sequence(int z, int batch, const int32_t* seq_lens,
+                                      BlockSmem<kWarps, kStages>& sm, Useful useful) {
+  constexpr int kThreads = kWarps * 32;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr int kHeld = 4;                 // page counts kept in registers per thread
+  int held[kHeld];
+  #pragma unroll
+  for (int e = 0; e < kHeld; ++e) {
+    const int s = static_cast<int>(threadIdx.x) + e * kThreads;
+    held[e] = s < batch ? page_count(seq_lens[s]) : -1;
+  }
+  for (int i = threadIdx.x; i <= kMaxPages; i += kThreads) sm.order.hist[i] = 0;
+  __syncthreads();
+  #pragma unroll
+  for (int e = 0; e < kHeld; ++e)
+    if (held[e] >= 0) atomicAdd(&sm.order.hist[held[e]], 1);
+  for (int s = static_cast<int>(threadIdx.x) + kHeld * kThreads; s < batch; s += kThreads)
+    atomicAdd(&sm.order.hist[page_count(seq_lens[s])], 1);
+  __syncthreads();
+  // bucket of rank z: lane l owns the buckets kMaxPages - 4l - e (e < 4),
+  // most pages first; bucket 0 comes last
+  if (warp == 0) {
+    int cnt[4], sum = 0;
+    #pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      cnt[e] = sm.order.hist[kMaxPages - 4 * lane - e];
+      sum += cnt[e];
+    }
+    int incl = sum;
+    #pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int excl = incl - sum;
+    #pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (z >= excl && z < excl + cnt[e]) {
+        sm.order.pick[0] = kMaxPages - 4 * lane - e;
+        sm.order.pick[1] = z - excl;
+      }
+      excl += cnt[e];
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0 && z >= total) {
+      sm.order.pick[0] = 0;
+      sm.order.pick[1] = z - total;
+    }
+  }
+  __syncthreads();
+  const int p = sm.order.pick[0];
+  const int k = sm.order.pick[1];
+  if (!useful(p)) return -1;                // the same decision in every thread
+  // the k-th sequence (by index) with p pages
+  int seen = 0;
+  auto scan = [&](int s, int pc) {          // one pass over kThreads sequences
+    const bool hit = s < batch && pc == p;
+    const uint32_t ballot = __ballot_sync(0xffffffffu, hit);
+    if (lane == 0) sm.order.wsum[warp] = __popc(ballot);
+    __syncthreads();
+    int before = seen, total = 0;
+    #pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      before += w < warp ? sm.order.wsum[w] : 0;
+      total += sm.order.wsum[w];
+    }
+    if (hit && before + __popc(ballot & ((1u << lane) - 1u)) == k) sm.order.pick[2] = s;
+    seen += total;
+    __syncthreads();
+  };
+  #pragma unroll
+  for (int e = 0; e < kHeld; ++e) {
+    if (e * kThreads >= batch || seen > k) break;   // the same decision in every thread
+    scan(e * kThreads + static_cast<int>(threadIdx.x), held[e]);
+  }
+  for (int base = kHeld * kThreads; base < batch && seen <= k; base += kThreads) {
+    const int s = base + static_cast<int>(threadIdx.x);
+    scan(s, s < batch ? page_count(seq_lens[s]) : -1);
+  }
+  return sm.order.pick[2];
+}
+
 // ---------------------------------------------------------------- decode
 // kCluster: the splits of one (sequence, kv head) form one thread-block
 // cluster (gridDim.x == cluster size) and merge through distributed shared
@@ -566,9 +673,22 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
 
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
-  const int b = blockIdx.z;
+  int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if (!kCluster && prm.longest_first) {
+    // a split slot past the last range of a sequence with this many pages
+    // has nothing to do (split 0 always goes on: it reports invalid lengths)
+    auto useful = [&](int pages) {
+      if (split == 0) return true;
+      const int chunk = prm.num_splits > 0 ? (pages + prm.num_splits - 1) / prm.num_splits
+                                           : prm.chunk_pages;
+      return pages > 0 && split < (pages + chunk - 1) / chunk;
+    };
+    b = longest_first_sequence(static_cast<int>(blockIdx.z), static_cast<int>(gridDim.z),
+                               prm.seq_lens, sm, useful);
+    if (b < 0) return;
+  }
 
   // Before griddepcontrol.wait (programmatic dependent launch) this block
   // reads only seq_lens, the block table and pool rows below the appended
@@ -1135,6 +1255,8 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
       static_cast<long long>(cluster ? pool->cluster_blocks_per_sm : pool->blocks_per_sm) *
       pool->num_sms;
   prm.early_trigger = blocks <= resident ? 1 : 0;
+  // more than one wave of ticket-mode blocks: longest sequences first
+  prm.longest_first = (!cluster && num_splits == 0 && blocks > resident) ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid_splits, kHkv, batch);
@@ -1258,6 +1380,7 @@ pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_
   prm.num_splits = num_splits;
   prm.chunk_pages = 0;
   prm.early_trigger = 1;   // launched without programmatic dependent launch: no effect
+  prm.longest_first = 0;
   prm.rope_cos = nullptr;
   prm.rope_sin = nullptr;
   ticket_kernel<false><<<dim3(num_splits, kHkv, batch), block_threads(false), smem_bytes(false),

@@ -377,3 +377,33 @@ def test_long_context_split_counts_full_size(batch, splits):
     ref, _, _ = oracle_step(wl, hk, hv, q_b, kn_b, vn_b, table=table_s, lens=wl.seq_lens.copy(),
                             threads=16)
     assert_close(st.out.cpu().numpy(), ref, f"B={batch} S={splits}")
+
+
+def test_longest_first_order_large_batch():
+    """A batch of 400 ragged sequences (more than one wave of blocks, so the
+    decode launch hands out sequences longest first): every output against
+    the oracle; then one invalid length is flagged while the other
+    sequences still match."""
+    rng = np.random.default_rng(440)
+    lens = rng.integers(1, 300, size=400).astype(np.int32)
+    lens[:5] = [1, 16, 17, 299, 2]
+    wl = W.custom(lens, num_layers=1, seed=441, name="longest-first")
+    st = DeviceState(wl)
+    pool = _pool(wl)
+    pkv.pkv_append_attend(pool, 0, st.q[0], st.k_new[0], st.v_new[0], st.k_pool, st.v_pool,
+                          st.table, st.lens, st.out[0])
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    ref, ok, ov = oracle_step(wl, st.host_k, st.host_v, *_host_inputs(st))
+    assert np.array_equal(bits(st.k_pool), ok) and np.array_equal(bits(st.v_pool), ov)
+    assert_close(st.out.cpu().numpy(), ref, "longest first")
+    # an invalid length: flagged, its rows untouched, the others unchanged
+    bad = st.lens.clone()
+    bad[7] = 0
+    out = torch.full_like(st.out[0], float("nan"))
+    pkv.pkv_decode_attention(pool, 0, st.q[0], st.k_pool, st.v_pool, st.table, bad, out)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_ERR_OUT_OF_RANGE
+    got = out.cpu().numpy()
+    assert np.all(np.isnan(got[7]))
+    keep = np.ones(wl.batch, bool)
+    keep[7] = False
+    assert_close(got[keep], ref[0][keep], "others with one invalid length")
