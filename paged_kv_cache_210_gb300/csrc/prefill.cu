@@ -23,11 +23,12 @@
 //    3-stage ring, so loads run two to three steps ahead; a page's tile is
 //    addressed by its id in the block table, nothing is gathered into a
 //    contiguous buffer;
-//  * an MMA warp (one thread) issues S = Q K^T (M 128, N 64, K 64) one step
-//    ahead into a double-buffered tensor-memory tile and O += P V (M 128,
-//    N 64, K 64) into an FP32 accumulator that stays in tensor memory, as
-//    tcgen05.mma kind::f16 completed on mbarriers through tcgen05.commit,
-//    which also tell the loader when a stage is free;
+//  * a score warp (one thread) issues S = Q K^T (M 128, N 64, K 64) up to
+//    three steps ahead into three tensor-memory tiles, and a value warp (one
+//    thread) issues O += P V (M 128, N 64, K 64) into an FP32 accumulator
+//    that stays in tensor memory, as tcgen05.mma kind::f16 completed on
+//    mbarriers through tcgen05.commit, which also tell the loader when a
+//    stage is free and the score warp when a tile is;
 //  * eight softmax warps, two per tensor-memory lane quarter: each thread
 //    reads its half (32 keys) of its row's scores; online softmax in base 2
 //    whose max moves only when a row's max grows by more than 2^8 (then the
@@ -36,7 +37,7 @@
 //    into tensor memory over the scores they came from, as a BF16 high part
 //    (truncated) and a BF16 low part, and the value product reads them from
 //    there (A operand in tensor memory; ~16 significant bits for P from two
-//    MMAs). The score tiles are double-buffered, so P is too: the softmax
+//    MMAs). With three score tiles P is triple-buffered too: the softmax
 //    warps never wait for the previous value product, except to rescale O.
 //    An mbarrier with one arrival per softmax thread hands P over; the
 //    only block-level syncs in the step loop are two votes among the
@@ -80,12 +81,14 @@ constexpr int kStepPages = kStepKeys / kPage;        // 4
 constexpr int kSoftmaxWarps = 8;                     // two per tensor-memory lane quarter
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kLoadWarp = kSoftmaxWarps;             // TMA copies
-constexpr int kMmaWarp = kSoftmaxWarps + 1;          // tensor-core products
-constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kScoreWarp = kSoftmaxWarps + 1;        // S = Q K^T products
+constexpr int kValueWarp = kSoftmaxWarps + 2;        // O += P V products
+constexpr int kThreads = kSoftmaxThreads + 96;
 constexpr int kKStages = 4;                          // K ring
 constexpr int kVStages = 3;                          // V ring
-constexpr uint32_t kTmemCols = 256;                  // S: 0..63 and 64..127, O: 128..191
-constexpr uint32_t kTmemO = 128;
+constexpr int kSTiles = 3;                           // score (then P) tiles in tensor memory
+constexpr uint32_t kTmemCols = 256;                  // S/P tiles: 0..191, O: 192..255
+constexpr uint32_t kTmemO = kSTiles * 64;
 constexpr float kRescaleLog2 = 8.f;                  // lazy max: p <= 2^8
 constexpr long long kWaitCycles = 4000000000LL;      // about two seconds
 
@@ -93,8 +96,8 @@ struct PrefillSmem {                                 // every tile 1024-byte ali
   uint8_t q[kRows * kRowBytes];                      // 16 KiB
   uint8_t k[kKStages][kStepKeys * kRowBytes];        // 4 x 8 KiB
   uint8_t v[kVStages][kStepKeys * kRowBytes];        // 3 x 8 KiB
-  unsigned long long bar_q, bar_k[kKStages], bar_v[kVStages], bar_s[2], bar_p, bar_o;
-  unsigned long long p_free[2];                      // tile (S, then P) read by its value product
+  unsigned long long bar_q, bar_k[kKStages], bar_v[kVStages], bar_s[kSTiles], bar_p[kSTiles], bar_o;
+  unsigned long long p_free[kSTiles];                // tile (S, then P) read by its value product
   unsigned long long k_free[kKStages], v_free[kVStages];   // stage read by its product
   uint32_t tmem_base;
   int abort_flag;
@@ -187,13 +190,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1,
-                                            int c2, int c3, unsigned long long* bar) {
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            unsigned long long* bar) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
-        "r"(c3), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+        "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -418,12 +421,13 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
     mbar_init(&sm.bar_q, 1);
     for (int i = 0; i < kKStages; ++i) mbar_init(&sm.bar_k[i], 1);
     for (int i = 0; i < kVStages; ++i) mbar_init(&sm.bar_v[i], 1);
-    mbar_init(&sm.bar_s[0], 1);
-    mbar_init(&sm.bar_s[1], 1);
-    mbar_init(&sm.bar_p, kSoftmaxThreads);
+    for (int i = 0; i < kSTiles; ++i) mbar_init(&sm.bar_s[i], 1);
+    // P(j) ready, one barrier per tile: the softmax warps may run up to two
+    // steps ahead of the value products, and a parity wait must never see
+    // two completed phases of one barrier
+    for (int i = 0; i < kSTiles; ++i) mbar_init(&sm.bar_p[i], kSoftmaxThreads);
     mbar_init(&sm.bar_o, 1);
-    mbar_init(&sm.p_free[0], 1);
-    mbar_init(&sm.p_free[1], 1);
+    for (int i = 0; i < kSTiles; ++i) mbar_init(&sm.p_free[i], 1);
     for (int i = 0; i < kKStages; ++i) mbar_init(&sm.k_free[i], 1);
     for (int i = 0; i < kVStages; ++i) mbar_init(&sm.v_free[i], 1);
     sm.abort_flag = 0;
@@ -467,7 +471,9 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
       if (ok && lane < kStepPages) {
         const int lp = j * kStepPages + lane;
         const int page = lp < n_pages ? sm.pages[lp] : -1;
-        if (page >= 0) tma_load_4d(dst + lane * kPage * kRowBytes, map, 0, 0, g, page, bar);
+        // the pool seen as rows of 64 dims: (page, kv head, token) -> row
+        if (page >= 0)
+          tma_load_2d(dst + lane * kPage * kRowBytes, map, 0, (page * kHkv + g) * kPage, bar);
       }
       __syncwarp();
       return ok;
@@ -504,79 +510,80 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
         if (uses > 0) mbar_wait(&sm.bar_v[st], (uses - 1) & 1);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kScoreWarp || warp == kValueWarp) {
     // ------------------------------------------------------------ tensor cores
+    // Two issuing threads, one for the score products and one for the value
+    // products (a tcgen05.commit tracks the products of its own thread), so
+    // scores can run ahead while the value products wait for P.
     if (lane_of(tid) == 0) {
-      const uint32_t idesc_s = instr_desc(kRows, kStepKeys, false);
-      const uint32_t idesc_o = instr_desc(kRows, kDim, true);
-      const uint64_t q_desc = smem_desc_sw128(smem_u32(sm.q), 16, 1024);
-      int s_issued = 0, o_issued = 0;
-      // the descriptor's start address counts 16-byte units: + bytes >> 4
-      // S(j) = Q K(j)^T into tile j & 1, once K(j) landed and the value
-      // product of P(j - 2), which the softmax warps wrote over S(j - 2) in
-      // that tile, is done
-      auto issue_s = [&](int j) -> bool {
-        if (!mbar_wait(&sm.bar_k[j % kKStages], (j / kKStages) & 1)) return false;
-        if (j >= 2 && !mbar_wait(&sm.p_free[j & 1], ((j - 2) >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t k_desc = smem_desc_sw128(smem_u32(sm.k[j % kKStages]), 16, 1024);
-        #pragma unroll
-        for (int kk = 0; kk < kDim / 16; ++kk)
-          mma_bf16(tmem + (j & 1) * kStepKeys, q_desc + kk * 2, k_desc + kk * 2, idesc_s, kk > 0);
-        mma_commit(&sm.bar_s[j & 1]);
-        mma_commit(&sm.k_free[j % kKStages]);
-        ++s_issued;
-        return true;
-      };
-      // O += P(j) V(j): P from tensor memory (tile j & 1: high part in
-      // columns 0..31, low part in 32..63, 16 keys per 8 columns)
-      auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(&sm.bar_p, j & 1) ||
-            !mbar_wait(&sm.bar_v[j % kVStages], (j / kVStages) & 1))
-          return false;
-        tc_fence_after();
-        const uint64_t v_desc = smem_desc_sw128(smem_u32(sm.v[j % kVStages]), 8192, 1024);
-        const uint32_t p_tile = tmem + (j & 1) * kStepKeys;
-        #pragma unroll
-        for (int kk = 0; kk < kStepKeys / 16; ++kk)
-          mma_bf16_tmem_a(tmem + kTmemO, p_tile + kk * 8, v_desc + kk * (16 * kRowBytes >> 4),
-                          idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-        #pragma unroll
-        for (int kk = 0; kk < kStepKeys / 16; ++kk)
-          mma_bf16_tmem_a(tmem + kTmemO, p_tile + 32 + kk * 8, v_desc + kk * (16 * kRowBytes >> 4),
-                          idesc_o, 1u);
-        mma_commit(&sm.bar_o);
-        mma_commit(&sm.v_free[j % kVStages]);
-        mma_commit(&sm.p_free[j & 1]);
-        ++o_issued;
-        return true;
-      };
-      bool ok = mbar_wait(&sm.bar_q, 0);
-      // S one step ahead of the value product: S(j), then P(j - 1) V(j - 1)
-      for (int j = 0; ok && j <= n_steps; ++j) {
-        if (*abort_flag) {
-          ok = false;
-          break;
+      const bool scores = warp == kScoreWarp;
+      int issued = 0;
+      bool ok = true;
+      if (scores) {
+        const uint32_t idesc_s = instr_desc(kRows, kStepKeys, false);
+        const uint64_t q_desc = smem_desc_sw128(smem_u32(sm.q), 16, 1024);
+        ok = mbar_wait(&sm.bar_q, 0);
+        for (int j = 0; ok && j < n_steps; ++j) {
+          // S(j) = Q K(j)^T into tile j % 3, once K(j) landed and the value
+          // product of P(j - 3), written over S(j - 3) in that tile, is done
+          if (*abort_flag || !mbar_wait(&sm.bar_k[j % kKStages], (j / kKStages) & 1) ||
+              (j >= kSTiles &&
+               !mbar_wait(&sm.p_free[j % kSTiles], ((j - kSTiles) / kSTiles) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t k_desc = smem_desc_sw128(smem_u32(sm.k[j % kKStages]), 16, 1024);
+          // the descriptor's start address counts 16-byte units: + bytes >> 4
+          #pragma unroll
+          for (int kk = 0; kk < kDim / 16; ++kk)
+            mma_bf16(tmem + (j % kSTiles) * kStepKeys, q_desc + kk * 2, k_desc + kk * 2, idesc_s,
+                     kk > 0);
+          mma_commit(&sm.bar_s[j % kSTiles]);
+          mma_commit(&sm.k_free[j % kKStages]);
+          ++issued;
         }
-        if (j < n_steps && !issue_s(j)) {
-          ok = false;
-          break;
-        }
-        if (j > 0 && !issue_pv(j - 1)) {
-          ok = false;
-          break;
+      } else {
+        const uint32_t idesc_o = instr_desc(kRows, kDim, true);
+        for (int j = 0; ok && j < n_steps; ++j) {
+          // O += P(j) V(j): P from tensor memory (tile j % 3: high part in
+          // columns 0..31, low part in 32..63, 16 keys per 8 columns), once
+          // the softmax warps handed it over and V(j) landed
+          if (*abort_flag || !mbar_wait(&sm.bar_p[j % kSTiles], (j / kSTiles) & 1) ||
+              !mbar_wait(&sm.bar_v[j % kVStages], (j / kVStages) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t v_desc = smem_desc_sw128(smem_u32(sm.v[j % kVStages]), 8192, 1024);
+          const uint32_t p_tile = tmem + (j % kSTiles) * kStepKeys;
+          #pragma unroll
+          for (int kk = 0; kk < kStepKeys / 16; ++kk)
+            mma_bf16_tmem_a(tmem + kTmemO, p_tile + kk * 8, v_desc + kk * (16 * kRowBytes >> 4),
+                            idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          #pragma unroll
+          for (int kk = 0; kk < kStepKeys / 16; ++kk)
+            mma_bf16_tmem_a(tmem + kTmemO, p_tile + 32 + kk * 8,
+                            v_desc + kk * (16 * kRowBytes >> 4), idesc_o, 1u);
+          mma_commit(&sm.bar_o);
+          mma_commit(&sm.v_free[j % kVStages]);
+          mma_commit(&sm.p_free[j % kSTiles]);
+          ++issued;
         }
       }
       if (!ok) {
         *abort_flag = 1;
         set_error(prm.err, PKV_DEV_ERR_TIMEOUT);
       }
-      // every product issued completes before the CTA frees its memory
-      for (int b2 = 0; b2 < 2; ++b2) {
-        const int uses = (s_issued - b2 + 1) / 2;
-        if (uses > 0) mbar_wait(&sm.bar_s[b2], (uses - 1) & 1);
+      // every product this thread issued completes before the CTA frees its memory
+      if (scores) {
+        for (int t = 0; t < kSTiles; ++t) {
+          const int uses = (issued - t + kSTiles - 1) / kSTiles;
+          if (uses > 0) mbar_wait(&sm.bar_s[t], (uses - 1) & 1);
+        }
+      } else if (issued > 0) {
+        mbar_wait(&sm.bar_o, (issued - 1) & 1);
       }
-      if (o_issued > 0) mbar_wait(&sm.bar_o, (o_issued - 1) & 1);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -591,10 +598,11 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
     for (int j = 0; j < n_steps; ++j) {
       // (a failed wait is voted on with the other softmax threads below, so
       // that every one of them leaves the loop at the same step)
-      bool failed = *abort_flag != 0 || !mbar_wait(&sm.bar_s[j & 1], (j >> 1) & 1);
+      bool failed = *abort_flag != 0 ||
+                    !mbar_wait(&sm.bar_s[j % kSTiles], (j / kSTiles) & 1);
       tc_fence_after();
       uint32_t sv[32];                                   // this half's 32 keys of the step
-      tmem_ld32(tmem + lane_addr + (j & 1) * kStepKeys + half * 32, sv);
+      tmem_ld32(tmem + lane_addr + (j % kSTiles) * kStepKeys + half * 32, sv);
 
       const int key0 = j * kStepKeys + half * 32;
       if (key0 + 31 > p_first) {                         // some key hidden from some row
@@ -687,12 +695,12 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
         break;
       }
       tc_fence_after();
-      const uint32_t p_tile = tmem + lane_addr + (j & 1) * kStepKeys;
+      const uint32_t p_tile = tmem + lane_addr + (j % kSTiles) * kStepKeys;
       tmem_st16(p_tile + half * 16, hi);
       tmem_st16(p_tile + 32 + half * 16, lo);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&sm.bar_p);
+      mbar_arrive(&sm.bar_p[j % kSTiles]);
     }
     if (!ok) {
       *abort_flag = 1;
@@ -832,12 +840,11 @@ pkv_status launch_attention(pkv_pool_t pool, int layer, const void* q, const voi
     if (!encode_bf16(&tq, q, 3, dims, strides, box)) return PKV_ERR_CUDA;
   }
   {
-    const cuuint64_t dims[4] = {kDim, kPage, kHkv, static_cast<cuuint64_t>(c.num_pages)};
-    const cuuint64_t strides[3] = {kRowBytes, static_cast<cuuint64_t>(kPage) * kRowBytes,
-                                   static_cast<cuuint64_t>(kHkv) * kPage * kRowBytes};
-    const cuuint32_t box[4] = {kDim, kPage, 1, 1};
-    if (!encode_bf16(&tk, k_pool, 4, dims, strides, box)) return PKV_ERR_CUDA;
-    if (!encode_bf16(&tv, v_pool, 4, dims, strides, box)) return PKV_ERR_CUDA;
+    const cuuint64_t dims[2] = {kDim, static_cast<cuuint64_t>(c.num_pages) * kHkv * kPage};
+    const cuuint64_t strides[1] = {kRowBytes};
+    const cuuint32_t box[2] = {kDim, kPage};
+    if (!encode_bf16(&tk, k_pool, 2, dims, strides, box)) return PKV_ERR_CUDA;
+    if (!encode_bf16(&tv, v_pool, 2, dims, strides, box)) return PKV_ERR_CUDA;
   }
   const int stride = c.max_seq_len / kPage;
   PrefillParams prm;
