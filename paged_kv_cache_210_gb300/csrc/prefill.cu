@@ -96,7 +96,8 @@ struct PrefillSmem {                                 // every tile 1024-byte ali
   uint8_t q[kRows * kRowBytes];                      // 16 KiB
   uint8_t k[kKStages][kStepKeys * kRowBytes];        // 4 x 8 KiB
   uint8_t v[kVStages][kStepKeys * kRowBytes];        // 3 x 8 KiB
-  unsigned long long bar_q, bar_k[kKStages], bar_v[kVStages], bar_s[kSTiles], bar_p[kSTiles], bar_o;
+  unsigned long long bar_q, bar_k[kKStages], bar_v[kVStages], bar_s[kSTiles], bar_p[kSTiles];
+  unsigned long long bar_o[kSTiles];   // P(j) V(j) (and every earlier product) done, per tile
   unsigned long long p_free[kSTiles];                // tile (S, then P) read by its value product
   unsigned long long k_free[kKStages], v_free[kVStages];   // stage read by its product
   uint32_t tmem_base;
@@ -426,7 +427,10 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
     // steps ahead of the value products, and a parity wait must never see
     // two completed phases of one barrier
     for (int i = 0; i < kSTiles; ++i) mbar_init(&sm.bar_p[i], kSoftmaxThreads);
-    mbar_init(&sm.bar_o, 1);
+    // one per tile as well: the softmax warps may be two value products
+    // ahead, and a parity wait on a single barrier could then return for an
+    // older product
+    for (int i = 0; i < kSTiles; ++i) mbar_init(&sm.bar_o[i], 1);
     for (int i = 0; i < kSTiles; ++i) mbar_init(&sm.p_free[i], 1);
     for (int i = 0; i < kKStages; ++i) mbar_init(&sm.k_free[i], 1);
     for (int i = 0; i < kVStages; ++i) mbar_init(&sm.v_free[i], 1);
@@ -565,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
           for (int kk = 0; kk < kStepKeys / 16; ++kk)
             mma_bf16_tmem_a(tmem + kTmemO, p_tile + 32 + kk * 8,
                             v_desc + kk * (16 * kRowBytes >> 4), idesc_o, 1u);
-          mma_commit(&sm.bar_o);
+          mma_commit(&sm.bar_o[j % kSTiles]);
           mma_commit(&sm.v_free[j % kVStages]);
           mma_commit(&sm.p_free[j % kSTiles]);
           ++issued;
@@ -582,7 +586,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
           if (uses > 0) mbar_wait(&sm.bar_s[t], (uses - 1) & 1);
         }
       } else if (issued > 0) {
-        mbar_wait(&sm.bar_o, (issued - 1) & 1);
+        // the last product's commit covers every earlier one of this thread
+        mbar_wait(&sm.bar_o[(issued - 1) % kSTiles], ((issued - 1) / kSTiles) & 1);
       }
     }
   } else {
@@ -661,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
       // a row that grew its max rescales O, once P(j - 1) V(j - 1) is done
       // (P(j) V(j) cannot start before this thread hands over P(j))
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        failed |= !mbar_wait(&sm.bar_o, (j - 1) & 1);
+        failed |= !mbar_wait(&sm.bar_o[(j - 1) % kSTiles], ((j - 1) / kSTiles) & 1);
         tc_fence_after();
         if (!failed) {
           uint32_t ov[32];
@@ -709,7 +714,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
     // the two halves' sums of each row meet in shared memory
     sm.lsum[half][r] = l_half;
     softmax_warps_sync();
-    if (ok && !*abort_flag && mbar_wait(&sm.bar_o, (n_steps - 1) & 1)) {
+    if (ok && !*abort_flag &&
+        mbar_wait(&sm.bar_o[(n_steps - 1) % kSTiles], ((n_steps - 1) / kSTiles) & 1)) {
       tc_fence_after();
       uint32_t ov[32];
       tmem_ld32(tmem + lane_addr + kTmemO + half * 32, ov);

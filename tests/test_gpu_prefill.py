@@ -181,3 +181,26 @@ def test_host_argument_errors():
     with pytest.raises(pkv.PkvError):
         pkv.pkv_prefill(pool, 0, st.qd[0], st.kd[0], st.vd[0], st.k_pool, st.v_pool, st.table,
                         st.cu, st.start, odd, 1)
+
+
+def test_late_large_scores_rescale_o():
+    """Key rows at positions 200..215 and 700..703 scaled by 16 (exact in
+    BF16): every later query's row max jumps by far more than the kernel's
+    2^8 lazy threshold several steps into the key range, so O is rescaled in
+    tensor memory mid-sequence; the result must still match the oracle."""
+    wl = W.prefill([900, 257], [0, 150], num_layers=1, seed=708, name="rescale")
+    st = State(wl)
+    k = st.k.clone()
+    cu = wl.cu_tokens
+    for b in range(wl.batch):
+        for pos in list(range(200, 216)) + list(range(700, 704)):
+            i = pos - int(wl.start_pos[b])
+            if 0 <= i < int(wl.chunk_lens[b]):
+                k[0, cu[b] + i] = k[0, cu[b] + i] * 16
+    st.k, st.kd = k, k.cuda()
+    pool = pkv.pkv_pool_create(1, wl.num_pages, wl.batch)
+    run(st, pool)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    ref, ok, ov = oracle_prefill(st)
+    assert np.array_equal(bits(st.k_pool.cpu()), ok)
+    assert_close(st.out.cpu().numpy(), ref, "late large scores")
