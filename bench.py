@@ -80,19 +80,29 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0}, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "decode": ("paged_kv_cache_210_gb300/csrc/pkv.cu",),
+    "prefill": ("paged_kv_cache_210_gb300/csrc/prefill.cu", "include/pkv_prefill.h"),
+}
+
+
+def kernel_source_hash(component="decode"):
+    """First 16 hex digits of the SHA-256 over the sources one kernel family is
+    compiled from (its .cu file, the shared device and pool headers, pkv.h)."""
     h = hashlib.sha256()
-    for rel in ("paged_kv_cache_210_gb300/csrc/pkv.cu", "paged_kv_cache_210_gb300/csrc/pool_internal.h",
-                "include/pkv.h"):
+    for rel in KERNEL_SOURCES[component] + ("paged_kv_cache_210_gb300/csrc/device_common.cuh",
+                                            "paged_kv_cache_210_gb300/csrc/pool_internal.h",
+                                            "include/pkv.h"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
-    or None when there is none for this kernel source and workload."""
-    path = os.path.join(ROOT, "profiles", f"decode_fused_{workload}.md")
+def recorded_traffic(profile, component="decode"):
+    """DRAM bytes per launch of a kernel from its committed ncu summary
+    (profiles/<profile>.md), or None when there is none for the current
+    kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{profile}.md")
     if not os.path.exists(path):
         return None
     fields = {}
@@ -101,7 +111,7 @@ def recorded_traffic(workload):
             if line.startswith("- ") and ": " in line:
                 k, v = line[2:].split(": ", 1)
                 fields[k.strip()] = v.strip().strip("`")
-    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+    if fields.get("kernel_source_sha256_16") != kernel_source_hash(component):
         return None
     try:
         return int(float(fields["dram_bytes_per_launch"]))
@@ -318,16 +328,24 @@ def run_ours(args, world, rank, local):
         return flush_buf.sum()
 
     stream = torch.cuda.Stream(device=dev)
-    made = [make_event() for _ in range(L + 3)]
+    launches = 1 if args.persistent else L        # kernel launches per step
+    made = [make_event() for _ in range(launches + 3)]
     external = all(e[1] for e in made)
-    events = [e[0] for e in made[:L + 1]]       # between the launches (per-launch pass)
-    t_start, t_end = made[L + 1][0], made[L + 2][0]
+    events = [e[0] for e in made[:launches + 1]]   # between the launches (per-launch pass)
+    t_start, t_end = made[launches + 1][0], made[launches + 2][0]
 
     def step(marks=None):
-        """The 16 launches; `marks` = events recorded before, between and after."""
+        """The 16 launches (or the one multi-layer launch); `marks` = events
+        recorded before, between and after."""
         s = torch.cuda.current_stream()
         if marks:
             marks[0].record(s)
+        if args.persistent:
+            pkv.pkv_append_attend_layers(pool, 0, q, k_new, v_new, k_pool, v_pool, table, lens,
+                                         out, stream=s)
+            if marks:
+                marks[-1].record(s)
+            return
         for layer in range(L):
             if args.rope:
                 pkv.pkv_append_attend_rope(pool, layer, q[layer], k_new[layer], v_new[layer],
@@ -416,10 +434,10 @@ def run_ours(args, world, rank, local):
     launch_ms, launch_step_ms = [], []
     if external:
         for _ in range(max(3, min(args.steps, 400))):
-            replay_timed(launch_graph, events[0], events[L])
+            replay_timed(launch_graph, events[0], events[launches])
             stream.synchronize()
-            launch_ms.extend(events[i].elapsed_time(events[i + 1]) for i in range(L))
-            launch_step_ms.append(events[0].elapsed_time(events[L]))
+            launch_ms.extend(events[i].elapsed_time(events[i + 1]) for i in range(launches))
+            launch_step_ms.append(events[0].elapsed_time(events[launches]))
 
     # e2e steps (host buffers, copies inside the timed events)
     e2e_ms = []
@@ -439,11 +457,22 @@ def run_ours(args, world, rank, local):
 
     # average launch duration: the timed region's events / launches (includes
     # the graph's gaps between launches, so an upper bound on kernel time)
-    per_launch_ms = ms_per_step / L
-    launch_source = "timed-region CUDA events (start/end of each step) / 16 launches"
+    per_launch_ms = ms_per_step / launches
+    launch_source = (f"timed-region CUDA events (start/end of each step) / {launches} launch"
+                     + ("es" if launches > 1 else ""))
     events_between = (round(statistics.mean(launch_ms), 6) if launch_ms else None)
-    achieved = (nbytes / L) / (per_launch_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload + ("-rope" if args.rope else ""))
+    achieved = (nbytes / launches) / (per_launch_ms * 1e-3) / 1e9
+    if args.persistent:
+        kernel_name = "decode_layers_kernel"
+        traffic = recorded_traffic("decode_layers_" + args.workload)
+        step_note = ("16 layers of fused append+attend in one persistent launch (per-sequence "
+                     "layer order kept by device-side waits), CUDA graph")
+    else:
+        kernel_name = "decode_kernel<fused>"
+        traffic = recorded_traffic("decode_fused_" + args.workload +
+                                   ("-rope" if args.rope else ""))
+        step_note = ("16 x fused append+attend (one launch per layer), CUDA graph" +
+                     ("" if args.no_pdl else ", programmatic dependent launch between layers"))
 
     if rank != 0:
         return
@@ -457,8 +486,7 @@ def run_ours(args, world, rank, local):
             "workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
             "batch": B, "layers": L, "seq_lens": "all 2048" if np.all(wl.seq_lens == 2048)
             else f"mean {float(wl.seq_lens.mean()):.1f}",
-            "step": "16 x fused append+attend (one launch per layer), CUDA graph" +
-                    ("" if args.no_pdl else ", programmatic dependent launch between layers"),
+            "step": step_note,
             "splits": chunk_note,
             "rope": f"key and queries rotated in the launch, base {ROPE_BASE:g}" if args.rope
                     else "none (keys arrive rotated)",
@@ -475,15 +503,15 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_total / len(e2e_ms), 5)},
-        "gpu_launches": L * args.steps,
+        "gpu_launches": launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "traffic": traffic, "kernel": "decode_kernel<fused>",
+                     "traffic": traffic, "kernel": kernel_name,
                      "per_launch_ms": round(per_launch_ms, 6), "per_launch_source": launch_source,
                      "per_launch_ms_with_events_between_launches": events_between,
-                     "bytes_per_launch": nbytes // L},
+                     "bytes_per_launch": nbytes // launches},
         "wall_s_timed_loop": round(wall, 3),
     }
     if not args.no_cpu_baseline:
@@ -720,7 +748,8 @@ def run_prefill_bench(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{kind} cuBLAS bf16 burst (MEASURED_PEAKS bf16_tflops)",
-                     "traffic": None, "kernel": "prefill_attention_kernel",
+                     "traffic": recorded_traffic(f"prefill_attention_{wl.name}", "prefill"),
+                     "kernel": "prefill_attention_kernel",
                      "per_launch_ms": round(attn_launch_ms, 5),
                      "fill_per_launch_ms": round(float(np.mean(fill_ms)), 5) if fill_ms else None},
     }
@@ -760,12 +789,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rope", action="store_true",
                     help="rotate the appended key and the queries inside the launches")
+    ap.add_argument("--persistent", action="store_true",
+                    help="decode: all 16 layers in one persistent launch "
+                         "(pkv_append_attend_layers)")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch")
     ap.add_argument("--component", choices=["decode", "scheduler", "prefill"], default="decode",
                     help="scheduler: the host admission scheduler; prefill: prefill over pages")
     ap.add_argument("--prompt-len", type=int, default=2048, help="prefill prompt length")
     args = ap.parse_args()
+    if args.persistent and args.rope:
+        ap.error("--persistent runs the unrotated fused step; drop --rope")
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.component == "scheduler":

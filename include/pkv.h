@@ -195,6 +195,43 @@ pkv_status pkv_append_attend_rope(pkv_pool_t pool, int layer, const void* q, con
                                   const float* rope_cos, const float* rope_sin, float* out,
                                   int batch, int num_splits, void* stream);
 
+/* Several consecutive layers of the fused step in one launch. A decode step
+ * runs the attention of every one of the model's 16 layers for each new
+ * token [6 Hours of YouTube and 85 handtyped pages of notes on LLM Inference
+ * - Start here, README feature list: the fixed 16-layer Llama 3.2 1B layout
+ * and the batched decode bullet]; at small batches each layer's work is a few
+ * microseconds, so the per-layer launch and the wait for the previous
+ * layer's completion dominate, and one persistent launch removes them.
+ *
+ * For j = 0 .. num_layers - 1 the same results (pool contents and out) as
+ *   pkv_append_attend(pool, layer_begin + j, q_j, k_j, v_j, k_pool, v_pool,
+ *                     block_tables, seq_lens, out_j, batch, 0, stream)
+ * in order of j, where q is [num_layers][batch][32][64] BF16 (q_j its j-th
+ * slab), k and v [num_layers][batch][8][64] BF16 and out
+ * [num_layers][batch][32][64] FP32; seq_lens (the post-append length) holds
+ * for every layer. Layers keep their order per sequence: the blocks of
+ * sequence b read q_j, k_j, v_j and write the appended slot of layer j only
+ * after every output row of b at layer j - 1 has been written, the order a
+ * model imposes between layers; pages of cached tokens, which no layer of
+ * the call writes, are read ahead across the layer boundary.
+ *
+ * Plan: one thread-block cluster of S blocks per (sequence, kv head), S the
+ * largest of 16, 8, 4, 2 for which every cluster of the grid is resident at
+ * once; the blocks of a sequence then wait for one another between layers
+ * (bounded: a wait that gives up flags PKV_ERR_DEVICE_TIMEOUT and the block
+ * carries on without waiting). A launch covers at most 512 / ceil(128 / S)
+ * layers (64 at S = 16, 8 at S = 2); longer calls are split into several. A
+ * batch for which even S = 2 does not fit runs as one pkv_append_attend launch
+ * per layer. Uses a per-sequence counter in the handle (zeroed on the stream
+ * before each launch), so one handle serves one such call at a time.
+ * Errors as for pkv_append_attend; layer_begin + num_layers must not exceed
+ * num_layers of the handle. num_layers == 0 or batch == 0 is a no-op. */
+pkv_status pkv_append_attend_layers(pkv_pool_t pool, int layer_begin, int num_layers,
+                                    const void* q, const void* k, const void* v, void* k_pool,
+                                    void* v_pool, const int32_t* block_tables,
+                                    const int32_t* seq_lens, float* out, int batch,
+                                    void* stream);
+
 /* Synchronises `stream`, then returns and clears the sticky device error
  * flag: PKV_OK, PKV_ERR_OUT_OF_RANGE or PKV_ERR_DEVICE_TIMEOUT (or CUDA if
  * the synchronisation itself failed). */

@@ -35,22 +35,19 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pkv.h"
+#include "device_common.cuh"
 #include "pool_internal.h"
+
+using namespace pkv_dev;
 
 namespace {
 
-constexpr int kPage = 16;
-constexpr int kHq = 32;
-constexpr int kHkv = 8;
-constexpr int kGroup = kHq / kHkv;
-constexpr int kDim = 64;
-constexpr int kMaxSeqLen = 2048;
-constexpr int kMaxPages = kMaxSeqLen / 16;
-constexpr int kRowBytes = kDim * 2;             // one token of one kv head: 128 B
 constexpr int kTileBytes = kPage * kRowBytes;   // one (page, kv head) tile: 2 KiB
+
 // Block shapes: 4 warps with 3 page stages per warp. The ticket-merge kernel
 // fits 4 blocks per SM (128 registers); the cluster-merge kernel (plus its
 // inbox) 3, so it may use up to 168 registers, and 3 per SM
@@ -72,8 +69,6 @@ constexpr int kErrPosition = PKV_DEV_ERR_POSITION;
 constexpr int kErrSeqLen = PKV_DEV_ERR_SEQ_LEN;
 constexpr int kErrTimeout = PKV_DEV_ERR_TIMEOUT;
 
-// about two seconds at the maximum SM clock
-constexpr long long kWaitCycles = 4000000000LL;
 
 template <int kStages>
 struct alignas(16) WarpSmem {
@@ -143,55 +138,6 @@ struct DecodeParams {
 };
 
 // ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// One try_wait on an mbarrier phase. The thread may sleep inside it until the
-// phase completes, for at most the hint (10 ms), so a waiting warp takes no
-// issue slots from the warps that compute.
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
-  constexpr uint32_t kSuspendHintNs = 10000000;
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-  return done != 0;
-}
-
-// Bounded wait on an mbarrier phase: false after about two seconds.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - start > kWaitCycles) return false;
-  }
-  return true;
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
 // Thread-block cluster barrier, split: arrive (release) and wait (acquire).
 // A wait completes once every non-exited thread of the cluster has arrived.
 __device__ __forceinline__ void cluster_arrive_release() {
@@ -253,14 +199,6 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Two FP32 values -> BF16 pair (element 0 in the low half), each rounded to
-// nearest, ties to even.
-__device__ __forceinline__ uint32_t float2_to_bf16x2(float e0, float e1) {
-  uint32_t w;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(e1), "f"(e0));
-  return w;
-}
-
 // cos (or sin) of the 8 rotary angles 8 c4 .. 8 c4 + 7 of one position row.
 __device__ __forceinline__ void load_angles(const float* row, int c4, float (&v)[8]) {
   const float4 a = __ldg(reinterpret_cast<const float4*>(row + 8 * c4));
@@ -298,22 +236,11 @@ __device__ __forceinline__ uint4 shfl_xor_uint4(uint4 v, int m) {
                     __shfl_xor_sync(0xffffffffu, v.z, m), __shfl_xor_sync(0xffffffffu, v.w, m));
 }
 
-// 2^x by the SFU's approximate exponential (PTX ex2.approx.ftz.f32: relative
-// error about 2^-22; results below 2^-126, i.e. softmax weights that cannot
-// contribute, flush to zero; 2^-inf = 0).
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return __ffma2_rn(a, b, c);
 }
 
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-
-__device__ __forceinline__ void set_error(int* err, int bits) { atomicOr(err, bits); }
 
 // ---------------------------------------------------------------- append
 // One block of 128 threads per sequence: thread t copies 16-byte chunk
@@ -558,6 +485,120 @@ __device__ __forceinline__ void reduce_warp_state(WarpState& st) {
       st.acc[g][h].x += __shfl_xor_sync(0xffffffffu, st.acc[g][h].x, 16);
       st.acc[g][h].y += __shfl_xor_sync(0xffffffffu, st.acc[g][h].y, 16);
     }
+  }
+}
+
+// ---------------------------------------------------------------- merges
+// Cluster merge of the S blocks of one (sequence, kv head) (S = the cluster
+// size): each warp stores its (m, l, o) for head g straight into the inbox of
+// the head's leader, block g mod S of the cluster; every thread arrives on the
+// cluster barrier, and each leader waits for all arrivals and combines its
+// heads into out_kv ([4][64], the kv head's query heads). A block that leads
+// no head returns after its arrival, or, with `wait_always` (blocks that go
+// on to use the cluster barrier again), after the wait as well.
+template <int kWarps, int kStages>
+__device__ __forceinline__ void cluster_merge(BlockSmem<kWarps, kStages>& sm, ClusterInbox& inbox,
+                                              const WarpState& st, const LaneRoles& rl, int warp,
+                                              int lane, float* out_kv, bool wait_always) {
+  static_assert(kWarps * kMaxClusterSize <= kInboxSlots, "inbox slots");
+  const int S = gridDim.x;
+  const int rank = static_cast<int>(cluster_rank());
+  const int slot = rank * kWarps + warp;
+  if (rl.tp == 0) {
+    const int at = (rl.gh / S) * (S * kWarps) + slot;
+    st_cluster(&inbox.m[at], rl.gh % S, st.m_run);
+    st_cluster(&inbox.l[at], rl.gh % S, st.l_run);
+  }
+  if (rl.tpar == 0) {
+    #pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      const int at = (g / S) * (S * kWarps) + slot;
+      st_cluster4(&inbox.o[at][4 * rl.dq], g % S,
+                  make_float4(st.acc[g][0].x, st.acc[g][0].y, st.acc[g][1].x, st.acc[g][1].y));
+    }
+  }
+  cluster_arrive_release();
+  if (rank >= kGroup) {   // leads no head
+    if (wait_always) cluster_wait_acquire();
+    return;
+  }
+  cluster_wait_acquire();
+  // combine: warp qq sums the slots p = qq, qq + 4, ... of a head for dims
+  // (d0, d0 + 1); the four warps' sums meet in shared memory
+  const int parts = S * kWarps;
+  const int qq = warp;
+  const int d0 = 2 * lane;
+  for (int hg = rank; hg < kGroup; hg += S) {
+    const int base = (hg / S) * parts;
+    float mx = -INFINITY;
+    for (int p = lane; p < parts; p += 32) mx = fmaxf(mx, inbox.m[base + p]);
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float LL = 0.f;
+    float2 OO = make_float2(0.f, 0.f);
+    #pragma unroll 4
+    for (int p = qq; p < parts; p += kWarps) {
+      const float mp = inbox.m[base + p];
+      const float w = mp == -INFINITY ? 0.f : fast_exp2(mp - mx);
+      const float2 op = *reinterpret_cast<const float2*>(&inbox.o[base + p][d0]);
+      LL += w * inbox.l[base + p];
+      OO.x += w * op.x;
+      OO.y += w * op.y;
+    }
+    sm.acc[qq][0][d0] = OO.x;
+    sm.acc[qq][0][d0 + 1] = OO.y;
+    if (lane == 0) sm.l[qq][0] = LL;
+    __syncthreads();
+    if (qq == 0) {
+      float L4 = 0.f, ox = 0.f, oy = 0.f;
+      #pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        L4 += sm.l[w][0];
+        ox += sm.acc[w][0][d0];
+        oy += sm.acc[w][0][d0 + 1];
+      }
+      const float inv = L4 > 0.f ? 1.f / L4 : 0.f;
+      *reinterpret_cast<float2*>(out_kv + hg * kDim + d0) = make_float2(ox * inv, oy * inv);
+    }
+    __syncthreads();
+  }
+}
+
+// The block's warps merged in shared memory: thread t < 128 gets the
+// log-sum-exp state of head g = (t / 32) % 4 for dims d0 = 2 (t % 32), d0 + 1
+// (M: max, L: sum, O: unnormalised output); the rest of an 8-warp block
+// computes an alias.
+template <int kWarps, int kStages>
+__device__ __forceinline__ void block_merge(BlockSmem<kWarps, kStages>& sm, const WarpState& st,
+                                            const LaneRoles& rl, int warp, float& M, float& L,
+                                            float2& O) {
+  if (rl.tp == 0) {
+    sm.m[warp][rl.gh] = st.m_run;
+    sm.l[warp][rl.gh] = st.l_run;
+  }
+  if (rl.tpar == 0) {
+    #pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      *reinterpret_cast<float4*>(&sm.acc[warp][g][4 * rl.dq]) =
+          make_float4(st.acc[g][0].x, st.acc[g][0].y, st.acc[g][1].x, st.acc[g][1].y);
+    }
+  }
+  __syncthreads();
+  const int g = (threadIdx.x >> 5) & (kGroup - 1);
+  const int d0 = 2 * (threadIdx.x & 31);
+  M = -INFINITY;
+  #pragma unroll
+  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[w][g]);
+  L = 0.f;
+  O = make_float2(0.f, 0.f);
+  #pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const float mw = sm.m[w][g];
+    if (mw == -INFINITY) continue;
+    const float f = fast_exp2(mw - M);
+    L += f * sm.l[w][g];
+    O.x += f * sm.acc[w][g][d0];
+    O.y += f * sm.acc[w][g][d0 + 1];
   }
 }
 
@@ -849,7 +890,6 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
   int issued = n_prefetch;
 
   const LaneRoles rl(lane);
-  const int tp = rl.tp, gh = rl.gh, dq = rl.dq, tpar = rl.tpar;
   float2 qa[kGroup][4], qb[kGroup][4];
   load_q<kRope>(prm.q + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim, rl, qa, qb, rcs,
                 rsn);
@@ -868,7 +908,8 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
     const int valid = lp == last_page ? len - lp * kPage : kPage;   // tokens in this page
     const int phys = __shfl_sync(0xffffffffu, my_phys, i);
     const bool ok = phys >= 0 && phys < prm.num_pages;
-    if (!mbar_wait(&ws.bar[stage], phase)) {
+    // one verdict per warp: the page work below shuffles across all lanes
+    if (!__all_sync(0xffffffffu, mbar_wait(&ws.bar[stage], phase))) {
       timed_out = true;
       break;
     }
@@ -901,115 +942,22 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
     st.m_run = -INFINITY;
     st.l_run = 0.f;
   }
-  const float m_run = st.m_run;
-  const float l_run = st.l_run;
-  const float2 (&acc)[kGroup][2] = st.acc;
   if constexpr (kCluster) {
     if (n_splits > 1) {
-      // ---- cluster merge: each warp stores its (m, l, o) for head g straight
-      // into the inbox of the head's leader, block g mod S of the cluster;
-      // every thread arrives on the cluster barrier, blocks that lead no head
-      // exit, and each leader waits for all arrivals and combines its heads.
-      static_assert(kWarps * kMaxClusterSize <= kInboxSlots, "inbox slots");
-      ClusterInbox& inbox = *reinterpret_cast<ClusterInbox*>(smem_raw + sizeof(Smem));
-      const int S = gridDim.x;
-      const int rank = static_cast<int>(cluster_rank());
-      const int slot = rank * kWarps + warp;
-      if (tp == 0) {
-        const int at = (gh / S) * (S * kWarps) + slot;
-        st_cluster(&inbox.m[at], gh % S, m_run);
-        st_cluster(&inbox.l[at], gh % S, l_run);
-      }
-      if (tpar == 0) {
-        #pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
-          const int at = (g / S) * (S * kWarps) + slot;
-          st_cluster4(&inbox.o[at][4 * dq], g % S,
-                      make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y));
-        }
-      }
-      cluster_arrive_release();
-      if (rank >= kGroup) return;   // leads no head
-      cluster_wait_acquire();
-      // combine: warp qq sums the slots p = qq, qq + 4, ... of a head for dims
-      // (d0, d0 + 1); the four warps' sums meet in shared memory
-      const int parts = S * kWarps;
-      const int qq = warp;
-      const int d0 = 2 * lane;
-      for (int hg = rank; hg < kGroup; hg += S) {
-        const int base = (hg / S) * parts;
-        float mx = -INFINITY;
-        for (int p = lane; p < parts; p += 32) mx = fmaxf(mx, inbox.m[base + p]);
-        #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float LL = 0.f;
-        float2 OO = make_float2(0.f, 0.f);
-        #pragma unroll 4
-        for (int p = qq; p < parts; p += kWarps) {
-          const float mp = inbox.m[base + p];
-          const float w = mp == -INFINITY ? 0.f : fast_exp2(mp - mx);
-          const float2 op = *reinterpret_cast<const float2*>(&inbox.o[base + p][d0]);
-          LL += w * inbox.l[base + p];
-          OO.x += w * op.x;
-          OO.y += w * op.y;
-        }
-        sm.acc[qq][0][d0] = OO.x;
-        sm.acc[qq][0][d0 + 1] = OO.y;
-        if (lane == 0) sm.l[qq][0] = LL;
-        __syncthreads();
-        if (qq == 0) {
-          float L4 = 0.f, ox = 0.f, oy = 0.f;
-          #pragma unroll
-          for (int w = 0; w < kWarps; ++w) {
-            L4 += sm.l[w][0];
-            ox += sm.acc[w][0][d0];
-            oy += sm.acc[w][0][d0 + 1];
-          }
-          const float inv = L4 > 0.f ? 1.f / L4 : 0.f;
-          *reinterpret_cast<float2*>(
-              prm.out + (static_cast<size_t>(b) * kHq + kvh * kGroup + hg) * kDim + d0) =
-              make_float2(ox * inv, oy * inv);
-        }
-        __syncthreads();
-      }
+      cluster_merge(sm, *reinterpret_cast<ClusterInbox*>(smem_raw + sizeof(Smem)), st, rl, warp,
+                    lane, prm.out + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim, false);
       return;
     }
   }
 
   // ---- block merge (every ticket-mode block; a cluster whose sequence has
   // a single split)
-  if (tp == 0) {
-    sm.m[warp][gh] = m_run;
-    sm.l[warp][gh] = l_run;
-  }
-  if (tpar == 0) {
-    #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-      *reinterpret_cast<float4*>(&sm.acc[warp][g][4 * dq]) =
-          make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
-    }
-  }
-  __syncthreads();
-
-  // ---- merge the warps: threads 0..127 own (head g, dims d0, d0 + 1); the
-  // rest of an 8-warp block computes an alias and writes nothing
+  float M, L;
+  float2 O;
+  block_merge(sm, st, rl, warp, M, L, O);
   const bool merger = threadIdx.x < kMergeThreads;
   const int g = (threadIdx.x >> 5) & (kGroup - 1);
   const int d0 = 2 * (threadIdx.x & 31);
-  float M = -INFINITY;
-  #pragma unroll
-  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[w][g]);
-  float L = 0.f;
-  float2 O = make_float2(0.f, 0.f);
-  #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const float mw = sm.m[w][g];
-    if (mw == -INFINITY) continue;
-    const float f = fast_exp2(mw - M);
-    L += f * sm.l[w][g];
-    O.x += f * sm.acc[w][g][d0];
-    O.y += f * sm.acc[w][g][d0 + 1];
-  }
   const int head = kvh * kGroup + g;
   const size_t out_row = (static_cast<size_t>(b) * kHq + head) * kDim;
   if (n_splits == 1) {
@@ -1107,6 +1055,269 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
   }  // ticket merge
 }
 
+// ---------------------------------------------------------------- layer stack
+// Consecutive layers of the fused step in one launch: the grid of the
+// cluster kernel (S blocks of 4 warps per (sequence, kv head), merged through
+// distributed shared memory), made persistent. Each block loops over the
+// layers, and each warp's ring of page stages runs on across the layer
+// boundary: the pages of cached tokens of layer l + 1, which nothing of layer
+// l writes, are in flight while layer l's merge and the wait below run.
+// Layer order per sequence: a block reads layer l's q and new k/v, and writes
+// its appended slot, only after every block of its sequence has finished
+// layer l - 1 (a per-sequence completion counter in global memory, bounded
+// wait), the order a model imposes through the rest of the layer. The blocks
+// of a sequence wait for one another, so the host launches this grid only
+// when all of its clusters are resident at once.
+constexpr int kLayerTab = 512;   // block-table entries a block keeps: layers x its pages
+
+struct LayersParams {
+  const uint16_t* q;          // [num_layers][batch][32][64]
+  const uint16_t* k_new;      // [num_layers][batch][8][64]
+  const uint16_t* v_new;
+  uint16_t* k_pool;           // [num_pages][8][16][64]
+  uint16_t* v_pool;
+  const int32_t* tables;      // block tables from the launch's first layer: [.][max_batch][table_stride]
+  const int32_t* seq_lens;    // [batch], the same for every layer
+  float* out;                 // [num_layers][batch][32][64]
+  int* seq_done;              // [batch]: layer completions of the sequence's blocks (zero at launch)
+  int* err;
+  int num_pages;
+  int table_stride;
+  size_t table_layer_stride;  // max_batch * table_stride
+  int max_seq_len;
+  int batch;
+  int num_layers;             // layers of this launch
+};
+
+struct alignas(16) LayersSmem {
+  BlockSmem<kClusterWarps, kClusterStages> blk;
+  ClusterInbox inbox;
+  int ptab[kLayerTab];        // physical page of (layer j, page o of the block's range): j * span + o
+  int flag;                   // thread 0's wait verdict for the block
+};
+
+// Bounded wait until *ctr >= target (acquire, GPU scope): false after about
+// two seconds.
+__device__ __forceinline__ bool wait_count(const int* ctr, int target) {
+  auto load = [&]() {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    return v;
+  };
+  if (load() >= target) return true;
+  const long long start = clock64();
+  while (load() < target) {
+    if (clock64() - start > kWaitCycles) return false;
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kClusterWarps * 32, 3) decode_layers_kernel(const LayersParams prm) {
+  constexpr int kWarps = kClusterWarps;
+  constexpr int kStages = kClusterStages;
+  constexpr int kThreads = kWarps * 32;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  LayersSmem& ls = *reinterpret_cast<LayersSmem*>(smem_raw);
+  BlockSmem<kWarps, kStages>& sm = ls.blk;
+
+  const int S = static_cast<int>(gridDim.x);
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int J = prm.num_layers;
+
+  // the plan depends on the length only, so every block of a sequence takes
+  // the same exits: no block waits for one that left
+  const int len = prm.seq_lens[b];
+  if (len < 1 || len > prm.max_seq_len) {
+    if (split == 0 && kvh == 0 && threadIdx.x == 0) set_error(prm.err, kErrSeqLen);
+    return;
+  }
+  const int n_pages = (len + kPage - 1) / kPage;
+  const int chunk = (n_pages + S - 1) / S;
+  const int n_splits = (n_pages + chunk - 1) / chunk;
+  if (n_splits == 1 && split > 0) return;            // one block serves the sequence
+  if (chunk * J > kLayerTab) {                        // the host sizes launches below this
+    if (split == 0 && kvh == 0 && threadIdx.x == 0) set_error(prm.err, kErrSeqLen);
+    return;
+  }
+  const int arrivals = kHkv * (n_splits == 1 ? 1 : S);   // blocks of the sequence
+  const bool active = split < n_splits;              // an idle cluster block only joins merges
+  const int page_begin = active ? split * chunk : 0;
+  const int span = active ? min(n_pages, page_begin + chunk) - page_begin : 0;
+  const int last_page = n_pages - 1;
+  const int new_slot = (len - 1) % kPage;
+
+  for (int e = threadIdx.x; e < span * J; e += kThreads) {
+    const int j = e / span;
+    ls.ptab[e] = prm.tables[static_cast<size_t>(j) * prm.table_layer_stride +
+                            static_cast<size_t>(b) * prm.table_stride + page_begin + (e - j * span)];
+  }
+  WarpSmem<kStages>& ws = sm.warp[warp];
+  // this warp's pages of the range: warp, warp + 4, ...; its items run over
+  // the layers: item k is page i = k % mine of layer j = k / mine
+  const int mine = warp < span ? (span - warp + kWarps - 1) / kWarps : 0;
+  const int total = mine * J;
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&ws.bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // the warp's page index (within a layer) that holds the appended slot
+  const int new_off = last_page - page_begin - warp;
+  const int i_new = active && new_off >= 0 && new_off % kWarps == 0 && new_off / kWarps < mine
+                        ? new_off / kWarps
+                        : -1;
+  auto phys_of = [&](int k) {
+    const int j = k / mine;
+    return ls.ptab[j * span + warp + kWarps * (k - j * mine)];
+  };
+  // Copy engine: item k into `stage` (lane 0 issues); the last page's copy
+  // stops before the appended row, which comes from k/v after the wait
+  auto issue_copy = [&](int k, int stage) {
+    if (lane != 0) return;
+    const int lp = page_begin + warp + kWarps * (k % mine);
+    const int phys = phys_of(k);
+    const bool ok = phys >= 0 && phys < prm.num_pages;
+    const int rows = lp == last_page ? new_slot : kPage;
+    if (!ok) set_error(prm.err, kErrPage);
+    if (ok && rows > 0) {
+      const uint32_t bytes = static_cast<uint32_t>(rows) * kRowBytes;
+      const size_t tile = (static_cast<size_t>(phys) * kHkv + kvh) * (kPage * kDim);
+      mbar_arrive_expect_tx(&ws.bar[stage], 2 * bytes);
+      bulk_load(ws.k[stage], prm.k_pool + tile, bytes, &ws.bar[stage]);
+      bulk_load(ws.v[stage], prm.v_pool + tile, bytes, &ws.bar[stage]);
+    } else {
+      mbar_arrive(&ws.bar[stage]);
+    }
+  };
+  // the appended row of layer j: lanes 0..7 K, 8..15 V, one 16-byte chunk each
+  auto load_new_row = [&](int j) {
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (lane < 16) {
+      const uint16_t* src = (lane >= 8 ? prm.v_new : prm.k_new) +
+                            ((static_cast<size_t>(j) * prm.batch + b) * kHkv + kvh) * kDim +
+                            (lane & 7) * 8;
+      val = __ldg(reinterpret_cast<const uint4*>(src));
+    }
+    return val;
+  };
+  // ... written to the pool and to the stage tile of its page
+  auto place_new_row = [&](int stage, int phys, uint4 val) {
+    if (lane >= 16 || phys < 0 || phys >= prm.num_pages) return;
+    const bool is_v = lane >= 8;
+    const int c = lane & 7;
+    uint16_t* pool = is_v ? prm.v_pool : prm.k_pool;
+    *reinterpret_cast<uint4*>(pool + ((static_cast<size_t>(phys) * kHkv + kvh) * kPage +
+                                      new_slot) * kDim + c * 8) = val;
+    uint8_t* tile = is_v ? ws.v[stage] : ws.k[stage];
+    *reinterpret_cast<uint4*>(tile + new_slot * kRowBytes + c * 16) = val;
+  };
+
+  int issued = min(total, kStages);
+  for (int k = 0; k < issued; ++k) issue_copy(k, k);
+
+  const LaneRoles rl(lane);
+  const float no_angles[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int k = 0;                 // next item to consume
+  int stage = 0;             // k % kStages
+  uint32_t phase = 0;        // (k / kStages) & 1
+  int consumed = 0;
+  bool broken = false;       // a page wait gave up: this warp copies and computes no more
+  bool waits_off = false;    // a sequence wait gave up: the block stops waiting (flagged)
+  for (int j = 0; j < J; ++j) {
+    if (j > 0 && !waits_off) {
+      if (threadIdx.x == 0) ls.flag = wait_count(prm.seq_done + b, j * arrivals) ? 0 : 1;
+      __syncthreads();
+      if (ls.flag) {
+        waits_off = true;
+        if (threadIdx.x == 0) set_error(prm.err, kErrTimeout);
+      }
+    }
+    // q and the new k/v rows of the next layer into L2 while this one runs
+    if (warp == 0 && lane < 6 && active && j + 1 < J) {
+      const size_t row = static_cast<size_t>(j + 1) * prm.batch + b;
+      const uint16_t* line = lane < 4 ? prm.q + (row * kHq + kvh * kGroup + lane) * kDim
+                                      : (lane == 4 ? prm.k_new : prm.v_new) +
+                                            (row * kHkv + kvh) * kDim;
+      prefetch_l2(line);
+    }
+    const int item_new = i_new >= 0 ? j * mine + i_new : -1;   // this layer's appended-row item
+    const bool place_now = item_new >= 0 && item_new < issued && !broken;
+    uint4 new_val = make_uint4(0u, 0u, 0u, 0u);
+    if (place_now) new_val = load_new_row(j);
+    float2 qa[kGroup][4], qb[kGroup][4];
+    load_q<false>(prm.q + ((static_cast<size_t>(j) * prm.batch + b) * kHq + kvh * kGroup) * kDim,
+                  rl, qa, qb, no_angles, no_angles);
+    if (place_now) place_new_row(item_new % kStages, phys_of(item_new), new_val);
+    __syncwarp();
+
+    WarpState st;
+    st.reset();
+    bool lost = false;       // this layer's pages are incomplete
+    for (int i = 0; i < mine; ++i, ++k) {
+      if (!broken) {
+        // one verdict per warp: the page work below shuffles across all lanes
+        if (!__all_sync(0xffffffffu, mbar_wait(&ws.bar[stage], phase))) {
+          broken = true;
+          if (lane == 0) set_error(prm.err, kErrTimeout);
+        } else {
+          consumed = k + 1;
+          const int lp = page_begin + warp + kWarps * i;
+          const int valid = lp == last_page ? len - lp * kPage : kPage;
+          const int phys = phys_of(k);
+          const bool ok = phys >= 0 && phys < prm.num_pages;
+          attend_page(ws.k[stage], ws.v[stage], ok ? valid : 0, qa, qb, ws.p, ws.alpha, rl, st);
+          const int kn = k + kStages;
+          if (kn < total) {
+            issue_copy(kn, stage);
+            // a later item of this layer holding the appended slot: its row now
+            if (kn == item_new) place_new_row(stage, phys_of(kn), load_new_row(j));
+            __syncwarp();
+            issued = kn + 1;
+          }
+        }
+      }
+      lost |= broken;
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    reduce_warp_state(st);
+    if (lost) {
+      st.m_run = -INFINITY;
+      st.l_run = 0.f;
+    }
+    float* out_kv = prm.out + ((static_cast<size_t>(j) * prm.batch + b) * kHq + kvh * kGroup) * kDim;
+    if (n_splits > 1) {
+      cluster_merge(sm, ls.inbox, st, rl, warp, lane, out_kv, true);
+    } else {
+      float M, L;
+      float2 O;
+      block_merge(sm, st, rl, warp, M, L, O);
+      const int g = (threadIdx.x >> 5) & (kGroup - 1);
+      const int d0 = 2 * (threadIdx.x & 31);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      *reinterpret_cast<float2*>(out_kv + g * kDim + d0) = make_float2(O.x * inv, O.y * inv);
+    }
+    // this block is done with layer j: its output rows are written
+    __syncthreads();
+    if (j + 1 < J && threadIdx.x == 0) {
+      __threadfence();
+      atomicAdd(prm.seq_done + b, 1);
+    }
+  }
+  if (broken) {
+    // let this warp's copies still in flight land before the block exits
+    // (each wait bounded again)
+    for (int kk = consumed; kk < issued; ++kk) mbar_wait(&ws.bar[kk % kStages], (kk / kStages) & 1);
+  }
+}
+
 }  // namespace
 
 // ================================================================= host side
@@ -1178,6 +1389,19 @@ int auto_cluster_splits(const pkv_pool* pool, int batch) {
   for (int s = pool->max_cluster; s >= 2; s /= 2) {
     if (s > pool->cfg.max_splits || s > max_pages) continue;
     if (static_cast<long long>(batch) * kHkv * s <= resident) return s;
+  }
+  return 0;
+}
+
+// Cluster size of the multi-layer launch: the largest S of 16, 8, 4, 2 (within
+// the device's cluster limit, max_splits and the pages of a full sequence)
+// for which all batch x 8 clusters are resident at once; 0 when none is.
+int layers_cluster_splits(const pkv_pool* pool, int batch) {
+  const int max_pages = pool->cfg.max_seq_len / kPage;
+  for (int e = 4; e >= 1; --e) {
+    const int s = 1 << e;
+    if (s > pool->max_cluster || s > pool->cfg.max_splits || s > max_pages) continue;
+    if (static_cast<long long>(batch) * kHkv <= pool->layer_clusters[e]) return s;
   }
   return 0;
 }
@@ -1428,6 +1652,8 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
   ok = ok && cudaMalloc(&pool->tickets, 2 * static_cast<size_t>(c.max_batch) * kHkv * sizeof(int)) ==
                  cudaSuccess;
   ok = ok && cudaMalloc(&pool->err, sizeof(int)) == cudaSuccess;
+  ok = ok && cudaMalloc(&pool->seq_done, static_cast<size_t>(c.max_batch) * sizeof(int)) ==
+                 cudaSuccess;
 
   ok = ok && cudaMemset(pool->tickets, 0, 2 * static_cast<size_t>(c.max_batch) * kHkv * sizeof(int)) ==
                  cudaSuccess;
@@ -1440,6 +1666,10 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
   ok = ok && set_kernel_attributes(ticket_kernel<true, true>, false);
   ok = ok && set_kernel_attributes(cluster_kernel<false, true>, true);
   ok = ok && set_kernel_attributes(cluster_kernel<true, true>, true);
+  ok = ok && cudaFuncSetAttribute(decode_layers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(sizeof(LayersSmem))) == cudaSuccess;
+  ok = ok && cudaFuncSetAttribute(decode_layers_kernel,
+                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
 
   ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                   &pool->blocks_per_sm, ticket_kernel<true>, block_threads(false),
@@ -1466,6 +1696,29 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
       pool->max_cluster = size;
     cudaGetLastError();   // a size the device refuses is not an error here
   }
+  // how many clusters of the multi-layer kernel the device holds at once,
+  // per cluster size: its blocks wait for one another, so it launches only
+  // grids that fit
+  for (int e = 0; e < 5; ++e) {
+    const int size = 1 << e;
+    pool->layer_clusters[e] = 0;
+    if (!ok) continue;
+    cudaLaunchConfig_t probe = {};
+    probe.gridDim = dim3(size, kHkv, 1);
+    probe.blockDim = dim3(kClusterWarps * 32, 1, 1);
+    probe.dynamicSmemBytes = sizeof(LayersSmem);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = size;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    probe.attrs = &attr;
+    probe.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, decode_layers_kernel, &probe) == cudaSuccess)
+      pool->layer_clusters[e] = clusters;
+    cudaGetLastError();   // a size the device refuses is not an error here
+  }
   if (ok && pool->blocks_per_sm < 1) pool->blocks_per_sm = 1;
   if (ok && pool->cluster_blocks_per_sm < 1) pool->cluster_blocks_per_sm = 1;
 
@@ -1485,6 +1738,7 @@ pkv_status pkv_pool_destroy(pkv_pool_t pool) {
   cudaFree(pool->part_ml);
   cudaFree(pool->tickets);
   cudaFree(pool->err);
+  cudaFree(pool->seq_done);
   delete pool;
   return st;
 }
@@ -1553,6 +1807,88 @@ pkv_status pkv_append_attend(pkv_pool_t pool, int layer, const void* q, const vo
                              int batch, int num_splits, void* stream) {
   return launch_decode<true>(pool, layer, q, k, v, k_pool, v_pool, block_tables, seq_lens, out,
                              batch, num_splits, stream);
+}
+
+pkv_status pkv_append_attend_layers(pkv_pool_t pool, int layer_begin, int num_layers,
+                                    const void* q, const void* k, const void* v, void* k_pool,
+                                    void* v_pool, const int32_t* block_tables,
+                                    const int32_t* seq_lens, float* out, int batch,
+                                    void* stream) {
+  if (!pool) return PKV_ERR_INVALID_ARG;
+  const pkv_pool_config& c = pool->cfg;
+  if (layer_begin < 0 || num_layers < 0 ||
+      static_cast<long long>(layer_begin) + num_layers > c.num_layers || batch < 0 ||
+      batch > c.max_batch)
+    return PKV_ERR_INVALID_ARG;
+  if (batch == 0 || num_layers == 0) return PKV_OK;
+  if (!q || !k || !v || !k_pool || !v_pool || !block_tables || !seq_lens || !out)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_pool) ||
+      !aligned16(v_pool) || !aligned16(block_tables) || !aligned16(seq_lens) || !aligned16(out))
+    return PKV_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_ERR_INVALID_ARG;
+
+  const size_t q_layer = static_cast<size_t>(batch) * kHq * kDim;     // elements per layer
+  const size_t kv_layer = static_cast<size_t>(batch) * kHkv * kDim;
+  const uint16_t* q16 = static_cast<const uint16_t*>(q);
+  const uint16_t* k16 = static_cast<const uint16_t*>(k);
+  const uint16_t* v16 = static_cast<const uint16_t*>(v);
+  const int S = layers_cluster_splits(pool, batch);
+  if (S == 0) {
+    // too many sequences for a resident grid: one fused launch per layer
+    for (int j = 0; j < num_layers; ++j) {
+      const pkv_status st = launch_decode<true>(pool, layer_begin + j, q16 + j * q_layer,
+                                                k16 + j * kv_layer, v16 + j * kv_layer, k_pool,
+                                                v_pool, block_tables, seq_lens, out + j * q_layer,
+                                                batch, 0, stream);
+      if (st != PKV_OK) return st;
+    }
+    return PKV_OK;
+  }
+
+  const int max_pages = c.max_seq_len / kPage;
+  const int chunk_max = (max_pages + S - 1) / S;
+  const int per_launch = kLayerTab / chunk_max;   // >= 8: chunk_max <= 64
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int j0 = 0; j0 < num_layers; j0 += per_launch) {
+    const int J = std::min(per_launch, num_layers - j0);
+    if (J > 1 && cudaMemsetAsync(pool->seq_done, 0, static_cast<size_t>(batch) * sizeof(int), s) !=
+                     cudaSuccess)
+      return PKV_ERR_CUDA;
+    LayersParams prm;
+    prm.q = q16 + j0 * q_layer;
+    prm.k_new = k16 + j0 * kv_layer;
+    prm.v_new = v16 + j0 * kv_layer;
+    prm.k_pool = static_cast<uint16_t*>(k_pool);
+    prm.v_pool = static_cast<uint16_t*>(v_pool);
+    prm.table_stride = max_pages;
+    prm.table_layer_stride = static_cast<size_t>(c.max_batch) * max_pages;
+    prm.tables = block_tables + static_cast<size_t>(layer_begin + j0) * prm.table_layer_stride;
+    prm.seq_lens = seq_lens;
+    prm.out = out + j0 * q_layer;
+    prm.seq_done = pool->seq_done;
+    prm.err = pool->err;
+    prm.num_pages = c.num_pages;
+    prm.max_seq_len = c.max_seq_len;
+    prm.batch = batch;
+    prm.num_layers = J;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S, kHkv, batch);
+    cfg.blockDim = dim3(kClusterWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(LayersSmem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = S;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_layers_kernel, prm) != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return check_launch();
 }
 
 pkv_status pkv_decode_attention_rope(pkv_pool_t pool, int layer, const void* q,

@@ -18,6 +18,8 @@ struct pkv_pool {
   float2* part_ml;   // [2][max_batch][32][max_splits]
   int* tickets;      // [2][max_batch][8]
   int* err;          // sticky error bits (PKV_DEV_ERR_*)
+  int* seq_done;     // [max_batch]: layer completions per sequence (multi-layer launch)
+  int layer_clusters[5];   // resident clusters of the multi-layer kernel, S = 1, 2, 4, 8, 16
 };
 
 // Sticky device error bits; pkv_get_error maps TIMEOUT to

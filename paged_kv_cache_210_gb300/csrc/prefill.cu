@@ -62,18 +62,13 @@
 
 #include "pkv.h"
 #include "pkv_prefill.h"
+#include "device_common.cuh"
 #include "pool_internal.h"
+
+using namespace pkv_dev;
 
 namespace {
 
-constexpr int kPage = 16;
-constexpr int kHq = 32;
-constexpr int kHkv = 8;
-constexpr int kGroup = kHq / kHkv;
-constexpr int kDim = 64;
-constexpr int kMaxSeqLen = 2048;
-constexpr int kMaxPages = kMaxSeqLen / kPage;
-constexpr int kRowBytes = kDim * 2;                  // 128 B: one swizzle row
 constexpr int kTileTokens = 32;                      // query tokens per CTA
 constexpr int kRows = kTileTokens * kGroup;          // 128: the MMA's M
 constexpr int kStepKeys = 64;                        // keys per step: the S MMA's N
@@ -90,7 +85,6 @@ constexpr int kSTiles = 3;                           // score (then P) tiles in 
 constexpr uint32_t kTmemCols = 256;                  // S/P tiles: 0..191, O: 192..255
 constexpr uint32_t kTmemO = kSTiles * 64;
 constexpr float kRescaleLog2 = 8.f;                  // lazy max: p <= 2^8
-constexpr long long kWaitCycles = 4000000000LL;      // about two seconds
 
 struct PrefillSmem {                                 // every tile 1024-byte aligned
   uint8_t q[kRows * kRowBytes];                      // 16 KiB
@@ -124,55 +118,7 @@ struct PrefillParams {
 };
 
 // ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void set_error(int* err, int bits) { atomicOr(err, bits); }
-
 __device__ __forceinline__ int lane_of(int tid) { return tid & 31; }
-
-__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
-  constexpr uint32_t kSuspendHintNs = 10000000;
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-  return done != 0;
-}
-
-// Bounded wait on an mbarrier phase: false after about two seconds.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - start > kWaitCycles) return false;
-  }
-  return true;
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
 
 // Generic-proxy writes to shared memory become visible to the tensor cores
 // and the copy engine (async proxy).
@@ -315,18 +261,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 __host__ __device__ constexpr uint32_t instr_desc(int m, int n, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  uint32_t w;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
-  return w;
 }
 
 
@@ -657,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
           const float2 h = make_float2(__uint_as_float(b0 & 0xffff0000u),
                                        __uint_as_float(b1 & 0xffff0000u));
           const float2 rest = __ffma2_rn(h, neg1, pp);
-          lo[i / 2] = pack_bf16x2(rest.x, rest.y);
+          lo[i / 2] = float2_to_bf16x2(rest.x, rest.y);
         }
         const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
         l_half += a.x + a.y;
