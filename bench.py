@@ -50,6 +50,8 @@ WORKLOADS = {
     "ragged-b256": W.large_ragged,
     "long-b1": lambda: W.long_context(1),
     "long-b4": lambda: W.long_context(4),
+    "long-b8": lambda: W.long_context(8),
+    "long-b16": lambda: W.long_context(16),
 }
 DESCRIPTIONS = {
     "llama-b2-2048": "Llama-3.2-1B decode step at the default 128 MiB pool: 16 layers, batch 2 at "
@@ -60,6 +62,8 @@ DESCRIPTIONS = {
                    "K x 4",
     "long-b1": "long context: 16 layers, batch 1 at 2048, 1 GiB pool",
     "long-b4": "long context: 16 layers, batch 4 at 2048, 1 GiB pool",
+    "long-b8": "long context: 16 layers, batch 8 at 2048, 1 GiB pool",
+    "long-b16": "long context: 16 layers, batch 16 at 2048, 1 GiB pool (every page used)",
 }
 
 

@@ -219,8 +219,8 @@ pkv_status pkv_append_attend_rope(pkv_pool_t pool, int layer, const void* q, con
  * largest of 16, 8, 4, 2 for which every cluster of the grid is resident at
  * once; the blocks of a sequence then wait for one another between layers
  * (bounded: a wait that gives up flags PKV_ERR_DEVICE_TIMEOUT and the block
- * carries on without waiting). A launch covers at most 512 / ceil(128 / S)
- * layers (64 at S = 16, 8 at S = 2); longer calls are split into several. A
+ * carries on without waiting). A launch covers at most 256 / ceil(128 / S)
+ * layers (32 at S = 16, 4 at S = 2); longer calls are split into several. A
  * batch for which even S = 2 does not fit runs as one pkv_append_attend launch
  * per layer. Uses a per-sequence counter in the handle (zeroed on the stream
  * before each launch), so one handle serves one such call at a time.

@@ -48,16 +48,20 @@ namespace {
 
 constexpr int kTileBytes = kPage * kRowBytes;   // one (page, kv head) tile: 2 KiB
 
-// Block shapes: 4 warps with 3 page stages per warp. The ticket-merge kernel
-// fits 4 blocks per SM (128 registers); the cluster-merge kernel (plus its
-// inbox) 3, so it may use up to 168 registers, and 3 per SM
-// leaves room for the next launch's blocks to become resident and prefetch
-// while this one finishes (8-warp cluster blocks, 2 per SM, measured slower
-// for 2 sequences because the next layer could not start early).
+// Block shapes, all 4 warps with a ring of page stages per warp:
+//  * ticket merge (large batches): 3 stages, 4 blocks per SM (128 registers);
+//  * narrow cluster (batches up to about 4): 3 stages, 3 blocks per SM, so up
+//    to 168 registers; about 256 blocks a launch leave room for the next
+//    launch's blocks to become resident and prefetch while this one finishes;
+//  * wide cluster (batches of about 5 to 32): 2 stages, 4 blocks per SM
+//    (128 registers), so twice the splits fit one wave.
+// (8-warp cluster blocks, 2 per SM, measured slower for 2 sequences because
+// the next layer could not start early.)
 constexpr int kTicketWarps = 4;
 constexpr int kTicketStages = 3;
 constexpr int kClusterWarps = 4;
-constexpr int kClusterStages = 3;
+constexpr int kNarrowStages = 3;
+constexpr int kWideStages = 2;
 constexpr int kMergeThreads = 128;               // one thread per (head, dim pair)
 constexpr int kDefaultMaxSplits = 64;
 constexpr int kMaxSplitsLimit = 128;
@@ -80,9 +84,9 @@ struct alignas(16) WarpSmem {
 };
 
 // A head leader's inbox (placed after BlockSmem, cluster kernels only): every
-// warp of the cluster stores its (m, l, o) for the heads this block leads.
-// Slot of warp w of block r for head g: (g / S) * (S * warps) + r * warps + w.
-constexpr int kInboxSlots = kMaxClusterSize * 4;   // cluster blocks x warps per block
+// block of the cluster stores its (m, l, o) for the heads this block leads.
+// Slot of block r for head g: (g / S) * S + r (at most 16 slots for S <= 16).
+constexpr int kInboxSlots = kMaxClusterSize;
 struct ClusterInbox {
   float o[kInboxSlots][kDim];
   float m[kInboxSlots];
@@ -106,11 +110,23 @@ struct alignas(16) BlockSmem {
   int last;
 };
 
-static_assert(sizeof(WarpSmem<kTicketStages>) % 16 == 0 && sizeof(WarpSmem<kClusterStages>) % 16 == 0,
+using TicketSmem = BlockSmem<kTicketWarps, kTicketStages>;
+using NarrowSmem = BlockSmem<kClusterWarps, kNarrowStages>;
+using WideSmem = BlockSmem<kClusterWarps, kWideStages>;
+static_assert(sizeof(WarpSmem<kTicketStages>) % 16 == 0 &&
+                  sizeof(WarpSmem<kWideStages>) % 16 == 0,
               "warp slabs keep 16-byte alignment");
-static_assert(sizeof(BlockSmem<kClusterWarps, kClusterStages>) % 16 == 0,
+static_assert(sizeof(NarrowSmem) % 16 == 0 && sizeof(WideSmem) % 16 == 0,
               "the cluster inbox follows BlockSmem 16-byte aligned");
 static_assert(sizeof(ClusterInbox) % 16 == 0, "inbox size keeps 16-byte alignment");
+// residency the kernels are shaped for: 228 KiB of shared memory per SM, 1 KiB
+// of it reserved per block; 4 ticket blocks or 3 cluster blocks per SM
+constexpr size_t kSmemPerSm = 228 * 1024;
+static_assert(4 * (sizeof(TicketSmem) + 1024) <= kSmemPerSm, "4 ticket blocks per SM");
+static_assert(3 * (sizeof(NarrowSmem) + sizeof(ClusterInbox) + 1024) <= kSmemPerSm,
+              "3 narrow cluster blocks per SM");
+static_assert(4 * (sizeof(WideSmem) + sizeof(ClusterInbox) + 1024) <= kSmemPerSm,
+              "4 wide cluster blocks per SM");
 
 struct DecodeParams {
   const uint16_t* q;          // [B][32][64]
@@ -155,11 +171,10 @@ __device__ __forceinline__ void st_cluster(float* p, uint32_t rank, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-__device__ __forceinline__ void st_cluster4(float* p, uint32_t rank, float4 v) {
+__device__ __forceinline__ void st_cluster2(float* p, uint32_t rank, float2 v) {
   uint32_t addr;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(p)), "r"(rank));
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
-               "f"(v.y), "f"(v.z), "f"(v.w)
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
                : "memory");
 }
 
@@ -366,15 +381,14 @@ __device__ __forceinline__ void load_q(const uint16_t* qrow, const LaneRoles& r,
   }
 }
 
-// One page: K tile kt and V tile vt in shared memory, `live` valid tokens
-// (the rest are masked by select, so stale data never leaks). p and alpha
-// are the warp's shared slots for the probabilities and the rescale factors.
-__device__ __forceinline__ void attend_page(const uint8_t* kt, const uint8_t* vt, int live,
+// Scores of one page for this lane: tokens tp and tp + 8 of K tile kt, all 4
+// heads over the lane's 16 dims, then a reduce-scatter over the 4 lanes of a
+// token pair so that the lane keeps head gh's full scores (base 2, scaled).
+// Tokens at or past `live` get -inf.
+__device__ __forceinline__ void page_scores(const uint8_t* kt, int live,
                                             const float2 (&qa)[kGroup][4],
-                                            const float2 (&qb)[kGroup][4],
-                                            float2 (*p)[kGroup], float2* alpha_s,
-                                            const LaneRoles& r, WarpState& st) {
-  // scores for tokens tp and tp + 8, all 4 heads, this lane's 16 dims
+                                            const float2 (&qb)[kGroup][4], const LaneRoles& r,
+                                            float (&sc)[2]) {
   float s[kGroup][2];
   #pragma unroll
   for (int j = 0; j < 2; ++j) {
@@ -395,57 +409,43 @@ __device__ __forceinline__ void attend_page(const uint8_t* kt, const uint8_t* vt
       s[g][j] = d.x + d.y;
     }
   }
-  // reduce-scatter over the 4 lanes of a token pair: the lane keeps head gh
-  float sc[2];
-  {
-    const bool hi1 = r.qd & 1;
-    const bool hi2 = r.qd & 2;
-    #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float send0 = hi1 ? s[0][j] : s[2][j];
-      const float send1 = hi1 ? s[1][j] : s[3][j];
-      float keep0 = hi1 ? s[2][j] : s[0][j];
-      float keep1 = hi1 ? s[3][j] : s[1][j];
-      keep0 += __shfl_xor_sync(0xffffffffu, send0, 1);
-      keep1 += __shfl_xor_sync(0xffffffffu, send1, 1);
-      const float send = hi2 ? keep0 : keep1;
-      float kept = hi2 ? keep1 : keep0;
-      kept += __shfl_xor_sync(0xffffffffu, send, 2);
-      sc[j] = kept;
-    }
+  const bool hi1 = r.qd & 1;
+  const bool hi2 = r.qd & 2;
+  #pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float send0 = hi1 ? s[0][j] : s[2][j];
+    const float send1 = hi1 ? s[1][j] : s[3][j];
+    float keep0 = hi1 ? s[2][j] : s[0][j];
+    float keep1 = hi1 ? s[3][j] : s[1][j];
+    keep0 += __shfl_xor_sync(0xffffffffu, send0, 1);
+    keep1 += __shfl_xor_sync(0xffffffffu, send1, 1);
+    const float send = hi2 ? keep0 : keep1;
+    float kept = hi2 ? keep1 : keep0;
+    kept += __shfl_xor_sync(0xffffffffu, send, 2);
+    sc[j] = kept;
   }
   sc[0] = r.tp < live ? sc[0] : -INFINITY;
   sc[1] = r.tp + 8 < live ? sc[1] : -INFINITY;
+}
 
-  // online softmax, base 2, per head over the page's 16 tokens
-  float pm = fmaxf(sc[0], sc[1]);
-  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-  const float m_new = fmaxf(st.m_run, pm);
-  const float m_use = m_new == -INFINITY ? 0.f : m_new;
-  const float alpha = fast_exp2(st.m_run - m_use);
-  const float p0 = fast_exp2(sc[0] - m_use);
-  const float p1 = fast_exp2(sc[1] - m_use);
-  st.l_run = st.l_run * alpha + p0 + p1;
-  st.m_run = m_new;
-  p[r.tp][r.gh] = make_float2(p0, p0);
-  p[r.tp + 8][r.gh] = make_float2(p1, p1);
-  if (r.tp == 0) alpha_s[r.gh] = make_float2(alpha, alpha);
-  __syncwarp();
-
-  // PV: rescale, then accumulate this lane's tokens
-  {
-    const float4 a01 = *reinterpret_cast<const float4*>(&alpha_s[0]);
-    const float4 a23 = *reinterpret_cast<const float4*>(&alpha_s[2]);
-    const float2 al[kGroup] = {make_float2(a01.x, a01.y), make_float2(a01.z, a01.w),
-                               make_float2(a23.x, a23.y), make_float2(a23.z, a23.w)};
-    #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-      st.acc[g][0] = fmul2(st.acc[g][0], al[g]);
-      st.acc[g][1] = fmul2(st.acc[g][1], al[g]);
-    }
+// Rescale of the accumulators by the per-head factors in alpha_s.
+__device__ __forceinline__ void rescale_acc(const float2* alpha_s, WarpState& st) {
+  const float4 a01 = *reinterpret_cast<const float4*>(&alpha_s[0]);
+  const float4 a23 = *reinterpret_cast<const float4*>(&alpha_s[2]);
+  const float2 al[kGroup] = {make_float2(a01.x, a01.y), make_float2(a01.z, a01.w),
+                             make_float2(a23.x, a23.y), make_float2(a23.z, a23.w)};
+  #pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+    st.acc[g][0] = fmul2(st.acc[g][0], al[g]);
+    st.acc[g][1] = fmul2(st.acc[g][1], al[g]);
   }
+}
+
+// P V of one page: this lane's 4 dims over its tokens 2 i + tpar of V tile vt
+// (the first `live`), with the probabilities of the 4 heads from p ([16][4],
+// each duplicated as a pair).
+__device__ __forceinline__ void page_pv(const uint8_t* vt, int live, const float2 (*p)[kGroup],
+                                        const LaneRoles& r, WarpState& st) {
   auto pv_token = [&](int t) {
     const uint2 vv = *reinterpret_cast<const uint2*>(vt + t * kRowBytes + r.dq * 8);
     const float2 v01 = bf16x2_to_float2(vv.x);
@@ -469,6 +469,39 @@ __device__ __forceinline__ void attend_page(const uint8_t* kt, const uint8_t* vt
       if (2 * t2 + r.tpar < live) pv_token(2 * t2 + r.tpar);
     }
   }
+}
+
+// One page: K tile kt and V tile vt in shared memory, `live` valid tokens
+// (the rest are masked by select, so stale data never leaks). p and alpha
+// are the warp's shared slots for the probabilities and the rescale factors.
+__device__ __forceinline__ void attend_page(const uint8_t* kt, const uint8_t* vt, int live,
+                                            const float2 (&qa)[kGroup][4],
+                                            const float2 (&qb)[kGroup][4],
+                                            float2 (*p)[kGroup], float2* alpha_s,
+                                            const LaneRoles& r, WarpState& st) {
+  float sc[2];
+  page_scores(kt, live, qa, qb, r, sc);
+
+  // online softmax, base 2, per head over the page's 16 tokens
+  float pm = fmaxf(sc[0], sc[1]);
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+  const float m_new = fmaxf(st.m_run, pm);
+  const float m_use = m_new == -INFINITY ? 0.f : m_new;
+  const float alpha = fast_exp2(st.m_run - m_use);
+  const float p0 = fast_exp2(sc[0] - m_use);
+  const float p1 = fast_exp2(sc[1] - m_use);
+  st.l_run = st.l_run * alpha + p0 + p1;
+  st.m_run = m_new;
+  p[r.tp][r.gh] = make_float2(p0, p0);
+  p[r.tp + 8][r.gh] = make_float2(p1, p1);
+  if (r.tp == 0) alpha_s[r.gh] = make_float2(alpha, alpha);
+  __syncwarp();
+
+  // PV: rescale, then accumulate this lane's tokens
+  rescale_acc(alpha_s, st);
+  page_pv(vt, live, p, r, st);
   __syncwarp();
 }
 
@@ -489,81 +522,6 @@ __device__ __forceinline__ void reduce_warp_state(WarpState& st) {
 }
 
 // ---------------------------------------------------------------- merges
-// Cluster merge of the S blocks of one (sequence, kv head) (S = the cluster
-// size): each warp stores its (m, l, o) for head g straight into the inbox of
-// the head's leader, block g mod S of the cluster; every thread arrives on the
-// cluster barrier, and each leader waits for all arrivals and combines its
-// heads into out_kv ([4][64], the kv head's query heads). A block that leads
-// no head returns after its arrival, or, with `wait_always` (blocks that go
-// on to use the cluster barrier again), after the wait as well.
-template <int kWarps, int kStages>
-__device__ __forceinline__ void cluster_merge(BlockSmem<kWarps, kStages>& sm, ClusterInbox& inbox,
-                                              const WarpState& st, const LaneRoles& rl, int warp,
-                                              int lane, float* out_kv, bool wait_always) {
-  static_assert(kWarps * kMaxClusterSize <= kInboxSlots, "inbox slots");
-  const int S = gridDim.x;
-  const int rank = static_cast<int>(cluster_rank());
-  const int slot = rank * kWarps + warp;
-  if (rl.tp == 0) {
-    const int at = (rl.gh / S) * (S * kWarps) + slot;
-    st_cluster(&inbox.m[at], rl.gh % S, st.m_run);
-    st_cluster(&inbox.l[at], rl.gh % S, st.l_run);
-  }
-  if (rl.tpar == 0) {
-    #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-      const int at = (g / S) * (S * kWarps) + slot;
-      st_cluster4(&inbox.o[at][4 * rl.dq], g % S,
-                  make_float4(st.acc[g][0].x, st.acc[g][0].y, st.acc[g][1].x, st.acc[g][1].y));
-    }
-  }
-  cluster_arrive_release();
-  if (rank >= kGroup) {   // leads no head
-    if (wait_always) cluster_wait_acquire();
-    return;
-  }
-  cluster_wait_acquire();
-  // combine: warp qq sums the slots p = qq, qq + 4, ... of a head for dims
-  // (d0, d0 + 1); the four warps' sums meet in shared memory
-  const int parts = S * kWarps;
-  const int qq = warp;
-  const int d0 = 2 * lane;
-  for (int hg = rank; hg < kGroup; hg += S) {
-    const int base = (hg / S) * parts;
-    float mx = -INFINITY;
-    for (int p = lane; p < parts; p += 32) mx = fmaxf(mx, inbox.m[base + p]);
-    #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float LL = 0.f;
-    float2 OO = make_float2(0.f, 0.f);
-    #pragma unroll 4
-    for (int p = qq; p < parts; p += kWarps) {
-      const float mp = inbox.m[base + p];
-      const float w = mp == -INFINITY ? 0.f : fast_exp2(mp - mx);
-      const float2 op = *reinterpret_cast<const float2*>(&inbox.o[base + p][d0]);
-      LL += w * inbox.l[base + p];
-      OO.x += w * op.x;
-      OO.y += w * op.y;
-    }
-    sm.acc[qq][0][d0] = OO.x;
-    sm.acc[qq][0][d0 + 1] = OO.y;
-    if (lane == 0) sm.l[qq][0] = LL;
-    __syncthreads();
-    if (qq == 0) {
-      float L4 = 0.f, ox = 0.f, oy = 0.f;
-      #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        L4 += sm.l[w][0];
-        ox += sm.acc[w][0][d0];
-        oy += sm.acc[w][0][d0 + 1];
-      }
-      const float inv = L4 > 0.f ? 1.f / L4 : 0.f;
-      *reinterpret_cast<float2*>(out_kv + hg * kDim + d0) = make_float2(ox * inv, oy * inv);
-    }
-    __syncthreads();
-  }
-}
-
 // The block's warps merged in shared memory: thread t < 128 gets the
 // log-sum-exp state of head g = (t / 32) % 4 for dims d0 = 2 (t % 32), d0 + 1
 // (M: max, L: sum, O: unnormalised output); the rest of an 8-warp block
@@ -599,6 +557,65 @@ __device__ __forceinline__ void block_merge(BlockSmem<kWarps, kStages>& sm, cons
     L += f * sm.l[w][g];
     O.x += f * sm.acc[w][g][d0];
     O.y += f * sm.acc[w][g][d0 + 1];
+  }
+}
+
+// Cluster merge of the S blocks of one (sequence, kv head) (S = the cluster
+// size): each block first merges its warps (block_merge), then sends one
+// (m, l, o) part per head straight into the inbox of the head's leader,
+// block g mod S of the cluster; every thread arrives on the cluster barrier,
+// and in each leader warp w combines the S parts of head rank + w S into
+// out_kv ([4][64], the kv head's query heads). A block that leads no head
+// returns after its arrival, or, with `wait_always` (blocks that go on to use
+// the cluster barrier again), after the wait as well.
+template <int kWarps, int kStages>
+__device__ __forceinline__ void cluster_merge(BlockSmem<kWarps, kStages>& sm,
+                                              ClusterInbox& inbox, const WarpState& st,
+                                              const LaneRoles& rl, int warp, int lane,
+                                              float* out_kv, bool wait_always) {
+  static_assert(kWarps == kGroup, "one merging thread per (head, dim pair)");
+  float M, L;
+  float2 O;
+  block_merge(sm, st, rl, warp, M, L, O);
+  const int S = gridDim.x;
+  const int rank = static_cast<int>(cluster_rank());
+  const int g = warp;               // thread t: head t / 32, dims 2 (t % 32), + 1
+  const int d0 = 2 * lane;
+  const int at = (g / S) * S + rank;
+  st_cluster2(&inbox.o[at][d0], g % S, O);
+  if (lane == 0) {
+    st_cluster(&inbox.m[at], g % S, M);
+    st_cluster(&inbox.l[at], g % S, L);
+  }
+  cluster_arrive_release();
+  if (rank >= kGroup) {   // leads no head
+    if (wait_always) cluster_wait_acquire();
+    return;
+  }
+  cluster_wait_acquire();
+  const int hg = rank + warp * S;   // head of this leader warp
+  if (hg < kGroup) {
+    const int base = warp * S;      // its parts: slots base .. base + S - 1, part p from rank p
+    const float mp = lane < S ? inbox.m[base + lane] : -INFINITY;
+    float mx = mp;
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float w = mp == -INFINITY ? 0.f : fast_exp2(mp - mx);
+    float lw = lane < S ? w * inbox.l[base + lane] : 0.f;
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+    float2 acc = make_float2(0.f, 0.f);
+    #pragma unroll
+    for (int p = 0; p < kMaxClusterSize; ++p) {
+      if (p < S) {
+        const float wp = __shfl_sync(0xffffffffu, w, p);
+        const float2 op = *reinterpret_cast<const float2*>(&inbox.o[base + p][d0]);
+        acc.x += wp * op.x;
+        acc.y += wp * op.y;
+      }
+    }
+    const float inv = lw > 0.f ? 1.f / lw : 0.f;
+    *reinterpret_cast<float2*>(out_kv + hg * kDim + d0) = make_float2(acc.x * inv, acc.y * inv);
   }
 }
 
@@ -706,7 +723,8 @@ __device__ int longest_first_sequence(int z, int batch, const int32_t* seq_lens,
 // cluster (gridDim.x == cluster size) and merge through distributed shared
 // memory; otherwise splits merge through global partials and a ticket.
 template <bool kFused, bool kCluster, int kWarps, int kStages, bool kRope>
-__global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decode_kernel(const DecodeParams prm) {
+__global__ void __launch_bounds__(kWarps * 32, kCluster && kStages == kNarrowStages ? 3 : 16 / kWarps)
+decode_kernel(const DecodeParams prm) {
   constexpr int kThreads = kWarps * 32;
   using Smem = BlockSmem<kWarps, kStages>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -901,20 +919,14 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
 
   bool timed_out = false;
   int consumed = 0;
-  int stage = 0;            // i % kStages
-  uint32_t phase = 0;       // (i / kStages) & 1
-  for (int i = 0; i < mine; ++i) {
+  // tokens of the warp's i-th page that count (0 for a page id out of range)
+  auto live_of = [&](int i, int phys) {
     const int lp = page_begin + warp + kWarps * i;
-    const int valid = lp == last_page ? len - lp * kPage : kPage;   // tokens in this page
-    const int phys = __shfl_sync(0xffffffffu, my_phys, i);
-    const bool ok = phys >= 0 && phys < prm.num_pages;
-    // one verdict per warp: the page work below shuffles across all lanes
-    if (!__all_sync(0xffffffffu, mbar_wait(&ws.bar[stage], phase))) {
-      timed_out = true;
-      break;
-    }
-    consumed = i + 1;
-    attend_page(ws.k[stage], ws.v[stage], ok ? valid : 0, qa, qb, ws.p, ws.alpha, rl, st);
+    const int valid = lp == last_page ? len - lp * kPage : kPage;
+    return phys >= 0 && phys < prm.num_pages ? valid : 0;
+  };
+  // after page i is consumed: the copy of page i + kStages into its stage
+  auto refill = [&](int i, int stage) {
     if (i + kStages < mine) {
       const int next_phys = __shfl_sync(0xffffffffu, my_phys, i + kStages);
       issue_copy(i + kStages, stage, next_phys);
@@ -922,6 +934,19 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
       __syncwarp();
       issued = i + kStages + 1;
     }
+  };
+  int stage = 0;            // i % kStages
+  uint32_t phase = 0;       // (i / kStages) & 1
+  for (int i = 0; i < mine; ++i) {
+    const int phys = __shfl_sync(0xffffffffu, my_phys, i);
+    // one verdict per warp: the page work below shuffles across all lanes
+    if (!__all_sync(0xffffffffu, mbar_wait(&ws.bar[stage], phase))) {
+      timed_out = true;
+      break;
+    }
+    consumed = i + 1;
+    attend_page(ws.k[stage], ws.v[stage], live_of(i, phys), qa, qb, ws.p, ws.alpha, rl, st);
+    refill(i, stage);
     if (++stage == kStages) {
       stage = 0;
       phase ^= 1u;
@@ -1068,7 +1093,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCluster ? 3 : 16 / kWarps) decod
 // wait), the order a model imposes through the rest of the layer. The blocks
 // of a sequence wait for one another, so the host launches this grid only
 // when all of its clusters are resident at once.
-constexpr int kLayerTab = 512;   // block-table entries a block keeps: layers x its pages
+constexpr int kLayerTab = 256;   // block-table entries a block keeps: layers x its pages
 
 struct LayersParams {
   const uint16_t* q;          // [num_layers][batch][32][64]
@@ -1090,7 +1115,7 @@ struct LayersParams {
 };
 
 struct alignas(16) LayersSmem {
-  BlockSmem<kClusterWarps, kClusterStages> blk;
+  WideSmem blk;
   ClusterInbox inbox;
   int ptab[kLayerTab];        // physical page of (layer j, page o of the block's range): j * span + o
   int flag;                   // thread 0's wait verdict for the block
@@ -1098,6 +1123,8 @@ struct alignas(16) LayersSmem {
 
 // Bounded wait until *ctr >= target (acquire, GPU scope): false after about
 // two seconds.
+static_assert(4 * (sizeof(LayersSmem) + 1024) <= kSmemPerSm, "4 multi-layer blocks per SM");
+
 __device__ __forceinline__ bool wait_count(const int* ctr, int target) {
   auto load = [&]() {
     int v;
@@ -1112,13 +1139,13 @@ __device__ __forceinline__ bool wait_count(const int* ctr, int target) {
   return true;
 }
 
-__global__ void __launch_bounds__(kClusterWarps * 32, 3) decode_layers_kernel(const LayersParams prm) {
+__global__ void __launch_bounds__(kClusterWarps * 32, 4) decode_layers_kernel(const LayersParams prm) {
   constexpr int kWarps = kClusterWarps;
-  constexpr int kStages = kClusterStages;
+  constexpr int kStages = kWideStages;
   constexpr int kThreads = kWarps * 32;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   LayersSmem& ls = *reinterpret_cast<LayersSmem*>(smem_raw);
-  BlockSmem<kWarps, kStages>& sm = ls.blk;
+  WideSmem& sm = ls.blk;
 
   const int S = static_cast<int>(gridDim.x);
   const int split = blockIdx.x;
@@ -1223,8 +1250,6 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 3) decode_layers_kernel(co
   const LaneRoles rl(lane);
   const float no_angles[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   int k = 0;                 // next item to consume
-  int stage = 0;             // k % kStages
-  uint32_t phase = 0;        // (k / kStages) & 1
   int consumed = 0;
   bool broken = false;       // a page wait gave up: this warp copies and computes no more
   bool waits_off = false;    // a sequence wait gave up: the block stops waiting (flagged)
@@ -1258,35 +1283,38 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 3) decode_layers_kernel(co
     WarpState st;
     st.reset();
     bool lost = false;       // this layer's pages are incomplete
-    for (int i = 0; i < mine; ++i, ++k) {
-      if (!broken) {
-        // one verdict per warp: the page work below shuffles across all lanes
-        if (!__all_sync(0xffffffffu, mbar_wait(&ws.bar[stage], phase))) {
-          broken = true;
-          if (lane == 0) set_error(prm.err, kErrTimeout);
-        } else {
-          consumed = k + 1;
-          const int lp = page_begin + warp + kWarps * i;
-          const int valid = lp == last_page ? len - lp * kPage : kPage;
-          const int phys = phys_of(k);
-          const bool ok = phys >= 0 && phys < prm.num_pages;
-          attend_page(ws.k[stage], ws.v[stage], ok ? valid : 0, qa, qb, ws.p, ws.alpha, rl, st);
-          const int kn = k + kStages;
-          if (kn < total) {
-            issue_copy(kn, stage);
-            // a later item of this layer holding the appended slot: its row now
-            if (kn == item_new) place_new_row(stage, phys_of(kn), load_new_row(j));
-            __syncwarp();
-            issued = kn + 1;
-          }
-        }
+    // tokens of item k (page i of this layer) that count
+    auto live_of = [&](int k, int i) {
+      const int lp = page_begin + warp + kWarps * i;
+      const int valid = lp == last_page ? len - lp * kPage : kPage;
+      const int phys = phys_of(k);
+      return phys >= 0 && phys < prm.num_pages ? valid : 0;
+    };
+    // after item k is consumed: the copy of item k + kStages into its stage
+    auto refill = [&](int k) {
+      const int kn = k + kStages;
+      if (kn < total) {
+        issue_copy(kn, k % kStages);
+        // a later item of this layer holding the appended slot: its row now
+        if (kn == item_new) place_new_row(k % kStages, phys_of(kn), load_new_row(j));
+        __syncwarp();
+        issued = kn + 1;
       }
-      lost |= broken;
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
+    };
+    for (int i = 0; i < mine && !broken; ++i, ++k) {
+      // one verdict per warp: the page work below shuffles across all lanes
+      if (!__all_sync(0xffffffffu, mbar_wait(&ws.bar[k % kStages], (k / kStages) & 1))) {
+        broken = true;
+        if (lane == 0) set_error(prm.err, kErrTimeout);
+        break;
       }
+      consumed = k + 1;
+      attend_page(ws.k[k % kStages], ws.v[k % kStages], live_of(k, i), qa, qb, ws.p, ws.alpha,
+                  rl, st);
+      refill(k);
     }
+    lost |= broken;
+    k = (j + 1) * mine;      // the next layer's first item (also after a break)
     reduce_warp_state(st);
     if (lost) {
       st.m_run = -INFINITY;
@@ -1326,26 +1354,33 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The two kernel shapes: ticket merge and cluster merge (4 warps, 3 stages
-// each; the cluster kernel adds the leader's inbox).
+// The three kernel shapes (the cluster kernels add the leaders' inbox).
+enum Shape { kTicketShape = 0, kNarrowShape = 1, kWideShape = 2 };
 template <bool kFused, bool kRope = false>
 constexpr auto ticket_kernel = decode_kernel<kFused, false, kTicketWarps, kTicketStages, kRope>;
 template <bool kFused, bool kRope = false>
-constexpr auto cluster_kernel = decode_kernel<kFused, true, kClusterWarps, kClusterStages, kRope>;
+constexpr auto narrow_kernel = decode_kernel<kFused, true, kClusterWarps, kNarrowStages, kRope>;
+template <bool kFused, bool kRope = false>
+constexpr auto wide_kernel = decode_kernel<kFused, true, kClusterWarps, kWideStages, kRope>;
 
-size_t smem_bytes(bool cluster) {
-  return cluster ? sizeof(BlockSmem<kClusterWarps, kClusterStages>) + sizeof(ClusterInbox)
-                 : sizeof(BlockSmem<kTicketWarps, kTicketStages>);
+size_t smem_bytes(Shape shape) {
+  switch (shape) {
+    case kNarrowShape: return sizeof(NarrowSmem) + sizeof(ClusterInbox);
+    case kWideShape: return sizeof(WideSmem) + sizeof(ClusterInbox);
+    default: return sizeof(TicketSmem);
+  }
 }
 
-int block_threads(bool cluster) { return 32 * (cluster ? kClusterWarps : kTicketWarps); }
+int block_threads(Shape shape) {
+  return 32 * (shape == kTicketShape ? kTicketWarps : kClusterWarps);
+}
 
 template <typename Kernel>
-bool set_kernel_attributes(Kernel kernel, bool cluster) {
+bool set_kernel_attributes(Kernel kernel, Shape shape) {
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem_bytes(cluster))) != cudaSuccess)
+                           static_cast<int>(smem_bytes(shape))) != cudaSuccess)
     return false;
-  if (cluster &&
+  if (shape != kTicketShape &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
           cudaSuccess)
     return false;
@@ -1380,17 +1415,39 @@ int auto_chunk_pages(const pkv_pool* pool, int batch) {
   return chunk < min_chunk ? min_chunk : chunk;
 }
 
-// Splits per sequence for a cluster merge when the library chooses: the
-// largest cluster (16, 8, 4, 2) for which batch x 8 kv heads x S blocks fit in
-// one wave of resident blocks; 0 when even S = 2 would not (large batches).
-int auto_cluster_splits(const pkv_pool* pool, int batch) {
-  const long long resident = static_cast<long long>(pool->cluster_blocks_per_sm) * pool->num_sms;
+// Cluster plan when the library chooses: the split count S (16, 8, 4, 2) and
+// the block shape. Measured on a 152-SM GB300 with full-length sequences
+// (GB/s per 16-layer step, the plans per batch):
+//   batch 2:  narrow S = 16 (256 blocks) 1522; wide S = 16 1453; S = 8 1337;
+//   batch 4:  narrow S = 8 (256) 2304; narrow S = 16 1404; wide S = 8 2015;
+//   batch 8:  wide S = 8 (512) 3462; narrow S = 4 (256) 2680; wide S = 16 2016;
+//   batch 16: wide S = 4 (512) 4214; narrow S = 2 (256) 3187; wide S = 8 3443.
+// So: the narrow shape with the largest S whose blocks take at most 9/16 of
+// its resident slots (256 of 456, leaving room for the next launch), if that
+// S is at least 8; else the wide shape with the largest S <= 8 whose blocks
+// take at most 27/32 of its slots (512 of 608); S = 0 when even S = 2 does
+// not fit (large batches: ticket merge).
+struct ClusterPlan {
+  int splits;
+  Shape shape;
+};
+
+ClusterPlan auto_cluster_plan(const pkv_pool* pool, int batch) {
   const int max_pages = pool->cfg.max_seq_len / kPage;
-  for (int s = pool->max_cluster; s >= 2; s /= 2) {
-    if (s > pool->cfg.max_splits || s > max_pages) continue;
-    if (static_cast<long long>(batch) * kHkv * s <= resident) return s;
+  const long long narrow = static_cast<long long>(pool->cluster_blocks_per_sm) * pool->num_sms;
+  const long long wide = static_cast<long long>(pool->wide_blocks_per_sm) * pool->num_sms;
+  auto usable = [&](int s) {
+    return s <= pool->max_cluster && s <= pool->cfg.max_splits && s <= max_pages;
+  };
+  for (int s = kMaxClusterSize; s >= 8; s /= 2) {
+    if (usable(s) && 16 * static_cast<long long>(batch) * kHkv * s <= 9 * narrow)
+      return {s, kNarrowShape};
   }
-  return 0;
+  for (int s = 8; s >= 2; s /= 2) {
+    if (usable(s) && 32 * static_cast<long long>(batch) * kHkv * s <= 27 * wide)
+      return {s, kWideShape};
+  }
+  return {0, kTicketShape};
 }
 
 // Cluster size of the multi-layer launch: the largest S of 16, 8, 4, 2 (within
@@ -1457,8 +1514,11 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   // largest cluster this device schedules; otherwise (S = 1, S larger, or a
   // batch too large for one wave of clusters) global partials and a ticket.
   int cluster = 0;
+  Shape shape = kTicketShape;
   if (num_splits == 0) {
-    cluster = auto_cluster_splits(pool, batch);
+    const ClusterPlan plan = auto_cluster_plan(pool, batch);
+    cluster = plan.splits;
+    shape = plan.shape;
     if (cluster >= 2) {
       prm.num_splits = cluster;
       prm.chunk_pages = 0;
@@ -1470,22 +1530,31 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   } else {
     prm.num_splits = num_splits;
     prm.chunk_pages = 0;
-    if (num_splits >= 2 && num_splits <= pool->max_cluster) cluster = num_splits;
+    if (num_splits >= 2 && num_splits <= pool->max_cluster) {
+      // a chosen split count takes the narrow shape while its blocks fit one
+      // wave of it, the wide shape beyond
+      cluster = num_splits;
+      shape = static_cast<long long>(batch) * kHkv * num_splits <=
+                      static_cast<long long>(pool->cluster_blocks_per_sm) * pool->num_sms
+                  ? kNarrowShape
+                  : kWideShape;
+    }
   }
   const int grid_splits = prm.num_splits > 0 ? prm.num_splits
                                              : (max_pages + prm.chunk_pages - 1) / prm.chunk_pages;
   const long long blocks = static_cast<long long>(grid_splits) * kHkv * batch;
-  const long long resident =
-      static_cast<long long>(cluster ? pool->cluster_blocks_per_sm : pool->blocks_per_sm) *
-      pool->num_sms;
+  const int per_sm = shape == kNarrowShape  ? pool->cluster_blocks_per_sm
+                     : shape == kWideShape ? pool->wide_blocks_per_sm
+                                           : pool->blocks_per_sm;
+  const long long resident = static_cast<long long>(per_sm) * pool->num_sms;
   prm.early_trigger = blocks <= resident ? 1 : 0;
   // more than one wave of ticket-mode blocks: longest sequences first
   prm.longest_first = (!cluster && num_splits == 0 && blocks > resident) ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid_splits, kHkv, batch);
-  cfg.blockDim = dim3(block_threads(cluster != 0), 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(cluster != 0);
+  cfg.blockDim = dim3(block_threads(shape), 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes(shape);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attrs[2];
   int n_attrs = 0;
@@ -1505,11 +1574,13 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   cfg.numAttrs = n_attrs;
   cudaError_t e;
   if (rope) {
-    e = cluster ? cudaLaunchKernelEx(&cfg, cluster_kernel<kFused, true>, prm)
-                : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused, true>, prm);
+    e = shape == kNarrowShape ? cudaLaunchKernelEx(&cfg, narrow_kernel<kFused, true>, prm)
+        : shape == kWideShape ? cudaLaunchKernelEx(&cfg, wide_kernel<kFused, true>, prm)
+                              : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused, true>, prm);
   } else {
-    e = cluster ? cudaLaunchKernelEx(&cfg, cluster_kernel<kFused>, prm)
-                : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused>, prm);
+    e = shape == kNarrowShape ? cudaLaunchKernelEx(&cfg, narrow_kernel<kFused>, prm)
+        : shape == kWideShape ? cudaLaunchKernelEx(&cfg, wide_kernel<kFused>, prm)
+                              : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused>, prm);
   }
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return check_launch();
@@ -1542,7 +1613,7 @@ pkv_status static_scratch_address(StaticScratch** out) {
   if (!address[dev]) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return PKV_ERR_CUDA;
-    if (!set_kernel_attributes(ticket_kernel<false>, false)) return PKV_ERR_CUDA;
+    if (!set_kernel_attributes(ticket_kernel<false>, kTicketShape)) return PKV_ERR_CUDA;
     address[dev] = static_cast<StaticScratch*>(ptr);
   }
   *out = address[dev];
@@ -1607,7 +1678,8 @@ pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_
   prm.longest_first = 0;
   prm.rope_cos = nullptr;
   prm.rope_sin = nullptr;
-  ticket_kernel<false><<<dim3(num_splits, kHkv, batch), block_threads(false), smem_bytes(false),
+  ticket_kernel<false><<<dim3(num_splits, kHkv, batch), block_threads(kTicketShape),
+                         smem_bytes(kTicketShape),
                          s>>>(prm);
   return check_launch();
 }
@@ -1658,31 +1730,38 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
   ok = ok && cudaMemset(pool->tickets, 0, 2 * static_cast<size_t>(c.max_batch) * kHkv * sizeof(int)) ==
                  cudaSuccess;
   ok = ok && cudaMemset(pool->err, 0, sizeof(int)) == cudaSuccess;
-  ok = ok && set_kernel_attributes(ticket_kernel<false>, false);
-  ok = ok && set_kernel_attributes(ticket_kernel<true>, false);
-  ok = ok && set_kernel_attributes(cluster_kernel<false>, true);
-  ok = ok && set_kernel_attributes(cluster_kernel<true>, true);
-  ok = ok && set_kernel_attributes(ticket_kernel<false, true>, false);
-  ok = ok && set_kernel_attributes(ticket_kernel<true, true>, false);
-  ok = ok && set_kernel_attributes(cluster_kernel<false, true>, true);
-  ok = ok && set_kernel_attributes(cluster_kernel<true, true>, true);
+  ok = ok && set_kernel_attributes(ticket_kernel<false>, kTicketShape);
+  ok = ok && set_kernel_attributes(ticket_kernel<true>, kTicketShape);
+  ok = ok && set_kernel_attributes(narrow_kernel<false>, kNarrowShape);
+  ok = ok && set_kernel_attributes(narrow_kernel<true>, kNarrowShape);
+  ok = ok && set_kernel_attributes(wide_kernel<false>, kWideShape);
+  ok = ok && set_kernel_attributes(wide_kernel<true>, kWideShape);
+  ok = ok && set_kernel_attributes(ticket_kernel<false, true>, kTicketShape);
+  ok = ok && set_kernel_attributes(ticket_kernel<true, true>, kTicketShape);
+  ok = ok && set_kernel_attributes(narrow_kernel<false, true>, kNarrowShape);
+  ok = ok && set_kernel_attributes(narrow_kernel<true, true>, kNarrowShape);
+  ok = ok && set_kernel_attributes(wide_kernel<false, true>, kWideShape);
+  ok = ok && set_kernel_attributes(wide_kernel<true, true>, kWideShape);
   ok = ok && cudaFuncSetAttribute(decode_layers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(sizeof(LayersSmem))) == cudaSuccess;
   ok = ok && cudaFuncSetAttribute(decode_layers_kernel,
                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
 
   ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                  &pool->blocks_per_sm, ticket_kernel<true>, block_threads(false),
-                  smem_bytes(false)) == cudaSuccess;
+                  &pool->blocks_per_sm, ticket_kernel<true>, block_threads(kTicketShape),
+                  smem_bytes(kTicketShape)) == cudaSuccess;
   ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                  &pool->cluster_blocks_per_sm, cluster_kernel<true>, block_threads(true),
-                  smem_bytes(true)) == cudaSuccess;
+                  &pool->cluster_blocks_per_sm, narrow_kernel<true>, block_threads(kNarrowShape),
+                  smem_bytes(kNarrowShape)) == cudaSuccess;
+  ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                  &pool->wide_blocks_per_sm, wide_kernel<true>, block_threads(kWideShape),
+                  smem_bytes(kWideShape)) == cudaSuccess;
   pool->max_cluster = 0;
   for (int size = kMaxClusterSize; ok && size >= 2 && !pool->max_cluster; size /= 2) {
     cudaLaunchConfig_t probe = {};
     probe.gridDim = dim3(size, kHkv, 1);
-    probe.blockDim = dim3(block_threads(true), 1, 1);
-    probe.dynamicSmemBytes = smem_bytes(true);
+    probe.blockDim = dim3(block_threads(kNarrowShape), 1, 1);
+    probe.dynamicSmemBytes = smem_bytes(kNarrowShape);
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = size;
@@ -1691,7 +1770,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
     probe.attrs = &attr;
     probe.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, cluster_kernel<true>, &probe) ==
+    if (cudaOccupancyMaxActiveClusters(&clusters, narrow_kernel<true>, &probe) ==
             cudaSuccess && clusters > 0)
       pool->max_cluster = size;
     cudaGetLastError();   // a size the device refuses is not an error here
@@ -1721,6 +1800,7 @@ pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {
   }
   if (ok && pool->blocks_per_sm < 1) pool->blocks_per_sm = 1;
   if (ok && pool->cluster_blocks_per_sm < 1) pool->cluster_blocks_per_sm = 1;
+  if (ok && pool->wide_blocks_per_sm < 1) pool->wide_blocks_per_sm = 1;
 
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
@@ -1849,7 +1929,7 @@ pkv_status pkv_append_attend_layers(pkv_pool_t pool, int layer_begin, int num_la
 
   const int max_pages = c.max_seq_len / kPage;
   const int chunk_max = (max_pages + S - 1) / S;
-  const int per_launch = kLayerTab / chunk_max;   // >= 8: chunk_max <= 64
+  const int per_launch = kLayerTab / chunk_max;   // >= 4: chunk_max <= 64
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int j0 = 0; j0 < num_layers; j0 += per_launch) {
     const int J = std::min(per_launch, num_layers - j0);

@@ -12,7 +12,8 @@ struct pkv_pool {
   int device;
   int num_sms;
   int blocks_per_sm;           // resident decode blocks per SM (occupancy API)
-  int cluster_blocks_per_sm;   // the same for the cluster-merge kernel
+  int cluster_blocks_per_sm;   // the same for the narrow cluster-merge kernel
+  int wide_blocks_per_sm;      // the same for the wide cluster-merge kernel
   int max_cluster;     // largest cluster size (power of two <= 16) the device schedules
   float* part_o;     // [2][max_batch][32][max_splits][64]
   float2* part_ml;   // [2][max_batch][32][max_splits]

@@ -55,7 +55,7 @@ WORKLOADS = {
     # every page-boundary case, 3 layers, fragmented pool
     "edges": lambda: W.custom([1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 1000, 2047, 2048],
                               num_layers=3, seed=702, hole_every=3, name="edges"),
-    # 16 sequences: S = 2, so 8 layers per launch and 20 layers take 3 launches
+    # 16 sequences: S = 2, so 4 layers per launch and 20 layers take 5 launches
     "b16-20layers": lambda: W.custom(list(np.random.default_rng(703).integers(1, 300, 16)),
                                      num_layers=20, seed=703, name="b16-20"),
 }

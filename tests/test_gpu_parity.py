@@ -113,6 +113,36 @@ def test_split_counts_against_unsplit_oracle(batch):
     assert np.abs(results[1] - results[32]).max() <= 2 * 5e-4
 
 
+@pytest.mark.parametrize("batch", [5, 8, 16, 32])
+def test_library_cluster_plans_match_oracle(batch):
+    """Batches whose library plan is the wide cluster shape (2 page stages, 4
+    blocks per SM; S = 8 for 5..8 sequences, 4 for 16, 2 for 32), with
+    mixed lengths, fused and unfused, against the unsplit oracle."""
+    rng = np.random.default_rng(310 + batch)
+    lens = rng.integers(1, 2049, batch)
+    lens[0] = 2048
+    wl = W.custom(list(lens), num_layers=2, seed=310 + batch, name=f"wide-b{batch}")
+    st = DeviceState(wl)
+    q_b, kn_b, vn_b = _host_inputs(st)
+    ref, ok, ov = oracle_step(wl, st.host_k, st.host_v, q_b, kn_b, vn_b)
+    for fused in (True, False):
+        pool = _pool(wl)
+        k0, v0 = st.k_pool.clone(), st.v_pool.clone()
+        out = torch.full_like(st.out, float("nan"))
+        for layer in range(wl.num_layers):
+            if fused:
+                pkv.pkv_append_attend(pool, layer, st.q[layer], st.k_new[layer], st.v_new[layer],
+                                      k0, v0, st.table, st.lens, out[layer])
+            else:
+                pkv.pkv_append(pool, layer, st.k_new[layer], st.v_new[layer], k0, v0, st.table,
+                               st.positions)
+                pkv.pkv_decode_attention(pool, layer, st.q[layer], k0, v0, st.table, st.lens,
+                                         out[layer])
+        assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+        assert np.array_equal(bits(k0), ok) and np.array_equal(bits(v0), ov)
+        assert_close(out.cpu().numpy(), ref, f"B={batch} fused={fused}")
+
+
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("graph", [False, True])
 def test_programmatic_dependent_launch_chain_matches_oracle(fused, graph):
