@@ -718,6 +718,103 @@ __device__ int longest_first_sequence(int z, int batch, const int32_t* seq_lens,
   return sm.order.pick[2];
 }
 
+// ---------------------------------------------------------------- ticket merge
+// A split's partial (M, L, O from block_merge: thread t of the 4-warp block
+// owns head t / 32, dims 2 (t % 32), + 1) into the handle's partials, one
+// ticket per (sequence, kv head), and the last split's log-sum-exp merge of
+// all n_splits partials into out. Called by every thread of the block.
+template <class Smem>
+__device__ __forceinline__ void ticket_merge(Smem& sm, float* part_o, float2* part_ml,
+                                             int* tickets, int max_splits, float* out, int b,
+                                             int kvh, int split, int n_splits, float M, float L,
+                                             float2 O, int warp, int lane) {
+  const int g = (threadIdx.x >> 5) & (kGroup - 1);
+  const int d0 = 2 * (threadIdx.x & 31);
+  // ---- split partial, ticket, and the last block's log-sum-exp merge
+  const size_t head0 = (static_cast<size_t>(b) * kHq + kvh * kGroup) * max_splits;
+  const size_t prow = head0 + static_cast<size_t>(g) * max_splits;
+  *reinterpret_cast<float2*>(part_o + (prow + split) * kDim + d0) = O;
+  if (d0 == 0) part_ml[prow + split] = make_float2(M, L);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // One acquire-release atomic after the barrier: its release publishes the
+    // partials every thread of this block wrote; for the last block its
+    // acquire makes the other blocks' partials visible (the barrier below
+    // passes that on to the block's other threads).
+    int* ticket = tickets + static_cast<size_t>(b) * kHkv + kvh;
+    int arrived;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                 : "=r"(arrived)
+                 : "l"(ticket)
+                 : "memory");
+    const int last = arrived == n_splits - 1;
+    if (last) *ticket = 0;   // every split has arrived: reset for the next launch
+    sm.last = last;
+  }
+  __syncthreads();
+  if (!sm.last) return;
+
+  // Warp hg merges head hg; lane (quad, half) owns dims 4 quad .. 4 quad + 3
+  // over the splits s = half, half + 2, ...: an online log-sum-exp merge of
+  // (m_s, l_s, o_s) loaded straight from L2 (bypassing L1, which may hold
+  // lines of an earlier launch), then the two halves combine by shuffle.
+  {
+    const int hg = warp;
+    const int quad = lane & 15;
+    const int half = lane >> 4;
+    const size_t hrow = head0 + static_cast<size_t>(hg) * max_splits;
+    float mrun = -INFINITY, lrun = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = half; s0 < n_splits; s0 += 16) {
+      float2 ml[8];
+      float4 v[8];
+      #pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int s = s0 + 2 * j;
+        ml[j] = s < n_splits ? __ldcg(&part_ml[hrow + s]) : make_float2(-INFINITY, 0.f);
+        v[j] = s < n_splits
+                   ? __ldcg(reinterpret_cast<const float4*>(part_o + (hrow + s) * kDim + 4 * quad))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float mnew = mrun;
+      #pragma unroll
+      for (int j = 0; j < 8; ++j) mnew = fmaxf(mnew, ml[j].x);
+      if (mnew == -INFINITY) continue;
+      const float a = fast_exp2(mrun - mnew);   // 0 while nothing was merged
+      lrun *= a;
+      o = make_float4(o.x * a, o.y * a, o.z * a, o.w * a);
+      #pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w = fast_exp2(ml[j].x - mnew);   // 0 for an absent split
+        lrun += w * ml[j].y;
+        o.x += w * v[j].x;
+        o.y += w * v[j].y;
+        o.z += w * v[j].z;
+        o.w += w * v[j].w;
+      }
+      mrun = mnew;
+    }
+    // combine with the other half (lane ^ 16)
+    const float mo = __shfl_xor_sync(0xffffffffu, mrun, 16);
+    const float lo = __shfl_xor_sync(0xffffffffu, lrun, 16);
+    const float4 oo = make_float4(__shfl_xor_sync(0xffffffffu, o.x, 16),
+                                  __shfl_xor_sync(0xffffffffu, o.y, 16),
+                                  __shfl_xor_sync(0xffffffffu, o.z, 16),
+                                  __shfl_xor_sync(0xffffffffu, o.w, 16));
+    const float mx = fmaxf(mrun, mo);
+    const float wa = mrun == -INFINITY ? 0.f : fast_exp2(mrun - mx);
+    const float wb = mo == -INFINITY ? 0.f : fast_exp2(mo - mx);
+    const float LL = wa * lrun + wb * lo;
+    if (half == 0) {
+      const float inv = LL > 0.f ? 1.f / LL : 0.f;
+      *reinterpret_cast<float4*>(out + (static_cast<size_t>(b) * kHq + kvh * kGroup + hg) *
+                                               kDim + 4 * quad) =
+          make_float4((wa * o.x + wb * oo.x) * inv, (wa * o.y + wb * oo.y) * inv,
+                      (wa * o.z + wb * oo.z) * inv, (wa * o.w + wb * oo.w) * inv);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- decode
 // kCluster: the splits of one (sequence, kv head) form one thread-block
 // cluster (gridDim.x == cluster size) and merge through distributed shared
@@ -993,91 +1090,10 @@ decode_kernel(const DecodeParams prm) {
   }
 
   if constexpr (!kCluster) {
-  static_assert(kWarps == kGroup, "the ticket merge maps one warp to each head");
-  // ---- split partial, ticket, and the last block's log-sum-exp merge
-  const size_t head0 = (static_cast<size_t>(b) * kHq + kvh * kGroup) * prm.max_splits;
-  const size_t prow = head0 + static_cast<size_t>(g) * prm.max_splits;
-  *reinterpret_cast<float2*>(prm.part_o + (prow + split) * kDim + d0) = O;
-  if (d0 == 0) prm.part_ml[prow + split] = make_float2(M, L);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    // One acquire-release atomic after the barrier: its release publishes the
-    // partials every thread of this block wrote; for the last block its
-    // acquire makes the other blocks' partials visible (the barrier below
-    // passes that on to the block's other threads).
-    int* ticket = prm.tickets + static_cast<size_t>(b) * kHkv + kvh;
-    int arrived;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                 : "=r"(arrived)
-                 : "l"(ticket)
-                 : "memory");
-    const int last = arrived == n_splits - 1;
-    if (last) *ticket = 0;   // every split has arrived: reset for the next launch
-    sm.last = last;
+    static_assert(kWarps == kGroup, "the ticket merge maps one warp to each head");
+    ticket_merge(sm, prm.part_o, prm.part_ml, prm.tickets, prm.max_splits, prm.out, b, kvh, split,
+                 n_splits, M, L, O, warp, lane);
   }
-  __syncthreads();
-  if (!sm.last) return;
-
-  // Warp hg merges head hg; lane (quad, half) owns dims 4 quad .. 4 quad + 3
-  // over the splits s = half, half + 2, ...: an online log-sum-exp merge of
-  // (m_s, l_s, o_s) loaded straight from L2 (bypassing L1, which may hold
-  // lines of an earlier launch), then the two halves combine by shuffle.
-  {
-    const int hg = warp;
-    const int quad = lane & 15;
-    const int half = lane >> 4;
-    const size_t hrow = head0 + static_cast<size_t>(hg) * prm.max_splits;
-    float mrun = -INFINITY, lrun = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = half; s0 < n_splits; s0 += 16) {
-      float2 ml[8];
-      float4 v[8];
-      #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int s = s0 + 2 * j;
-        ml[j] = s < n_splits ? __ldcg(&prm.part_ml[hrow + s]) : make_float2(-INFINITY, 0.f);
-        v[j] = s < n_splits
-                   ? __ldcg(reinterpret_cast<const float4*>(prm.part_o + (hrow + s) * kDim + 4 * quad))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      float mnew = mrun;
-      #pragma unroll
-      for (int j = 0; j < 8; ++j) mnew = fmaxf(mnew, ml[j].x);
-      if (mnew == -INFINITY) continue;
-      const float a = fast_exp2(mrun - mnew);   // 0 while nothing was merged
-      lrun *= a;
-      o = make_float4(o.x * a, o.y * a, o.z * a, o.w * a);
-      #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float w = fast_exp2(ml[j].x - mnew);   // 0 for an absent split
-        lrun += w * ml[j].y;
-        o.x += w * v[j].x;
-        o.y += w * v[j].y;
-        o.z += w * v[j].z;
-        o.w += w * v[j].w;
-      }
-      mrun = mnew;
-    }
-    // combine with the other half (lane ^ 16)
-    const float mo = __shfl_xor_sync(0xffffffffu, mrun, 16);
-    const float lo = __shfl_xor_sync(0xffffffffu, lrun, 16);
-    const float4 oo = make_float4(__shfl_xor_sync(0xffffffffu, o.x, 16),
-                                  __shfl_xor_sync(0xffffffffu, o.y, 16),
-                                  __shfl_xor_sync(0xffffffffu, o.z, 16),
-                                  __shfl_xor_sync(0xffffffffu, o.w, 16));
-    const float mx = fmaxf(mrun, mo);
-    const float wa = mrun == -INFINITY ? 0.f : fast_exp2(mrun - mx);
-    const float wb = mo == -INFINITY ? 0.f : fast_exp2(mo - mx);
-    const float LL = wa * lrun + wb * lo;
-    if (half == 0) {
-      const float inv = LL > 0.f ? 1.f / LL : 0.f;
-      *reinterpret_cast<float4*>(prm.out + (static_cast<size_t>(b) * kHq + kvh * kGroup + hg) *
-                                               kDim + 4 * quad) =
-          make_float4((wa * o.x + wb * oo.x) * inv, (wa * o.y + wb * oo.y) * inv,
-                      (wa * o.z + wb * oo.z) * inv, (wa * o.w + wb * oo.w) * inv);
-    }
-  }
-  }  // ticket merge
 }
 
 // ---------------------------------------------------------------- layer stack

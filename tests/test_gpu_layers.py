@@ -134,6 +134,7 @@ def test_graph_replay_repeats_the_step():
     st = DeviceState(wl, host_pools=False)
     pool = _pool(wl)
     s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())   # the inputs were made on the current stream
     with torch.cuda.stream(s):
         pkv.pkv_append_attend_layers(pool, 0, st.q, st.k_new, st.v_new, st.k_pool, st.v_pool,
                                      st.table, st.lens, st.out, stream=s)

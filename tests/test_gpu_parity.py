@@ -437,3 +437,59 @@ def test_longest_first_order_large_batch():
     keep = np.ones(wl.batch, bool)
     keep[7] = False
     assert_close(got[keep], ref[0][keep], "others with one invalid length")
+
+
+@pytest.mark.parametrize("pdl", [False, True])
+def test_large_batch_fused_chain_matches_oracle(pdl):
+    """The fused step at a large batch (the library's ticket-merge plan,
+    sequences handed out longest first): lengths over the whole range,
+    page-boundary cases, a fragmented pool, three layers chained (with
+    programmatic dependent launch, also replayed from a CUDA graph), against
+    the oracle; then one invalid length is flagged and skipped."""
+    rng = np.random.default_rng(450)
+    lens = rng.integers(1, 2049, size=120).astype(np.int32)
+    lens[:8] = [1, 16, 17, 128, 129, 2047, 2048, 8 * 16 + 1]
+    wl = W.custom(lens, num_layers=3, seed=451, hole_every=3, name="large-fused")
+    st = DeviceState(wl)
+    ref, ok, ov = oracle_step(wl, st.host_k, st.host_v, *_host_inputs(st))
+    pool = _pool(wl, flags=pkv.PKV_FLAG_PDL if pdl else 0)
+    kp, vp = st.k_pool.clone(), st.v_pool.clone()
+    out = torch.full_like(st.out, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())   # the copies above run on the current stream
+
+    def chain(stream):
+        for layer in range(wl.num_layers):
+            pkv.pkv_append_attend(pool, layer, st.q[layer], st.k_new[layer], st.v_new[layer], kp,
+                                  vp, st.table, st.lens, out[layer], stream=stream)
+
+    with torch.cuda.stream(s):
+        chain(s)
+    s.synchronize()
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    assert np.array_equal(bits(kp), ok) and np.array_equal(bits(vp), ov)
+    assert_close(out.cpu().numpy(), ref, f"large batch pdl={pdl}")
+    if pdl:
+        first = out.clone()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            chain(torch.cuda.current_stream())
+        for _ in range(2):
+            out.fill_(float("nan"))
+            with torch.cuda.stream(s):
+                graph.replay()
+            s.synchronize()
+            assert torch.equal(out.view(torch.int32), first.view(torch.int32))
+        assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    bad = st.lens.clone()
+    bad[9] = 0
+    out2 = torch.full_like(st.out[0], float("nan"))
+    kp2, vp2 = kp.clone(), vp.clone()
+    pkv.pkv_append_attend(pool, 0, st.q[0], st.k_new[0], st.v_new[0], kp2, vp2, st.table, bad,
+                          out2)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_ERR_OUT_OF_RANGE
+    got = out2.cpu().numpy()
+    assert np.all(np.isnan(got[9]))
+    keep = np.ones(wl.batch, bool)
+    keep[9] = False
+    assert_close(got[keep], ref[0][keep], "large batch, one invalid length")
