@@ -232,6 +232,19 @@ pkv_status pkv_append_attend_layers(pkv_pool_t pool, int layer_begin, int num_la
                                     const int32_t* seq_lens, float* out, int batch,
                                     void* stream);
 
+/* Test hook for failure detection: the same launch as
+ * pkv_append_attend_layers with every between-layer wait made unreachable
+ * (its target raised by one), so each block's first wait runs out after about
+ * two seconds; the block flags PKV_ERR_DEVICE_TIMEOUT, stops waiting and
+ * finishes (outputs then carry no layer-order guarantee). No GPU fault; the
+ * context stays usable. Returns UNSUPPORTED for a batch that would run as
+ * per-layer launches. */
+pkv_status pkv_test_layers_wait_timeout(pkv_pool_t pool, int layer_begin, int num_layers,
+                                        const void* q, const void* k, const void* v,
+                                        void* k_pool, void* v_pool, const int32_t* block_tables,
+                                        const int32_t* seq_lens, float* out, int batch,
+                                        void* stream);
+
 /* Synchronises `stream`, then returns and clears the sticky device error
  * flag: PKV_OK, PKV_ERR_OUT_OF_RANGE or PKV_ERR_DEVICE_TIMEOUT (or CUDA if
  * the synchronisation itself failed). */

@@ -27,7 +27,8 @@ PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OUT_OF_RANGE, PKV_ERR_CUDA, PKV_ERR_UNSUPPO
 
 EXPORTED = ("pkv_pool_create", "pkv_pool_destroy", "pkv_append", "pkv_decode_attention",
             "pkv_append_attend", "pkv_append_rope", "pkv_decode_attention_rope",
-            "pkv_append_attend_rope", "pkv_append_attend_layers", "pkv_get_error", "pkv_decode_attention_noalloc",
+            "pkv_append_attend_rope", "pkv_append_attend_layers", "pkv_test_layers_wait_timeout",
+            "pkv_get_error", "pkv_decode_attention_noalloc",
             "pkv_sched_budget", "pkv_sched_create", "pkv_sched_destroy", "pkv_sched_submit",
             "pkv_sched_admit", "pkv_sched_extend", "pkv_sched_extend_batch", "pkv_sched_finish",
             "pkv_sched_decode_batch",
@@ -88,6 +89,7 @@ def load(path: str = None):
     lib.pkv_decode_attention_rope.argtypes = [P, i, P, P, P, P, P, P, P, P, i, i, P]
     lib.pkv_append_attend_rope.argtypes = [P, i, P, P, P, P, P, P, P, P, P, P, i, i, P]
     lib.pkv_append_attend_layers.argtypes = [P, i, i, P, P, P, P, P, P, P, P, i, P]
+    lib.pkv_test_layers_wait_timeout.argtypes = [P, i, i, P, P, P, P, P, P, P, P, i, P]
     lib.pkv_get_error.argtypes = [P, P]
     lib.pkv_decode_attention_noalloc.argtypes = [i, P, P, P, P, P, P, i, i, i, i, i, i, P, P]
     SC, SP = ctypes.POINTER(SchedConfig), ctypes.POINTER(ctypes.c_int)
@@ -249,6 +251,20 @@ def pkv_append_attend_layers(pool: Pool, layer_begin, q, k, v, k_pool, v_pool, b
                                             _addr(block_tables), _addr(seq_lens), _addr(out),
                                             _batch(seq_lens, batch), _stream(stream))
     _check(st, "pkv_append_attend_layers")
+
+
+def pkv_test_layers_wait_timeout(pool: Pool, layer_begin, q, k, v, k_pool, v_pool,
+                                 block_tables, seq_lens, out, num_layers=None, batch=None,
+                                 stream=None):
+    """Failure-detection test hook: pkv_append_attend_layers with every
+    between-layer wait unreachable; the device flags a timeout."""
+    J = int(q.shape[0]) if num_layers is None else int(num_layers)
+    st = pool._lib.pkv_test_layers_wait_timeout(pool.handle, int(layer_begin), J, _addr(q),
+                                                _addr(k), _addr(v), _addr(k_pool),
+                                                _addr(v_pool), _addr(block_tables),
+                                                _addr(seq_lens), _addr(out),
+                                                _batch(seq_lens, batch), _stream(stream))
+    _check(st, "pkv_test_layers_wait_timeout")
 
 
 def pkv_get_error(pool: Pool, stream=None) -> int:

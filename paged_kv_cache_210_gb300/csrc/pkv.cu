@@ -1128,6 +1128,7 @@ struct LayersParams {
   int max_seq_len;
   int batch;
   int num_layers;             // layers of this launch
+  int wait_extra;             // added to every wait's target: 0, or 1 from the timeout test hook
 };
 
 struct alignas(16) LayersSmem {
@@ -1271,7 +1272,8 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 4) decode_layers_kernel(co
   bool waits_off = false;    // a sequence wait gave up: the block stops waiting (flagged)
   for (int j = 0; j < J; ++j) {
     if (j > 0 && !waits_off) {
-      if (threadIdx.x == 0) ls.flag = wait_count(prm.seq_done + b, j * arrivals) ? 0 : 1;
+      if (threadIdx.x == 0)
+        ls.flag = wait_count(prm.seq_done + b, j * arrivals + prm.wait_extra) ? 0 : 1;
       __syncthreads();
       if (ls.flag) {
         waits_off = true;
@@ -1905,11 +1907,16 @@ pkv_status pkv_append_attend(pkv_pool_t pool, int layer, const void* q, const vo
                              batch, num_splits, stream);
 }
 
-pkv_status pkv_append_attend_layers(pkv_pool_t pool, int layer_begin, int num_layers,
-                                    const void* q, const void* k, const void* v, void* k_pool,
-                                    void* v_pool, const int32_t* block_tables,
-                                    const int32_t* seq_lens, float* out, int batch,
-                                    void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The multi-layer step; wait_extra > 0 makes every layer wait unreachable
+// (the timeout test hook), and then there is no per-layer fallback.
+pkv_status launch_layers(pkv_pool_t pool, int layer_begin, int num_layers, const void* q,
+                         const void* k, const void* v, void* k_pool, void* v_pool,
+                         const int32_t* block_tables, const int32_t* seq_lens, float* out,
+                         int batch, void* stream, int wait_extra) {
   if (!pool) return PKV_ERR_INVALID_ARG;
   const pkv_pool_config& c = pool->cfg;
   if (layer_begin < 0 || num_layers < 0 ||
@@ -1931,6 +1938,7 @@ pkv_status pkv_append_attend_layers(pkv_pool_t pool, int layer_begin, int num_la
   const uint16_t* k16 = static_cast<const uint16_t*>(k);
   const uint16_t* v16 = static_cast<const uint16_t*>(v);
   const int S = layers_cluster_splits(pool, batch);
+  if (S == 0 && wait_extra) return PKV_ERR_UNSUPPORTED;
   if (S == 0) {
     // too many sequences for a resident grid: one fused launch per layer
     for (int j = 0; j < num_layers; ++j) {
@@ -1969,6 +1977,7 @@ pkv_status pkv_append_attend_layers(pkv_pool_t pool, int layer_begin, int num_la
     prm.max_seq_len = c.max_seq_len;
     prm.batch = batch;
     prm.num_layers = J;
+    prm.wait_extra = wait_extra;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, kHkv, batch);
@@ -1985,6 +1994,28 @@ pkv_status pkv_append_attend_layers(pkv_pool_t pool, int layer_begin, int num_la
     if (cudaLaunchKernelEx(&cfg, decode_layers_kernel, prm) != cudaSuccess) return PKV_ERR_CUDA;
   }
   return check_launch();
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_append_attend_layers(pkv_pool_t pool, int layer_begin, int num_layers,
+                                    const void* q, const void* k, const void* v, void* k_pool,
+                                    void* v_pool, const int32_t* block_tables,
+                                    const int32_t* seq_lens, float* out, int batch,
+                                    void* stream) {
+  return launch_layers(pool, layer_begin, num_layers, q, k, v, k_pool, v_pool, block_tables,
+                       seq_lens, out, batch, stream, 0);
+}
+
+pkv_status pkv_test_layers_wait_timeout(pkv_pool_t pool, int layer_begin, int num_layers,
+                                        const void* q, const void* k, const void* v,
+                                        void* k_pool, void* v_pool, const int32_t* block_tables,
+                                        const int32_t* seq_lens, float* out, int batch,
+                                        void* stream) {
+  return launch_layers(pool, layer_begin, num_layers, q, k, v, k_pool, v_pool, block_tables,
+                       seq_lens, out, batch, stream, 1);
 }
 
 pkv_status pkv_decode_attention_rope(pkv_pool_t pool, int layer, const void* q,

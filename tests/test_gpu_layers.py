@@ -203,3 +203,25 @@ def test_host_argument_checks():
     pkv.pkv_append_attend_layers(pool, 0, st.q, st.k_new, st.v_new, st.k_pool, st.v_pool,
                                  st.table, st.lens, st.out, num_layers=0)
     assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+
+
+def test_layer_wait_timeout_is_flagged_and_the_context_stays_usable():
+    """Failure detection without a GPU fault: the test hook makes every
+    between-layer wait unreachable, so each block gives up after its bounded
+    wait (about two seconds), flags the timeout and finishes; the host reads
+    PKV_ERR_DEVICE_TIMEOUT, and the next normal step is correct."""
+    wl = W.custom([300, 2048], num_layers=2, seed=708, name="timeout")
+    st = DeviceState(wl)
+    pool = _pool(wl)
+    kp, vp = st.k_pool.clone(), st.v_pool.clone()
+    out = torch.full_like(st.out, float("nan"))
+    pkv.pkv_test_layers_wait_timeout(pool, 0, st.q, st.k_new, st.v_new, kp, vp, st.table,
+                                     st.lens, out)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_ERR_DEVICE_TIMEOUT
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK          # the flag was cleared
+    pkv.pkv_append_attend_layers(pool, 0, st.q, st.k_new, st.v_new, st.k_pool, st.v_pool,
+                                 st.table, st.lens, st.out)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    ref, ok, ov = oracle_step(wl, st.host_k, st.host_v, *_host_inputs(st))
+    assert np.array_equal(bits(st.k_pool), ok) and np.array_equal(bits(st.v_pool), ov)
+    assert_close(st.out.cpu().numpy(), ref, "after a timeout")
