@@ -103,7 +103,8 @@ typedef struct pkv_pool* pkv_pool_t;
 /* Validates the geometry and creates a handle on the current device. The
  * handle owns only device scratch: the split-KV partials (two layer-parity
  * copies of max_batch x 32 x max_splits x (64 + 2) floats), one ticket
- * counter per (sequence, kv head) and parity, and the sticky error flag.
+ * counter per (sequence, kv head) and parity, one layer counter per sequence
+ * (pkv_append_attend_layers) and the sticky error flag.
  * It does not own the pools, tables or tensors. Returns INVALID_ARG for a
  * null argument, UNSUPPORTED for a geometry other than the one above, CUDA
  * if an allocation fails. */
@@ -136,8 +137,10 @@ pkv_status pkv_append(pkv_pool_t pool, int layer, const void* k, const void* v, 
  * blocks of a (sequence, kv head) form a thread-block cluster and merge
  * through distributed shared memory; otherwise through the handle's global
  * partials and a ticket (the last block to finish merges). num_splits = 0
- * lets the library choose: a cluster split sized so the batch fits one wave
- * of resident blocks, or for large batches ranges of a fixed page count.
+ * lets the library choose: for up to 32 sequences a cluster split and a
+ * block shape (page stages per warp, blocks per SM) from plans measured on
+ * GB300, for larger batches ranges of a fixed page count with the ticket
+ * merge, longest sequences first.
  * S must not exceed max_splits. The
  * output does not depend on which physical pages hold the data. A sequence
  * with an invalid seq_len is skipped (its out rows are left untouched) and
