@@ -248,6 +248,55 @@ pkv_status pkv_test_layers_wait_timeout(pkv_pool_t pool, int layer_begin, int nu
                                         const int32_t* seq_lens, float* out, int batch,
                                         void* stream);
 
+/* The launch plan of pkv_decode_attention and pkv_append_attend (and their
+ * rotary variants) for a batch, from the device figures a handle records.
+ * pkv_plan_decode is plain host arithmetic (no GPU needed), the same function
+ * the launches call.
+ *
+ * Plans (num_splits = 0): for up to 32 sequences a thread-block cluster of S
+ * blocks per (sequence, kv head) in the narrow shape (3 page stages per
+ * warp) with S = 16 or 8 while its blocks take at most 9/16 of the narrow
+ * shape's resident slots, else the wide shape (2 stages, 4 blocks per SM)
+ * with the largest S <= 8 whose blocks take at most 27/32 of its slots;
+ * larger batches take the ticket merge with ranges of 128, 64, 32 or 16
+ * pages (the largest leaving >= 3 blocks per resident ticket slot for
+ * full-length sequences, at least max_seq_len / 16 / max_splits). A chosen
+ * num_splits = S takes a cluster for 2 <= S <= max_cluster (narrow while its
+ * blocks fit one wave of it, else wide), the ticket merge otherwise. */
+typedef struct {
+  int num_sms;                /* streaming multiprocessors */
+  int ticket_blocks_per_sm;   /* resident blocks per SM of the ticket-merge shape */
+  int narrow_blocks_per_sm;   /* ... of the narrow cluster shape */
+  int wide_blocks_per_sm;     /* ... of the wide cluster shape */
+  int max_cluster;            /* largest cluster (power of two <= 16) the device schedules; 0: none */
+  int max_splits;             /* the handle's max_splits (after the default) */
+  int max_seq_len;            /* the handle's max_seq_len */
+} pkv_device_figures;
+
+#define PKV_SHAPE_TICKET 0
+#define PKV_SHAPE_NARROW 1
+#define PKV_SHAPE_WIDE 2
+
+typedef struct {
+  int shape;          /* PKV_SHAPE_* */
+  int cluster;        /* blocks per cluster (the split count) for the cluster shapes, else 0 */
+  int num_splits;     /* splits per sequence (cluster plans, chosen counts), else 0 */
+  int chunk_pages;    /* pages per range when num_splits == 0, else 0 */
+  int grid_splits;    /* blocks per (sequence, kv head) in the grid */
+  int early_trigger;  /* the grid fits one wave: dependents may start after the prefetch */
+  int longest_first;  /* several waves of ticket blocks: sequences taken longest first */
+} pkv_plan;
+
+/* INVALID_ARG for null pointers, figures out of range (num_sms, blocks per
+ * SM < 1; max_splits outside [1, 128]; max_seq_len not a multiple of 16 in
+ * [16, 2048]; max_cluster outside [0, 16]), batch < 1 or num_splits outside
+ * [0, max_splits]. */
+pkv_status pkv_plan_decode(const pkv_device_figures* dev, int batch, int num_splits,
+                           pkv_plan* out);
+
+/* The figures of the handle's device and geometry (no GPU work). */
+pkv_status pkv_pool_device_figures(pkv_pool_t pool, pkv_device_figures* out);
+
 /* Synchronises `stream`, then returns and clears the sticky device error
  * flag: PKV_OK, PKV_ERR_OUT_OF_RANGE or PKV_ERR_DEVICE_TIMEOUT (or CUDA if
  * the synchronisation itself failed). */

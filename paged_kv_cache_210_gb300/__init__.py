@@ -33,7 +33,8 @@ EXPORTED = ("pkv_pool_create", "pkv_pool_destroy", "pkv_append", "pkv_decode_att
             "pkv_sched_admit", "pkv_sched_extend", "pkv_sched_extend_batch", "pkv_sched_finish",
             "pkv_sched_decode_batch",
             "pkv_sched_block_tables", "pkv_sched_get_stats", "pkv_prefill_fill",
-            "pkv_prefill_attention", "pkv_prefill", "pkv_status_string")
+            "pkv_prefill_attention", "pkv_prefill", "pkv_plan_decode",
+            "pkv_pool_device_figures", "pkv_status_string")
 
 
 class PkvError(RuntimeError):
@@ -61,6 +62,21 @@ class PoolConfig(ctypes.Structure):
 
 
 PKV_FLAG_PDL = 1
+
+
+class DeviceFigures(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "num_sms", "ticket_blocks_per_sm", "narrow_blocks_per_sm", "wide_blocks_per_sm",
+        "max_cluster", "max_splits", "max_seq_len")]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "shape", "cluster", "num_splits", "chunk_pages", "grid_splits", "early_trigger",
+        "longest_first")]
+
+
+PKV_SHAPE_TICKET, PKV_SHAPE_NARROW, PKV_SHAPE_WIDE = 0, 1, 2
 
 
 _lib = None
@@ -107,6 +123,8 @@ def load(path: str = None):
     lib.pkv_prefill_fill.argtypes = [P, i, P, P, P, P, P, P, P, i, i, i, P]
     lib.pkv_prefill_attention.argtypes = [P, i, P, P, P, P, P, P, P, i, i, i, P]
     lib.pkv_prefill.argtypes = [P, i, P, P, P, P, P, P, P, P, P, i, i, i, P]
+    lib.pkv_plan_decode.argtypes = [ctypes.POINTER(DeviceFigures), i, i, ctypes.POINTER(Plan)]
+    lib.pkv_pool_device_figures.argtypes = [P, ctypes.POINTER(DeviceFigures)]
     lib.pkv_status_string.argtypes = [i]
     lib.pkv_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -265,6 +283,22 @@ def pkv_test_layers_wait_timeout(pool: Pool, layer_begin, q, k, v, k_pool, v_poo
                                                 _addr(seq_lens), _addr(out),
                                                 _batch(seq_lens, batch), _stream(stream))
     _check(st, "pkv_test_layers_wait_timeout")
+
+
+def pkv_plan_decode(figures: DeviceFigures, batch, num_splits=0, lib=None) -> Plan:
+    """The decode launch plan for a batch on a device (host arithmetic, no GPU)."""
+    lib = lib or load()
+    plan = Plan()
+    _check(lib.pkv_plan_decode(ctypes.byref(figures), int(batch), int(num_splits),
+                               ctypes.byref(plan)), "pkv_plan_decode")
+    return plan
+
+
+def pkv_pool_device_figures(pool: Pool) -> DeviceFigures:
+    figures = DeviceFigures()
+    _check(pool._lib.pkv_pool_device_figures(pool.handle, ctypes.byref(figures)),
+           "pkv_pool_device_figures")
+    return figures
 
 
 def pkv_get_error(pool: Pool, stream=None) -> int:

@@ -1410,6 +1410,10 @@ pkv_status check_launch() {
 }
 
 
+static_assert(kTicketShape == PKV_SHAPE_TICKET && kNarrowShape == PKV_SHAPE_NARROW &&
+                  kWideShape == PKV_SHAPE_WIDE,
+              "the plan's shape codes are the kernel shapes");
+
 // Pages per block when the caller leaves the choice to the library and the
 // batch is too large for a cluster split: the largest of 128, 64, 32, 16
 // pages for which a batch of full-length sequences still yields at least
@@ -1417,10 +1421,10 @@ pkv_status check_launch() {
 // blocks per slot leave SMs idle behind the longest sequences; more, smaller
 // ranges pay a partial merge for nothing (measured: 256 sequences run best
 // unsplit, 64 log-uniform ones with 32-page ranges).
-int auto_chunk_pages(const pkv_pool* pool, int batch) {
-  const int max_pages = pool->cfg.max_seq_len / kPage;
-  const int min_chunk = (max_pages + pool->cfg.max_splits - 1) / pool->cfg.max_splits;
-  const long long resident = static_cast<long long>(pool->blocks_per_sm) * pool->num_sms;
+int auto_chunk_pages(const pkv_device_figures& d, int batch) {
+  const int max_pages = d.max_seq_len / kPage;
+  const int min_chunk = (max_pages + d.max_splits - 1) / d.max_splits;
+  const long long resident = static_cast<long long>(d.ticket_blocks_per_sm) * d.num_sms;
   int chunk = 16;
   for (int c = 128; c >= 16; c /= 2) {
     const long long blocks = static_cast<long long>(batch) * kHkv * ((max_pages + c - 1) / c);
@@ -1433,9 +1437,9 @@ int auto_chunk_pages(const pkv_pool* pool, int batch) {
   return chunk < min_chunk ? min_chunk : chunk;
 }
 
-// Cluster plan when the library chooses: the split count S (16, 8, 4, 2) and
-// the block shape. Measured on a 152-SM GB300 with full-length sequences
-// (GB/s per 16-layer step, the plans per batch):
+// The launch plan for a batch. Cluster plans when the library chooses: the
+// split count S (16, 8, 4, 2) and the block shape, from a sweep on a 152-SM
+// GB300 with full-length sequences (GB/s per 16-layer step):
 //   batch 2:  narrow S = 16 (256 blocks) 1522; wide S = 16 1453; S = 8 1337;
 //   batch 4:  narrow S = 8 (256) 2304; narrow S = 16 1404; wide S = 8 2015;
 //   batch 8:  wide S = 8 (512) 3462; narrow S = 4 (256) 2680; wide S = 16 2016;
@@ -1443,29 +1447,68 @@ int auto_chunk_pages(const pkv_pool* pool, int batch) {
 // So: the narrow shape with the largest S whose blocks take at most 9/16 of
 // its resident slots (256 of 456, leaving room for the next launch), if that
 // S is at least 8; else the wide shape with the largest S <= 8 whose blocks
-// take at most 27/32 of its slots (512 of 608); S = 0 when even S = 2 does
-// not fit (large batches: ticket merge).
-struct ClusterPlan {
-  int splits;
-  Shape shape;
-};
+// take at most 27/32 of its slots (512 of 608); else (large batches) the
+// ticket merge over page ranges.
+pkv_plan plan_decode(const pkv_device_figures& d, int batch, int num_splits) {
+  const int max_pages = d.max_seq_len / kPage;
+  const long long narrow = static_cast<long long>(d.narrow_blocks_per_sm) * d.num_sms;
+  const long long wide = static_cast<long long>(d.wide_blocks_per_sm) * d.num_sms;
+  pkv_plan p = {};
+  p.shape = kTicketShape;
+  if (num_splits == 0) {
+    auto usable = [&](int s) {
+      return s <= d.max_cluster && s <= d.max_splits && s <= max_pages;
+    };
+    for (int s = kMaxClusterSize; s >= 8 && !p.cluster; s /= 2) {
+      if (usable(s) && 16 * static_cast<long long>(batch) * kHkv * s <= 9 * narrow) {
+        p.cluster = s;
+        p.shape = kNarrowShape;
+      }
+    }
+    for (int s = 8; s >= 2 && !p.cluster; s /= 2) {
+      if (usable(s) && 32 * static_cast<long long>(batch) * kHkv * s <= 27 * wide) {
+        p.cluster = s;
+        p.shape = kWideShape;
+      }
+    }
+    if (p.cluster) {
+      p.num_splits = p.cluster;
+    } else {
+      p.chunk_pages = auto_chunk_pages(d, batch);
+    }
+  } else {
+    p.num_splits = num_splits;
+    if (num_splits >= 2 && num_splits <= d.max_cluster) {
+      // a chosen split count takes the narrow shape while its blocks fit one
+      // wave of it, the wide shape beyond
+      p.cluster = num_splits;
+      p.shape = static_cast<long long>(batch) * kHkv * num_splits <= narrow ? kNarrowShape
+                                                                           : kWideShape;
+    }
+  }
+  p.grid_splits = p.num_splits > 0 ? p.num_splits
+                                   : (max_pages + p.chunk_pages - 1) / p.chunk_pages;
+  const long long blocks = static_cast<long long>(p.grid_splits) * kHkv * batch;
+  const int per_sm = p.shape == kNarrowShape  ? d.narrow_blocks_per_sm
+                     : p.shape == kWideShape ? d.wide_blocks_per_sm
+                                             : d.ticket_blocks_per_sm;
+  const long long resident = static_cast<long long>(per_sm) * d.num_sms;
+  p.early_trigger = blocks <= resident ? 1 : 0;
+  // more than one wave of ticket-mode blocks: longest sequences first
+  p.longest_first = (!p.cluster && num_splits == 0 && blocks > resident) ? 1 : 0;
+  return p;
+}
 
-ClusterPlan auto_cluster_plan(const pkv_pool* pool, int batch) {
-  const int max_pages = pool->cfg.max_seq_len / kPage;
-  const long long narrow = static_cast<long long>(pool->cluster_blocks_per_sm) * pool->num_sms;
-  const long long wide = static_cast<long long>(pool->wide_blocks_per_sm) * pool->num_sms;
-  auto usable = [&](int s) {
-    return s <= pool->max_cluster && s <= pool->cfg.max_splits && s <= max_pages;
-  };
-  for (int s = kMaxClusterSize; s >= 8; s /= 2) {
-    if (usable(s) && 16 * static_cast<long long>(batch) * kHkv * s <= 9 * narrow)
-      return {s, kNarrowShape};
-  }
-  for (int s = 8; s >= 2; s /= 2) {
-    if (usable(s) && 32 * static_cast<long long>(batch) * kHkv * s <= 27 * wide)
-      return {s, kWideShape};
-  }
-  return {0, kTicketShape};
+pkv_device_figures figures_of(const pkv_pool* pool) {
+  pkv_device_figures d;
+  d.num_sms = pool->num_sms;
+  d.ticket_blocks_per_sm = pool->blocks_per_sm;
+  d.narrow_blocks_per_sm = pool->cluster_blocks_per_sm;
+  d.wide_blocks_per_sm = pool->wide_blocks_per_sm;
+  d.max_cluster = pool->max_cluster;
+  d.max_splits = pool->cfg.max_splits;
+  d.max_seq_len = pool->cfg.max_seq_len;
+  return d;
 }
 
 // Cluster size of the multi-layer launch: the largest S of 16, 8, 4, 2 (within
@@ -1531,43 +1574,14 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   // Plan: S splits per sequence merged in a cluster when 2 <= S <= the
   // largest cluster this device schedules; otherwise (S = 1, S larger, or a
   // batch too large for one wave of clusters) global partials and a ticket.
-  int cluster = 0;
-  Shape shape = kTicketShape;
-  if (num_splits == 0) {
-    const ClusterPlan plan = auto_cluster_plan(pool, batch);
-    cluster = plan.splits;
-    shape = plan.shape;
-    if (cluster >= 2) {
-      prm.num_splits = cluster;
-      prm.chunk_pages = 0;
-    } else {
-      cluster = 0;
-      prm.num_splits = 0;
-      prm.chunk_pages = auto_chunk_pages(pool, batch);
-    }
-  } else {
-    prm.num_splits = num_splits;
-    prm.chunk_pages = 0;
-    if (num_splits >= 2 && num_splits <= pool->max_cluster) {
-      // a chosen split count takes the narrow shape while its blocks fit one
-      // wave of it, the wide shape beyond
-      cluster = num_splits;
-      shape = static_cast<long long>(batch) * kHkv * num_splits <=
-                      static_cast<long long>(pool->cluster_blocks_per_sm) * pool->num_sms
-                  ? kNarrowShape
-                  : kWideShape;
-    }
-  }
-  const int grid_splits = prm.num_splits > 0 ? prm.num_splits
-                                             : (max_pages + prm.chunk_pages - 1) / prm.chunk_pages;
-  const long long blocks = static_cast<long long>(grid_splits) * kHkv * batch;
-  const int per_sm = shape == kNarrowShape  ? pool->cluster_blocks_per_sm
-                     : shape == kWideShape ? pool->wide_blocks_per_sm
-                                           : pool->blocks_per_sm;
-  const long long resident = static_cast<long long>(per_sm) * pool->num_sms;
-  prm.early_trigger = blocks <= resident ? 1 : 0;
-  // more than one wave of ticket-mode blocks: longest sequences first
-  prm.longest_first = (!cluster && num_splits == 0 && blocks > resident) ? 1 : 0;
+  const pkv_plan plan = plan_decode(figures_of(pool), batch, num_splits);
+  const Shape shape = static_cast<Shape>(plan.shape);
+  const int cluster = plan.cluster;
+  const int grid_splits = plan.grid_splits;
+  prm.num_splits = plan.num_splits;
+  prm.chunk_pages = plan.chunk_pages;
+  prm.early_trigger = plan.early_trigger;
+  prm.longest_first = plan.longest_first;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid_splits, kHkv, batch);
@@ -1713,6 +1727,26 @@ const char* pkv_status_string(pkv_status status) {
     case PKV_ERR_STATIC_LIMIT: return "request exceeds the no-allocation entry point's scratch";
   }
   return "unknown status";
+}
+
+pkv_status pkv_plan_decode(const pkv_device_figures* dev, int batch, int num_splits,
+                           pkv_plan* out) {
+  if (!dev || !out) return PKV_ERR_INVALID_ARG;
+  const pkv_device_figures& d = *dev;
+  if (d.num_sms < 1 || d.ticket_blocks_per_sm < 1 || d.narrow_blocks_per_sm < 1 ||
+      d.wide_blocks_per_sm < 1 || d.max_cluster < 0 || d.max_cluster > kMaxClusterSize ||
+      d.max_splits < 1 || d.max_splits > kMaxSplitsLimit || d.max_seq_len < kPage ||
+      d.max_seq_len > kMaxSeqLen || d.max_seq_len % kPage != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (batch < 1 || num_splits < 0 || num_splits > d.max_splits) return PKV_ERR_INVALID_ARG;
+  *out = plan_decode(d, batch, num_splits);
+  return PKV_OK;
+}
+
+pkv_status pkv_pool_device_figures(pkv_pool_t pool, pkv_device_figures* out) {
+  if (!pool || !out) return PKV_ERR_INVALID_ARG;
+  *out = figures_of(pool);
+  return PKV_OK;
 }
 
 pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out) {

@@ -1,0 +1,109 @@
+"""The decode launch planner (pkv_plan_decode), host arithmetic behind every
+decode launch, checked on the CPU: the plans measured best on GB300 for each
+batch, the limits every plan keeps, and argument checks."""
+
+import pytest
+
+import paged_kv_cache_210_gb300 as pkv
+from paged_kv_cache_210_gb300 import build as lib_build
+
+T, N, WD = pkv.PKV_SHAPE_TICKET, pkv.PKV_SHAPE_NARROW, pkv.PKV_SHAPE_WIDE
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return pkv.load()
+
+
+def gb300(**kw):
+    """A GB300's figures with a default handle: 152 SMs, 4 ticket / 3 narrow /
+    4 wide blocks per SM, 16-block clusters, 64 splits, 2048 tokens."""
+    f = dict(num_sms=152, ticket_blocks_per_sm=4, narrow_blocks_per_sm=3, wide_blocks_per_sm=4,
+             max_cluster=16, max_splits=64, max_seq_len=2048)
+    f.update(kw)
+    return pkv.DeviceFigures(**f)
+
+
+def plan(lib, batch, num_splits=0, **kw):
+    return pkv.pkv_plan_decode(gb300(**kw), batch, num_splits, lib=lib)
+
+
+@pytest.mark.parametrize("batch,shape,splits", [
+    (1, N, 16), (2, N, 16), (3, N, 8), (4, N, 8),
+    (5, WD, 8), (8, WD, 8), (9, WD, 4), (16, WD, 4), (17, WD, 2), (32, WD, 2),
+])
+def test_cluster_plans_by_batch(lib, batch, shape, splits):
+    p = plan(lib, batch)
+    assert (p.shape, p.cluster, p.num_splits, p.chunk_pages) == (shape, splits, splits, 0)
+    assert p.grid_splits == splits and p.longest_first == 0 and p.early_trigger == 1
+
+
+@pytest.mark.parametrize("batch,chunk", [(33, 16), (64, 32), (100, 32), (128, 64), (256, 128),
+                                         (1000, 128)])
+def test_ticket_plans_by_batch(lib, batch, chunk):
+    p = plan(lib, batch)
+    assert (p.shape, p.cluster, p.num_splits, p.chunk_pages) == (T, 0, 0, chunk)
+    assert p.grid_splits == 128 // chunk
+    blocks = batch * 8 * p.grid_splits
+    # at least three blocks per resident ticket slot, so several waves
+    assert blocks >= 3 * 4 * 152
+    assert p.longest_first == 1 and p.early_trigger == 0
+
+
+def test_every_library_plan_keeps_its_limits(lib):
+    for sms in (20, 76, 132, 152):
+        for max_cluster in (0, 2, 8, 16):
+            for max_splits in (1, 4, 16, 64, 128):
+                for batch in list(range(1, 70)) + [100, 255, 256, 1000, 4096]:
+                    p = plan(lib, batch, num_sms=sms, max_cluster=max_cluster,
+                             max_splits=max_splits)
+                    if p.cluster:
+                        s = p.cluster
+                        assert p.shape in (N, WD) and s in (2, 4, 8, 16)
+                        assert s <= max_cluster and s <= max_splits
+                        per_sm = 3 if p.shape == N else 4
+                        # the whole launch is one wave of its shape's blocks
+                        assert batch * 8 * s <= per_sm * sms
+                        assert p.early_trigger == 1 and p.longest_first == 0
+                    else:
+                        assert p.shape == T and p.num_splits == 0
+                        c = p.chunk_pages
+                        assert c in (16, 32, 64, 128) or c == -(-128 // max_splits)
+                        assert p.grid_splits == -(-128 // c) <= max_splits
+                        waves = batch * 8 * p.grid_splits > 4 * sms
+                        assert p.longest_first == int(waves) and p.early_trigger == int(not waves)
+
+
+def test_chosen_split_counts(lib):
+    p = plan(lib, 2, num_splits=4)
+    assert (p.shape, p.cluster, p.grid_splits) == (N, 4, 4)
+    p = plan(lib, 4, num_splits=16)          # 512 blocks: more than one narrow wave
+    assert (p.shape, p.cluster) == (WD, 16)
+    p = plan(lib, 2, num_splits=3)           # any size up to the cluster limit
+    assert (p.shape, p.cluster, p.grid_splits) == (N, 3, 3)
+    p = plan(lib, 2, num_splits=32)          # beyond the cluster limit: ticket
+    assert (p.shape, p.cluster, p.num_splits, p.grid_splits) == (T, 0, 32, 32)
+    p = plan(lib, 300, num_splits=1)
+    assert (p.shape, p.cluster, p.num_splits, p.grid_splits, p.longest_first) == (T, 0, 1, 1, 0)
+    p = plan(lib, 2, num_splits=8, max_cluster=0)   # no clusters on the device
+    assert (p.shape, p.cluster) == (T, 0)
+
+
+def test_shorter_context_caps_ranges(lib):
+    p = plan(lib, 2, max_seq_len=64)          # 4 pages: S = 16 or 8 would leave empty blocks
+    assert p.cluster <= 4 and p.grid_splits == p.cluster
+    p = plan(lib, 1000, max_seq_len=256)      # 16 pages: one range of all of them
+    assert (p.shape, p.chunk_pages, p.grid_splits) == (T, 16, 1)
+
+
+def test_invalid_arguments(lib):
+    bad = [dict(num_sms=0), dict(ticket_blocks_per_sm=0), dict(wide_blocks_per_sm=0),
+           dict(max_cluster=17), dict(max_cluster=-1), dict(max_splits=0),
+           dict(max_splits=129), dict(max_seq_len=100), dict(max_seq_len=4096)]
+    for kw in bad:
+        with pytest.raises(pkv.PkvError):
+            plan(lib, 2, **kw)
+    for batch, splits in ((0, 0), (-1, 0), (2, -1), (2, 65)):
+        with pytest.raises(pkv.PkvError):
+            plan(lib, batch, splits)
