@@ -225,3 +225,20 @@ def test_layer_wait_timeout_is_flagged_and_the_context_stays_usable():
     ref, ok, ov = oracle_step(wl, st.host_k, st.host_v, *_host_inputs(st))
     assert np.array_equal(bits(st.k_pool), ok) and np.array_equal(bits(st.v_pool), ov)
     assert_close(st.out.cpu().numpy(), ref, "after a timeout")
+
+
+def test_pool_device_figures_and_plan():
+    """The handle's device figures (occupancy of the three decode shapes,
+    cluster limit) feed the same planner the CPU tests check."""
+    wl = W.tiny(False)
+    pool = pkv.pkv_pool_create(1, wl.num_pages, 4, max_splits=32)
+    f = pkv.pkv_pool_device_figures(pool)
+    assert f.num_sms == torch.cuda.get_device_properties(0).multi_processor_count
+    assert min(f.ticket_blocks_per_sm, f.narrow_blocks_per_sm, f.wide_blocks_per_sm) >= 1
+    assert f.narrow_blocks_per_sm <= f.wide_blocks_per_sm
+    assert f.max_cluster in (0, 2, 4, 8, 16)
+    assert (f.max_splits, f.max_seq_len) == (32, 2048)
+    p = pkv.pkv_plan_decode(f, 2)
+    if f.max_cluster >= 2:
+        assert p.cluster >= 2 and p.shape in (pkv.PKV_SHAPE_NARROW, pkv.PKV_SHAPE_WIDE)
+    pool.close()
