@@ -85,7 +85,10 @@ def measured_peaks():
 
 
 KERNEL_SOURCES = {
-    "decode": ("paged_kv_cache_210_gb300/csrc/pkv.cu",),
+    "decode": ("paged_kv_cache_210_gb300/csrc/pkv.cu",
+               "paged_kv_cache_210_gb300/csrc/decode_device.cuh"),
+    "layers": ("paged_kv_cache_210_gb300/csrc/layers.cu",
+               "paged_kv_cache_210_gb300/csrc/decode_device.cuh"),
     "prefill": ("paged_kv_cache_210_gb300/csrc/prefill.cu", "include/pkv_prefill.h"),
 }
 
@@ -468,7 +471,7 @@ def run_ours(args, world, rank, local):
     achieved = (nbytes / launches) / (per_launch_ms * 1e-3) / 1e9
     if args.persistent:
         kernel_name = "decode_layers_kernel"
-        traffic = recorded_traffic("decode_layers_" + args.workload)
+        traffic = recorded_traffic("decode_layers_" + args.workload, "layers")
         step_note = ("16 layers of fused append+attend in one persistent launch (per-sequence "
                      "layer order kept by device-side waits), CUDA graph")
     else:

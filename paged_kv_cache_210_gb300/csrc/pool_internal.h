@@ -4,6 +4,7 @@
 #define PKV_POOL_INTERNAL_H
 
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 #include "pkv.h"
 
@@ -31,5 +32,16 @@ enum : int {
   PKV_DEV_ERR_SEQ_LEN = 4,    // a length outside [1, max_seq_len]
   PKV_DEV_ERR_TIMEOUT = 8,    // a bounded wait gave up
 };
+
+// Host helpers of the entry points.
+inline bool pkv_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline pkv_status pkv_check_launch() {
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// layers.cu: the multi-layer kernel's attributes and, per cluster size, how
+// many of its clusters the device holds at once (pool->layer_clusters).
+bool pkv_layers_setup(pkv_pool* pool);
 
 #endif  // PKV_POOL_INTERNAL_H

@@ -674,7 +674,6 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
 }
 
 // ---------------------------------------------------------------- host
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::once_flag once;
@@ -726,8 +725,8 @@ pkv_status check_common(pkv_pool_t pool, int layer, int batch, int max_chunk_tok
     return PKV_ERR_INVALID_ARG;
   if (batch == 0) return PKV_OK;
   if (max_chunk_tokens < 1 || max_chunk_tokens > c.max_seq_len) return PKV_ERR_INVALID_ARG;
-  if (!block_tables || !cu_tokens || !start_pos || !aligned16(block_tables) ||
-      !aligned16(cu_tokens) || !aligned16(start_pos))
+  if (!block_tables || !cu_tokens || !start_pos || !pkv_aligned16(block_tables) ||
+      !pkv_aligned16(cu_tokens) || !pkv_aligned16(start_pos))
     return PKV_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_ERR_INVALID_ARG;
@@ -743,8 +742,8 @@ pkv_status launch_fill(pkv_pool_t pool, int layer, const void* k, const void* v,
   if (st != PKV_OK || batch == 0) return st;
   if (total_tokens < 0) return PKV_ERR_INVALID_ARG;
   if (total_tokens == 0) return PKV_OK;
-  if (!k || !v || !k_pool || !v_pool || !aligned16(k) || !aligned16(v) || !aligned16(k_pool) ||
-      !aligned16(v_pool))
+  if (!k || !v || !k_pool || !v_pool || !pkv_aligned16(k) || !pkv_aligned16(v) || !pkv_aligned16(k_pool) ||
+      !pkv_aligned16(v_pool))
     return PKV_ERR_INVALID_ARG;
   const pkv_pool_config& c = pool->cfg;
   const int stride = c.max_seq_len / kPage;
@@ -766,8 +765,8 @@ pkv_status launch_attention(pkv_pool_t pool, int layer, const void* q, const voi
   if (st != PKV_OK || batch == 0) return st;
   if (total_tokens < 0) return PKV_ERR_INVALID_ARG;
   if (total_tokens == 0) return PKV_OK;
-  if (!q || !k_pool || !v_pool || !out || !aligned16(q) || !aligned16(k_pool) ||
-      !aligned16(v_pool) || !aligned16(out))
+  if (!q || !k_pool || !v_pool || !out || !pkv_aligned16(q) || !pkv_aligned16(k_pool) ||
+      !pkv_aligned16(v_pool) || !pkv_aligned16(out))
     return PKV_ERR_INVALID_ARG;
   const pkv_pool_config& c = pool->cfg;
   if (!set_smem_attribute(pool->device)) return PKV_ERR_CUDA;
