@@ -42,7 +42,8 @@ struct LayersParams {
   const uint16_t* v_new;
   uint16_t* k_pool;           // [num_pages][8][16][64]
   uint16_t* v_pool;
-  const int32_t* tables;      // block tables from the launch's first layer: [.][max_batch][table_stride]
+  const int32_t* tables;      // block tables from the launch's first layer on:
+                              // [layer][max_batch][table_stride]
   const int32_t* seq_lens;    // [batch], the same for every layer
   float* out;                 // [num_layers][batch][32][64]
   int* seq_done;              // [batch]: layer completions of the sequence's blocks (zero at launch)
@@ -318,7 +319,8 @@ pkv_status launch_layers(pkv_pool_t pool, int layer_begin, int num_layers, const
   if (!q || !k || !v || !k_pool || !v_pool || !block_tables || !seq_lens || !out)
     return PKV_ERR_INVALID_ARG;
   if (!pkv_aligned16(q) || !pkv_aligned16(k) || !pkv_aligned16(v) || !pkv_aligned16(k_pool) ||
-      !pkv_aligned16(v_pool) || !pkv_aligned16(block_tables) || !pkv_aligned16(seq_lens) || !pkv_aligned16(out))
+      !pkv_aligned16(v_pool) || !pkv_aligned16(block_tables) || !pkv_aligned16(seq_lens) ||
+      !pkv_aligned16(out))
     return PKV_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_ERR_INVALID_ARG;

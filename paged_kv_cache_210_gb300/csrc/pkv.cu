@@ -532,8 +532,8 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   if (batch == 0) return PKV_OK;
   if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PKV_ERR_INVALID_ARG;
   if (kFused && (!k || !v)) return PKV_ERR_INVALID_ARG;
-  if (!pkv_aligned16(q) || !pkv_aligned16(k_pool) || !pkv_aligned16(v_pool) || !pkv_aligned16(block_tables) ||
-      !pkv_aligned16(seq_lens) || !pkv_aligned16(out))
+  if (!pkv_aligned16(q) || !pkv_aligned16(k_pool) || !pkv_aligned16(v_pool) ||
+      !pkv_aligned16(block_tables) || !pkv_aligned16(seq_lens) || !pkv_aligned16(out))
     return PKV_ERR_INVALID_ARG;
   if (kFused && (!pkv_aligned16(k) || !pkv_aligned16(v))) return PKV_ERR_INVALID_ARG;
   if (rope && (!rope_cos || !rope_sin || !pkv_aligned16(rope_cos) || !pkv_aligned16(rope_sin)))
@@ -665,8 +665,8 @@ pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_
     return PKV_ERR_STATIC_LIMIT;
   if (batch == 0) return PKV_OK;
   if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PKV_ERR_INVALID_ARG;
-  if (!pkv_aligned16(q) || !pkv_aligned16(k_pool) || !pkv_aligned16(v_pool) || !pkv_aligned16(block_tables) ||
-      !pkv_aligned16(seq_lens) || !pkv_aligned16(out) ||
+  if (!pkv_aligned16(q) || !pkv_aligned16(k_pool) || !pkv_aligned16(v_pool) ||
+      !pkv_aligned16(block_tables) || !pkv_aligned16(seq_lens) || !pkv_aligned16(out) ||
       (reinterpret_cast<uintptr_t>(error_bits) & 3u) != 0)
     return PKV_ERR_INVALID_ARG;
 

@@ -742,8 +742,8 @@ pkv_status launch_fill(pkv_pool_t pool, int layer, const void* k, const void* v,
   if (st != PKV_OK || batch == 0) return st;
   if (total_tokens < 0) return PKV_ERR_INVALID_ARG;
   if (total_tokens == 0) return PKV_OK;
-  if (!k || !v || !k_pool || !v_pool || !pkv_aligned16(k) || !pkv_aligned16(v) || !pkv_aligned16(k_pool) ||
-      !pkv_aligned16(v_pool))
+  if (!k || !v || !k_pool || !v_pool || !pkv_aligned16(k) || !pkv_aligned16(v) ||
+      !pkv_aligned16(k_pool) || !pkv_aligned16(v_pool))
     return PKV_ERR_INVALID_ARG;
   const pkv_pool_config& c = pool->cfg;
   const int stride = c.max_seq_len / kPage;
