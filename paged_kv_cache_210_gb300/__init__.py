@@ -134,13 +134,36 @@ def load(path: str = None):
     return lib
 
 
-def _addr(x):
-    """Device address of a tensor (or an int address, or None)."""
+def _addr(x, dtype=None, what="tensor"):
+    """Address of a tensor (or an int address, or None). A tensor must be
+    contiguous and, when `dtype` is given ("bfloat16", "float32", "int32"),
+    of that dtype: the library reads raw memory in the layouts include/*.h
+    documents."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if not x.is_contiguous():
+        raise ValueError(f"{what}: the library takes contiguous tensors")
+    if dtype is not None and str(x.dtype) != "torch." + dtype:
+        raise ValueError(f"{what}: expected {dtype}, got {x.dtype}")
     return x.data_ptr()
+
+
+def _i32(x, what):
+    return _addr(x, "int32", what)
+
+
+# the dtype of each tensor argument of the CUDA entry points, by parameter name
+_DTYPES = {"q": "bfloat16", "k": "bfloat16", "v": "bfloat16", "k_pool": "bfloat16",
+           "v_pool": "bfloat16", "block_tables": "int32", "positions": "int32",
+           "seq_lens": "int32", "cu_tokens": "int32", "start_pos": "int32", "out": "float32",
+           "rope_cos": "float32", "rope_sin": "float32"}
+
+
+def _ptrs(**tensors):
+    """Checked addresses of the named tensor arguments, in the order given."""
+    return [_addr(t, _DTYPES[name], name) for name, t in tensors.items()]
 
 
 def _stream(stream):
@@ -198,29 +221,33 @@ def _batch(x, batch):
 def pkv_append(pool: Pool, layer, k, v, k_pool, v_pool, block_tables, positions, batch=None,
                stream=None):
     """k, v: bf16 [B][8][64]; pools bf16 [P][8][16][64]; tables int32 [L][max_batch][pages]."""
-    st = pool._lib.pkv_append(pool.handle, int(layer), _addr(k), _addr(v), _addr(k_pool),
-                              _addr(v_pool), _addr(block_tables), _addr(positions),
-                              _batch(positions, batch), _stream(stream))
+    st = pool._lib.pkv_append(
+        pool.handle, int(layer),
+        *_ptrs(k=k, v=v, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables,
+               positions=positions),
+        _batch(positions, batch), _stream(stream))
     _check(st, "pkv_append")
 
 
 def pkv_decode_attention(pool: Pool, layer, q, k_pool, v_pool, block_tables, seq_lens, out,
                          batch=None, num_splits=0, stream=None):
     """q: bf16 [B][32][64]; out: fp32 [B][32][64]; seq_lens: int32 [B] (after the append)."""
-    st = pool._lib.pkv_decode_attention(pool.handle, int(layer), _addr(q), _addr(k_pool),
-                                        _addr(v_pool), _addr(block_tables), _addr(seq_lens),
-                                        _addr(out), _batch(seq_lens, batch), int(num_splits),
-                                        _stream(stream))
+    st = pool._lib.pkv_decode_attention(
+        pool.handle, int(layer),
+        *_ptrs(q=q, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables, seq_lens=seq_lens,
+               out=out),
+        _batch(seq_lens, batch), int(num_splits), _stream(stream))
     _check(st, "pkv_decode_attention")
 
 
 def pkv_append_attend(pool: Pool, layer, q, k, v, k_pool, v_pool, block_tables, seq_lens, out,
                       batch=None, num_splits=0, stream=None):
     """Fused append (at seq_lens - 1) and decode attention for one layer."""
-    st = pool._lib.pkv_append_attend(pool.handle, int(layer), _addr(q), _addr(k), _addr(v),
-                                     _addr(k_pool), _addr(v_pool), _addr(block_tables),
-                                     _addr(seq_lens), _addr(out), _batch(seq_lens, batch),
-                                     int(num_splits), _stream(stream))
+    st = pool._lib.pkv_append_attend(
+        pool.handle, int(layer),
+        *_ptrs(q=q, k=k, v=v, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables,
+               seq_lens=seq_lens, out=out),
+        _batch(seq_lens, batch), int(num_splits), _stream(stream))
     _check(st, "pkv_append_attend")
 
 
@@ -228,32 +255,33 @@ def pkv_append_rope(pool: Pool, layer, k, v, k_pool, v_pool, block_tables, posit
                     rope_cos, rope_sin, batch=None, stream=None):
     """pkv_append with each key rotated to its position; rope_cos/rope_sin:
     fp32 [max_seq_len][32] on the device."""
-    st = pool._lib.pkv_append_rope(pool.handle, int(layer), _addr(k), _addr(v), _addr(k_pool),
-                                   _addr(v_pool), _addr(block_tables), _addr(positions),
-                                   _addr(rope_cos), _addr(rope_sin), _batch(positions, batch),
-                                   _stream(stream))
+    st = pool._lib.pkv_append_rope(
+        pool.handle, int(layer),
+        *_ptrs(k=k, v=v, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables,
+               positions=positions, rope_cos=rope_cos, rope_sin=rope_sin),
+        _batch(positions, batch), _stream(stream))
     _check(st, "pkv_append_rope")
 
 
 def pkv_decode_attention_rope(pool: Pool, layer, q, k_pool, v_pool, block_tables, seq_lens,
                               rope_cos, rope_sin, out, batch=None, num_splits=0, stream=None):
     """pkv_decode_attention with each query rotated to position seq_lens - 1."""
-    st = pool._lib.pkv_decode_attention_rope(pool.handle, int(layer), _addr(q), _addr(k_pool),
-                                             _addr(v_pool), _addr(block_tables),
-                                             _addr(seq_lens), _addr(rope_cos), _addr(rope_sin),
-                                             _addr(out), _batch(seq_lens, batch),
-                                             int(num_splits), _stream(stream))
+    st = pool._lib.pkv_decode_attention_rope(
+        pool.handle, int(layer),
+        *_ptrs(q=q, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables, seq_lens=seq_lens,
+               rope_cos=rope_cos, rope_sin=rope_sin, out=out),
+        _batch(seq_lens, batch), int(num_splits), _stream(stream))
     _check(st, "pkv_decode_attention_rope")
 
 
 def pkv_append_attend_rope(pool: Pool, layer, q, k, v, k_pool, v_pool, block_tables, seq_lens,
                            rope_cos, rope_sin, out, batch=None, num_splits=0, stream=None):
     """pkv_append_attend with the key and the queries rotated to seq_lens - 1."""
-    st = pool._lib.pkv_append_attend_rope(pool.handle, int(layer), _addr(q), _addr(k), _addr(v),
-                                          _addr(k_pool), _addr(v_pool), _addr(block_tables),
-                                          _addr(seq_lens), _addr(rope_cos), _addr(rope_sin),
-                                          _addr(out), _batch(seq_lens, batch),
-                                          int(num_splits), _stream(stream))
+    st = pool._lib.pkv_append_attend_rope(
+        pool.handle, int(layer),
+        *_ptrs(q=q, k=k, v=v, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables,
+               seq_lens=seq_lens, rope_cos=rope_cos, rope_sin=rope_sin, out=out),
+        _batch(seq_lens, batch), int(num_splits), _stream(stream))
     _check(st, "pkv_append_attend_rope")
 
 
@@ -264,10 +292,11 @@ def pkv_append_attend_layers(pool: Pool, layer_begin, q, k, v, k_pool, v_pool, b
     k, v: bf16 [J][B][8][64]; out: fp32 [J][B][32][64]; J = num_layers
     (default: q's first dimension)."""
     J = int(q.shape[0]) if num_layers is None else int(num_layers)
-    st = pool._lib.pkv_append_attend_layers(pool.handle, int(layer_begin), J, _addr(q), _addr(k),
-                                            _addr(v), _addr(k_pool), _addr(v_pool),
-                                            _addr(block_tables), _addr(seq_lens), _addr(out),
-                                            _batch(seq_lens, batch), _stream(stream))
+    st = pool._lib.pkv_append_attend_layers(
+        pool.handle, int(layer_begin), J,
+        *_ptrs(q=q, k=k, v=v, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables,
+               seq_lens=seq_lens, out=out),
+        _batch(seq_lens, batch), _stream(stream))
     _check(st, "pkv_append_attend_layers")
 
 
@@ -277,11 +306,11 @@ def pkv_test_layers_wait_timeout(pool: Pool, layer_begin, q, k, v, k_pool, v_poo
     """Failure-detection test hook: pkv_append_attend_layers with every
     between-layer wait unreachable; the device flags a timeout."""
     J = int(q.shape[0]) if num_layers is None else int(num_layers)
-    st = pool._lib.pkv_test_layers_wait_timeout(pool.handle, int(layer_begin), J, _addr(q),
-                                                _addr(k), _addr(v), _addr(k_pool),
-                                                _addr(v_pool), _addr(block_tables),
-                                                _addr(seq_lens), _addr(out),
-                                                _batch(seq_lens, batch), _stream(stream))
+    st = pool._lib.pkv_test_layers_wait_timeout(
+        pool.handle, int(layer_begin), J,
+        *_ptrs(q=q, k=k, v=v, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables,
+               seq_lens=seq_lens, out=out),
+        _batch(seq_lens, batch), _stream(stream))
     _check(st, "pkv_test_layers_wait_timeout")
 
 
@@ -314,11 +343,13 @@ def pkv_decode_attention_noalloc(layer, q, k_pool, v_pool, block_tables, seq_len
     pool handle, scratch in the library's own static device array (limits and
     the one-time set-up on first use are described in include/pkv.h)."""
     lib = lib or load()
-    st = lib.pkv_decode_attention_noalloc(int(layer), _addr(q), _addr(k_pool), _addr(v_pool),
-                                          _addr(block_tables), _addr(seq_lens), _addr(out),
-                                          int(num_layers), int(num_pages), int(max_batch),
-                                          int(max_seq_len), _batch(seq_lens, batch),
-                                          int(num_splits), _addr(error_bits), _stream(stream))
+    st = lib.pkv_decode_attention_noalloc(
+        int(layer),
+        *_ptrs(q=q, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables, seq_lens=seq_lens,
+               out=out),
+        int(num_layers), int(num_pages), int(max_batch), int(max_seq_len),
+        _batch(seq_lens, batch), int(num_splits), _i32(error_bits, "error_bits"),
+        _stream(stream))
     _check(st, "pkv_decode_attention_noalloc")
 
 
@@ -328,10 +359,11 @@ def pkv_prefill_fill(pool: Pool, layer, k, v, k_pool, v_pool, block_tables, cu_t
     """Writes chunk tokens' K/V (bf16 [T][8][64]) into their pages."""
     batch = int(start_pos.shape[0]) if batch is None else int(batch)
     total = int(k.shape[0]) if total_tokens is None else int(total_tokens)
-    st = pool._lib.pkv_prefill_fill(pool.handle, int(layer), _addr(k), _addr(v), _addr(k_pool),
-                                    _addr(v_pool), _addr(block_tables), _addr(cu_tokens),
-                                    _addr(start_pos), batch, total, int(max_chunk_tokens),
-                                    _stream(stream))
+    st = pool._lib.pkv_prefill_fill(
+        pool.handle, int(layer),
+        *_ptrs(k=k, v=v, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables,
+               cu_tokens=cu_tokens, start_pos=start_pos),
+        batch, total, int(max_chunk_tokens), _stream(stream))
     _check(st, "pkv_prefill_fill")
 
 
@@ -340,10 +372,11 @@ def pkv_prefill_attention(pool: Pool, layer, q, k_pool, v_pool, block_tables, cu
     """Causal attention of chunk tokens (q bf16 [T][32][64]) over the pages; out fp32."""
     batch = int(start_pos.shape[0]) if batch is None else int(batch)
     total = int(q.shape[0]) if total_tokens is None else int(total_tokens)
-    st = pool._lib.pkv_prefill_attention(pool.handle, int(layer), _addr(q), _addr(k_pool),
-                                         _addr(v_pool), _addr(block_tables), _addr(cu_tokens),
-                                         _addr(start_pos), _addr(out), batch, total,
-                                         int(max_chunk_tokens), _stream(stream))
+    st = pool._lib.pkv_prefill_attention(
+        pool.handle, int(layer),
+        *_ptrs(q=q, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables,
+               cu_tokens=cu_tokens, start_pos=start_pos, out=out),
+        batch, total, int(max_chunk_tokens), _stream(stream))
     _check(st, "pkv_prefill_attention")
 
 
@@ -352,10 +385,11 @@ def pkv_prefill(pool: Pool, layer, q, k, v, k_pool, v_pool, block_tables, cu_tok
     """pkv_prefill_fill then pkv_prefill_attention."""
     batch = int(start_pos.shape[0]) if batch is None else int(batch)
     total = int(q.shape[0]) if total_tokens is None else int(total_tokens)
-    st = pool._lib.pkv_prefill(pool.handle, int(layer), _addr(q), _addr(k), _addr(v),
-                               _addr(k_pool), _addr(v_pool), _addr(block_tables),
-                               _addr(cu_tokens), _addr(start_pos), _addr(out), batch, total,
-                               int(max_chunk_tokens), _stream(stream))
+    st = pool._lib.pkv_prefill(
+        pool.handle, int(layer),
+        *_ptrs(q=q, k=k, v=v, k_pool=k_pool, v_pool=v_pool, block_tables=block_tables,
+               cu_tokens=cu_tokens, start_pos=start_pos, out=out),
+        batch, total, int(max_chunk_tokens), _stream(stream))
     _check(st, "pkv_prefill")
 
 
