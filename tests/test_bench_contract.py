@@ -36,3 +36,17 @@ def test_reference_arm_line():
 def test_rejects_rope_with_the_multi_layer_launch():
     r = _run("--persistent", "--rope", "--steps", "1", "--warmup", "3")
     assert r.returncode != 0 and "--persistent" in r.stderr
+
+
+def test_algorithmic_bytes():
+    """Per (sequence, layer): seq_len x 2048 (every K/V row read once, the new
+    one included) + 2048 (the new row written) + 4096 (q) + 8192 (FP32 out),
+    + 256 with rotary tables (two 32-float angle rows)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    wl = W.llama_default()
+    assert bench.step_bytes(wl) == 16 * 2 * (2048 * 2048 + 2048 + 4096 + 8192) == 134_676_480
+    assert bench.step_bytes(wl, rope=True) == 134_676_480 + 16 * 2 * 256
+    wl = W.custom([1, 17, 2048], num_layers=3)
+    assert bench.step_bytes(wl) == 3 * sum(n * 2048 + 14336 for n in (1, 17, 2048))
