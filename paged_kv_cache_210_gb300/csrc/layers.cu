@@ -22,9 +22,9 @@ using namespace pkv_decode;
 namespace {
 
 // ---------------------------------------------------------------- layer stack
-// Consecutive layers of the fused step in one launch: the grid of the
-// cluster kernel (S blocks of 4 warps per (sequence, kv head), merged through
-// distributed shared memory), made persistent. Each block loops over the
+// Consecutive layers of the fused step in one launch: the grid of the wide
+// cluster shape (S blocks of 4 warps per (sequence, kv head), 2 page stages
+// per warp, merged through distributed shared memory), made persistent. Each block loops over the
 // layers, and each warp's ring of page stages runs on across the layer
 // boundary: the pages of cached tokens of layer l + 1, which nothing of layer
 // l writes, are in flight while layer l's merge and the wait below run.
@@ -64,10 +64,10 @@ struct alignas(16) LayersSmem {
   int flag;                   // thread 0's wait verdict for the block
 };
 
-// Bounded wait until *ctr >= target (acquire, GPU scope): false after about
-// two seconds.
 static_assert(4 * (sizeof(LayersSmem) + 1024) <= kSmemPerSm, "4 multi-layer blocks per SM");
 
+// Bounded wait until *ctr >= target (acquire, GPU scope): false after about
+// two seconds.
 __device__ __forceinline__ bool wait_count(const int* ctr, int target) {
   auto load = [&]() {
     int v;
