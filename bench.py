@@ -807,6 +807,8 @@ def main():
     args = ap.parse_args()
     if args.persistent and args.rope:
         ap.error("--persistent runs the unrotated fused step; drop --rope")
+    if args.persistent and args.splits:
+        ap.error("--persistent plans its own clusters; drop --splits")
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.component == "scheduler":

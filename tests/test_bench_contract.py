@@ -33,9 +33,10 @@ def test_reference_arm_line():
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
 
 
-def test_rejects_rope_with_the_multi_layer_launch():
-    r = _run("--persistent", "--rope", "--steps", "1", "--warmup", "3")
-    assert r.returncode != 0 and "--persistent" in r.stderr
+def test_rejects_options_the_multi_layer_launch_does_not_take():
+    for extra in (("--rope",), ("--splits", "4")):
+        r = _run("--persistent", *extra, "--steps", "1", "--warmup", "3")
+        assert r.returncode != 0 and "--persistent" in r.stderr
 
 
 def test_algorithmic_bytes():
