@@ -352,6 +352,8 @@ FULL = {
     "ragged-b256": (W.large_ragged, [0, 1, 2, 3, 4, 5, 100, 200, 255]),
     "long-b1": (lambda: W.long_context(1), None),
     "long-b4": (lambda: W.long_context(4), None),
+    "long-b8": (lambda: W.long_context(8), None),              # wide cluster shape, S = 8
+    "long-b16": (lambda: W.long_context(16), [0, 3, 7, 8, 12, 15]),   # wide, S = 4
 }
 
 
