@@ -93,9 +93,15 @@ typedef struct {
  * tables (the _rope entry points) and the pool rows below position
  * seq_lens[b] - 1 (the unfused decode defers the page holding that
  * position). q, k, v, out and the appended slot are read or written only
- * after the wait. Contract: the kernel immediately before a decode launch in
- * the stream must not write block_tables, seq_lens, the rotary tables or
- * those pool rows. Off by default. */
+ * after the wait. A decode launch lets the next one start only after its
+ * own wait, so every kernel two or more places earlier in the stream has
+ * completed before the next launch's pre-wait reads. Contract: the kernel
+ * immediately before a decode launch in the stream must not write
+ * block_tables, seq_lens, the rotary tables or those pool rows. (In a model
+ * of two or more layers, consecutive decode steps meet it: the step before
+ * wrote the rows of the same layer one launch per layer earlier. A
+ * one-layer model's consecutive fused steps do not: put another kernel
+ * between them or leave this flag off.) Off by default. */
 #define PKV_FLAG_PDL 1
 
 typedef struct pkv_pool* pkv_pool_t;
@@ -227,6 +233,13 @@ pkv_status pkv_append_attend_rope(pkv_pool_t pool, int layer, const void* q, con
  * batch for which even S = 2 does not fit runs as one pkv_append_attend launch
  * per layer. Uses a per-sequence counter in the handle (zeroed on the stream
  * before each launch), so one handle serves one such call at a time.
+ * Residency is checked against an idle device: the launch must not overlap
+ * other work on the device (another stream's kernels holding SMs can keep
+ * some clusters from becoming resident; the blocks of a sequence then wait
+ * for blocks that cannot start, every such wait gives up after about two
+ * seconds, PKV_ERR_DEVICE_TIMEOUT is flagged and that launch's outputs carry
+ * no layer-order guarantee). A caller that shares the device with other
+ * streams uses pkv_append_attend per layer instead.
  * Errors as for pkv_append_attend; layer_begin + num_layers must not exceed
  * num_layers of the handle. num_layers == 0 or batch == 0 is a no-op. */
 pkv_status pkv_append_attend_layers(pkv_pool_t pool, int layer_begin, int num_layers,

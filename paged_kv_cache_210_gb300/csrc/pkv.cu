@@ -271,12 +271,15 @@ decode_kernel(const DecodeParams prm) {
     }
     if (line) prefetch_l2(line);
   }
+  pdl_wait();
   // A launch that fits in one wave of resident blocks lets the next launch
   // start now, so its blocks prefetch while this one computes; a larger
   // launch triggers after its page loop, so waiting blocks of the next
-  // launch do not take slots this launch's later blocks need.
+  // launch do not take slots this launch's later blocks need. Either way the
+  // trigger comes after the wait: the next launch's pre-wait reads then start
+  // only once every launch before this one has completed, so only the launch
+  // immediately before it can still be writing.
   if (prm.early_trigger) pdl_launch_dependents();
-  pdl_wait();
   // the new row's load goes out before q's, so the two latencies overlap
   const bool new_in_prologue = i_new >= 0 && i_new < n_prefetch;
   uint4 new_val = make_uint4(0u, 0u, 0u, 0u);

@@ -376,6 +376,68 @@ def pin_rope_quarter_turn_swaps_halves(orc):
     np.testing.assert_array_equal(q64[..., half:], qf[..., :half])
 
 
+def pin_rope_key_uses_its_own_position(orc):
+    """Decode appends each token at its absolute rotary position (samir-vllm:
+    Build LLM Inference From Scratch in C++ and CUDA, "Architecture
+    walkthrough", KV cache paragraph), so the key takes the angle row of its
+    own position and of no other. Tables here hold a quarter turn at each
+    sequence's position, a half turn (plain negation) at the rows next to it
+    and no rotation anywhere else: the stored key must be the quarter turn,
+    exactly, and V must be stored unrotated."""
+    _, wl, kp, vp, kn, vn, g = _rope_case(504)
+    half = D // 2
+    cos_t = np.ones((W.MAX_SEQ_LEN, half), np.float32)
+    sin_t = np.zeros_like(cos_t)
+    pos = [int(p) for p in wl.positions]
+    for p in pos:
+        for r in (p - 1, p + 1):
+            cos_t[r] = -1.0
+    for p in pos:
+        cos_t[p], sin_t[p] = 0.0, 1.0
+    assert len(set(pos)) == len(pos) and min(pos) >= 1
+    assert orc.append_rope(g, 0, kn[0].copy(), vn[0].copy(), kp, vp, wl.block_tables,
+                           wl.positions, cos_t, sin_t) == oracle_pkg.OK
+    for b, p in enumerate(pos):
+        page, slot = wl.block_tables[0, b, p // P], p % P
+        got = bits_to_f64(kp[page, :, slot, :])
+        x = bits_to_f64(kn[0, b])
+        np.testing.assert_array_equal(got[:, :half], -x[:, half:])
+        np.testing.assert_array_equal(got[:, half:], x[:, :half])
+        np.testing.assert_array_equal(vp[page, :, slot, :], vn[0, b])
+
+
+def pin_rope_key_within_rounding_of_exact_rotation(orc):
+    """At general angles (base 10000, positions spread over the context) the
+    stored key is the exact rotation of the BF16 input by the table's FP32
+    angles, rounded to BF16: each stored value lies within half a BF16 unit
+    in the last place of the exact value, widened only by the FP32 rounding of
+    the two products and their sum, 2^-23 (|x c| + |y s|)."""
+    _, wl, kp, vp, kn, vn, g = _rope_case(505)
+    half = D // 2
+    cos_t, sin_t = W.rope_tables(base=10000.0)
+    positions = np.array([1999, 517, 3], np.int32)
+    table = wl.block_tables.copy()
+    for b, p in enumerate(positions.tolist()):        # the pages those positions need
+        table[0, b, p // P] = table[0, b, 0]
+    assert orc.append_rope(g, 0, kn[0].copy(), vn[0].copy(), kp, vp, table, positions,
+                           cos_t, sin_t) == oracle_pkg.OK
+    for b, p in enumerate(positions.tolist()):
+        got = bits_to_f64(kp[table[0, b, p // P], :, p % P, :])
+        x = bits_to_f64(kn[0, b])[:, :half]
+        y = bits_to_f64(kn[0, b])[:, half:]
+        c = cos_t[p].astype(np.float64)
+        s = sin_t[p].astype(np.float64)
+        exact = np.concatenate([x * c - y * s, y * c + x * s], axis=1)
+        f32_err = 2.0 ** -23 * np.concatenate([np.abs(x * c) + np.abs(y * s),
+                                               np.abs(y * c) + np.abs(x * s)], axis=1)
+        mag = np.abs(exact) + f32_err
+        half_ulp = np.where(mag > 0, 2.0 ** (np.floor(np.log2(np.maximum(mag, 1e-300))) - 8),
+                            0.0)
+        assert np.all(np.abs(got - exact) <= half_ulp + f32_err), (b, p)
+        # and the rotation is not the identity at these angles
+        assert np.any(got != bits_to_f64(kn[0, b]))
+
+
 def pin_rope_keeps_pair_norms_and_relative_scores(orc):
     """A rotation keeps |(x_i, x_{i+D/2})|, and q_p . k_t depends on p - t only."""
     rng = np.random.default_rng(503)
@@ -502,6 +564,8 @@ ALL_PINS = [pin_golden_closed_form, pin_pool_geometry_facts, pin_single_token_re
             pin_paged_equals_contiguous, pin_contiguous_matches_sdpa, pin_paged_matches_sdpa,
             pin_split_equals_unsplit, pin_mt_matches_single_thread, pin_append_closed_form,
             pin_append_rejects_out_of_range, pin_rope_zero_angle_is_identity,
-            pin_rope_quarter_turn_swaps_halves, pin_rope_keeps_pair_norms_and_relative_scores,
+            pin_rope_quarter_turn_swaps_halves, pin_rope_key_uses_its_own_position,
+            pin_rope_key_within_rounding_of_exact_rotation,
+            pin_rope_keeps_pair_norms_and_relative_scores,
             pin_prefill_matches_causal_sdpa, pin_prefill_first_token_returns_its_v_row,
             pin_prefill_chunks_compose, pin_prefill_fill_closed_form]

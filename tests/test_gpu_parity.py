@@ -185,6 +185,79 @@ def test_programmatic_dependent_launch_chain_matches_oracle(fused, graph):
         assert_close(out.cpu().numpy(), ref, f"pdl fused={fused} graph={graph} S={splits}")
 
 
+@pytest.mark.parametrize("layers,first_lens", [
+    (2, [1, 15, 16, 31, 200, 2040]),                      # a cluster-merge plan
+    (3, [1, 15, 16, 17, 33, 100, 300, 511, 1000, 2040] * 4),   # 40 sequences: ticket merge
+])
+def test_consecutive_decode_steps_under_pdl_match_oracle(layers, first_lens):
+    """Several decode steps of a 2- or 3-layer model, every layer's fused
+    launch chained to the one before by programmatic dependent launch inside
+    one CUDA graph. Step s appends each sequence's token at position
+    first_len + s - 1 and attends first_len + s tokens, so the launch of a
+    layer at step s + 1 reads, before its wait, the row that the same layer's
+    launch of step s wrote a few launches earlier; a launch must not run
+    ahead of those writes. Rows that no step has written yet hold NaN."""
+    steps = 5
+    first = np.asarray(first_lens, np.int32)
+    final = first + steps - 1
+    wl = W.custom(final, num_layers=layers, seed=460 + layers, name="pdl-steps")
+    kp_h, vp_h = (bits(p) for p in wl.pools("cpu", "nan"))
+    nan = np.uint16(W.BF16_NAN_BITS)
+    for layer in range(layers):
+        for b in range(wl.batch):
+            for p in range(int(first[b]) - 1, int(final[b])):
+                page = wl.block_tables[layer, b, p // 16]
+                kp_h[page, :, p % 16, :] = nan
+                vp_h[page, :, p % 16, :] = nan
+    gen = torch.Generator().manual_seed(470 + layers)
+
+    def draws(shape):
+        return torch.randn(shape, generator=gen).to(torch.bfloat16)
+
+    q = [draws((layers, wl.batch, 32, 64)) for _ in range(steps)]
+    kn = [draws((layers, wl.batch, 8, 64)) for _ in range(steps)]
+    vn = [draws((layers, wl.batch, 8, 64)) for _ in range(steps)]
+    lens = [torch.from_numpy(first + s) for s in range(steps)]
+
+    # oracle: the steps in order on host copies of the pools
+    refs = []
+    ok, ov = kp_h.copy(), vp_h.copy()
+    for s in range(steps):
+        ref, ok, ov = oracle_step(wl, ok, ov, bits(q[s]), bits(kn[s]), bits(vn[s]),
+                                  lens=(first + s).astype(np.int32))
+        refs.append(ref)
+
+    dev = "cuda"
+    table = torch.from_numpy(wl.block_tables).to(dev)
+    q_d = [x.to(dev) for x in q]
+    kn_d = [x.to(dev) for x in kn]
+    vn_d = [x.to(dev) for x in vn]
+    lens_d = [x.to(dev) for x in lens]
+    for splits in (0, 32):
+        pool = _pool(wl, flags=pkv.PKV_FLAG_PDL)
+        kp = torch.from_numpy(kp_h.view(np.int16)).view(torch.bfloat16).to(dev)
+        vp = torch.from_numpy(vp_h.view(np.int16)).view(torch.bfloat16).to(dev)
+        out = [torch.full((layers, wl.batch, 32, 64), float("nan"), device=dev)
+               for _ in range(steps)]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for step in range(steps):
+                for layer in range(layers):
+                    pkv.pkv_append_attend(pool, layer, q_d[step][layer], kn_d[step][layer],
+                                          vn_d[step][layer], kp, vp, table, lens_d[step],
+                                          out[step][layer], num_splits=splits,
+                                          stream=torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            g.replay()
+        s.synchronize()
+        assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+        assert np.array_equal(bits(kp), ok) and np.array_equal(bits(vp), ov)
+        for step in range(steps):
+            assert_close(out[step].cpu().numpy(), refs[step], f"step {step} S={splits}")
+
+
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("pdl", [False, True])
 def test_many_sequences_chain_matches_oracle(fused, pdl):

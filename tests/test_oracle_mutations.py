@@ -68,6 +68,17 @@ MUTATIONS = [
      "rotated[row + i] = float_to_bf16_rne(xc + ys);", 0),
     ("key rotation pairs neighbours", "const float y = bf16_bits_to_float(k_new[row + i + half]);",
      "const float y = bf16_bits_to_float(k_new[row + (i ^ 1)]);", 0),
+    ("key rotation uses the next position's cosine",
+     "const float c = cos_t[static_cast<size_t>(pos) * half + i];",
+     "const float c = cos_t[static_cast<size_t>(pos + 1) * half + i];", 0),
+    ("key rotation uses the previous position's sine",
+     "const float s = sin_t[static_cast<size_t>(pos) * half + i];",
+     "const float s = sin_t[static_cast<size_t>(pos - 1) * half + i];", 0),
+    ("key rotation reads the sequence index's row",
+     "const float c = cos_t[static_cast<size_t>(pos) * half + i];",
+     "const float c = cos_t[static_cast<size_t>(b) * half + i];", 0),
+    ("key rotation drops the sine term", "rotated[row + i + half] = float_to_bf16_rne(yc + xs);",
+     "rotated[row + i + half] = float_to_bf16_rne(yc);", 0),
     ("query rotation swaps cos and sin", "q_out[row + i + half] = y * c + x * s;",
      "q_out[row + i + half] = y * s + x * c;", 0),
     ("query rotation uses the wrong position",

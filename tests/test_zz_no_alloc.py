@@ -1,4 +1,5 @@
-"""The decode entry point that allocates nothing, against the pooled one.
+"""The decode entry point that allocates nothing, against the oracle and the
+pooled entry point.
 
 Some callers of this library may not allocate device memory: they run under
 another component's allocator that owns every device allocation, or in a
@@ -17,7 +18,7 @@ import torch
 
 import paged_kv_cache_210_gb300 as pkv
 import workloads as W
-from gpu_helpers import DeviceState, assert_close
+from gpu_helpers import DeviceState, assert_close, bits, oracle_step
 
 pytestmark = pytest.mark.gpu
 
@@ -40,14 +41,24 @@ def _noalloc(lib, st, wl, layer, out, num_splits, err, q=None):
         wl.batch, pkv.MAX_SEQ_LEN, wl.batch, num_splits, err.data_ptr(), s)
 
 
-def test_noalloc_matches_pooled_entry_point_on_two_calls(lib):
-    wl = W.custom([1, 16, 17, 300, 2047, 2048, 40, 1000], num_layers=2, seed=400,
-                  name="noalloc")
+def _appended_state(wl):
+    """Device state with every layer's new token appended, and the oracle's
+    output for it (FP64, computed from the host copies of the pools)."""
     st = DeviceState(wl)
     pool = pkv.pkv_pool_create(wl.num_layers, wl.num_pages, wl.batch)
     for layer in range(wl.num_layers):
         pkv.pkv_append(pool, layer, st.k_new[layer], st.v_new[layer], st.k_pool, st.v_pool,
                        st.table, st.positions)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    ref, _, _ = oracle_step(wl, st.host_k, st.host_v, bits(st.q.cpu()), bits(st.k_new.cpu()),
+                            bits(st.v_new.cpu()))
+    return st, pool, ref
+
+
+def test_noalloc_matches_oracle_and_pooled_entry_point_on_two_calls(lib):
+    wl = W.custom([1, 16, 17, 300, 2047, 2048, 40, 1000], num_layers=2, seed=400,
+                  name="noalloc")
+    st, pool, oracle_ref = _appended_state(wl)
     for splits in (4, 1, 16):
         ref = torch.full_like(st.out, float("nan"))
         for layer in range(wl.num_layers):
@@ -62,8 +73,29 @@ def test_noalloc_matches_pooled_entry_point_on_two_calls(lib):
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         for layer in range(wl.num_layers):
+            # against the FP64 oracle, and against the pooled entry point
+            assert_close(got[layer].cpu().numpy(), oracle_ref[layer],
+                         f"oracle, layer {layer} S={splits}")
             assert_close(got[layer].cpu().numpy(), ref[layer].cpu().double().numpy(),
-                         f"layer {layer} S={splits}")
+                         f"pooled, layer {layer} S={splits}")
+
+
+@pytest.mark.parametrize("batch,splits", [(32, 8), (16, 16), (256, 1)])
+def test_noalloc_at_the_scratch_limit_matches_oracle(lib, batch, splits):
+    """batch x splits = 256 (sequence, split) rows, the whole static scratch,
+    on two calls in a row (layer 0, then layer 1)."""
+    rng = np.random.default_rng(402 + batch)
+    lens = rng.integers(1, 2049 if batch <= 32 else 400, batch).astype(np.int32)
+    lens[:4] = [1, 16, 17, 2048 if batch <= 32 else 399]
+    wl = W.custom(lens, num_layers=2, seed=403 + batch, hole_every=3, name="noalloc-limit")
+    st, _, oracle_ref = _appended_state(wl)
+    got = torch.full_like(st.out, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for layer in range(wl.num_layers):
+        assert _noalloc(lib, st, wl, layer, got[layer], splits, err) == pkv.PKV_OK
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(got.cpu().numpy(), oracle_ref, f"B={batch} S={splits}")
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(lib):
