@@ -3,9 +3,14 @@
 A step is one decode step of the whole hot path over one batch: for each of
 the 16 layers, the fused append-then-attend launch (append the new token's
 K/V into its block-table slot, then paged GQA decode attention with split-KV
-and the in-launch merge). The default workload is a Llama-3.2-1B decode step
-at the pages' default pool: batch 2 at 2,048 tokens, 4,096-page (128 MiB)
-BF16 pool, pages shuffled, BF16 N(0,1) inputs.
+and the in-launch merge). The headline workload is the largest
+configuration that fits one GPU, the large ragged batch: 256 sequences with
+lengths uniform in [1, 2048] (1, 16, 32, 2048, 17 and 1024 among them), a
+pool sized to fit them, BF16 N(0,1) inputs with K scaled by 4, 32q/8kv heads,
+head_dim 64, 16-token pages. Beside it ("per_config") every other
+configuration is timed the same way for at least a second each: the
+Llama-3.2-1B default step (batch 2 at 2,048 tokens, 128 MiB pool), the
+batch-64 continuous-batching mix, and the long-context batches 1 and 4.
 
 Timing: the 16 launches of a step are captured in a CUDA graph with
 GPU-timestamped events before and after them; before every step an untimed
@@ -19,9 +24,15 @@ launches also rotate the appended key and the queries to their position
 (pkv_append_attend_rope; angle tables for base 500000), adding 256 bytes (the
 position's cos and sin rows) per (sequence, layer).
 
+e2e: the same step with its inputs copied from pinned host memory and its
+output copied back inside the timed region, (a) replaying a CUDA graph that
+holds the copies and the launches, (b) issuing the C-ABI calls from the host
+every step (what a decode loop without graphs pays).
+
 --impl reference times the CPU oracle (FP64 C++) on the host cores on a
 bounded sample of the same workload and prints the same line with
-"impl": "reference".
+"impl": "reference". cpu_baseline reports the oracle single-threaded and on
+every host core, with the core count and CPU model.
 """
 
 import argparse
@@ -44,15 +55,21 @@ import workloads as W  # noqa: E402
 
 METRIC = "paged decode attention KV GB/s and seq-layer steps/s; % of GB300 HBM peak"
 NOMINAL_HBM_GBS = 8000.0
+# each takes the number of layers (16: the model's; fewer only for profiling
+# captures, which launch the same per-layer kernels on a smaller pool)
 WORKLOADS = {
-    "llama-b2-2048": W.llama_default,
-    "mix-b64": W.continuous_mix,
-    "ragged-b256": W.large_ragged,
-    "long-b1": lambda: W.long_context(1),
-    "long-b4": lambda: W.long_context(4),
-    "long-b8": lambda: W.long_context(8),
-    "long-b16": lambda: W.long_context(16),
+    "llama-b2-2048": lambda n=16: W.llama_default(num_layers=n),
+    "mix-b64": lambda n=16: W.continuous_mix(num_layers=n),
+    "ragged-b256": lambda n=16: W.large_ragged(num_layers=n),
+    "long-b1": lambda n=16: W.long_context(1, num_layers=n),
+    "long-b4": lambda n=16: W.long_context(4, num_layers=n),
+    "long-b8": lambda n=16: W.long_context(8, num_layers=n),
+    "long-b16": lambda n=16: W.long_context(16, num_layers=n),
 }
+# the workloads timed beside the headline (every configuration of the task
+# that fits one GPU: the default decode step, the continuous-batching mix, the
+# large ragged batch, and the long-context batches 1 and 4)
+PER_CONFIG = ["llama-b2-2048", "mix-b64", "ragged-b256", "long-b1", "long-b4"]
 DESCRIPTIONS = {
     "llama-b2-2048": "Llama-3.2-1B decode step at the default 128 MiB pool: 16 layers, batch 2 at "
                      "seq_len 2048, 32q/8kv heads, head_dim 64, 4096 shuffled 16-token pages",
@@ -223,17 +240,33 @@ def oracle_inputs(wl):
     return bits(kp), bits(vp), bits(wl.q()), bits(wl.k_new()), bits(wl.v_new())
 
 
-def time_oracle(wl, layers_per_step, n_steps, threads, rope=False):
+def oracle_sample(wl, max_seqs=64, max_layers=4):
+    """A bounded sample of a workload for timing the CPU oracle: its first
+    `max_seqs` sequences (the same lengths, so the same length mix for the
+    ragged and log-uniform workloads) over `max_layers` layers, with a pool
+    of just their pages. Bytes per (sequence, layer) are those of the
+    workload, so GB/s compares directly."""
+    if wl.batch <= max_seqs and wl.num_layers <= max_layers:
+        return wl
+    return W.custom(wl.seq_lens[:max_seqs], num_layers=min(wl.num_layers, max_layers),
+                    seed=wl.seed, k_scale=wl.k_scale, name=wl.name + "-sample")
+
+
+def time_oracle(wl, layers_per_step, n_steps, threads, rope=False, inputs=None):
     """Runs the oracle (append + attention, rotated when `rope`) on
-    `layers_per_step` layers per step, layers in parallel over host threads;
-    returns (seconds, bytes)."""
+    `layers_per_step` layers per step over `threads` host threads: layers in
+    parallel, and within a layer sequences spread over the layer's share of
+    the threads. Returns (seconds, bytes, layer-steps, threads used)."""
     import oracle
     orc = oracle.load()
-    kp, vp, q, kn, vn = oracle_inputs(wl)
+    kp, vp, q, kn, vn = inputs if inputs is not None else oracle_inputs(wl)
     g = oracle.geometry(wl.num_layers, wl.num_pages, wl.batch)
     pos = wl.positions
     bytes_per_layer = step_bytes(wl, rope) // wl.num_layers
     cos_t, sin_t = W.rope_tables(base=ROPE_BASE)
+    workers = max(1, min(threads, layers_per_step))
+    per_layer = max(1, threads // workers)
+    used = workers * (1 if rope else min(per_layer, wl.batch))
 
     def one_layer(layer):
         if rope:
@@ -246,53 +279,111 @@ def time_oracle(wl, layers_per_step, n_steps, threads, rope=False):
             return layer
         st = orc.append(g, layer, kn[layer].copy(), vn[layer].copy(), kp, vp, wl.block_tables,
                         pos)
-        st2, _, _, _ = orc.decode_attention(g, layer, q[layer].copy(), kp, vp,
-                                            wl.block_tables, wl.seq_lens)
+        st2, _ = orc.decode_attention_mt(g, layer, q[layer].copy(), kp, vp, wl.block_tables,
+                                         wl.seq_lens, per_layer)
         assert st == st2 == oracle.OK
         return layer
 
     total_layers = 0
     t0 = time.perf_counter()
-    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
         for s in range(n_steps):
             layers = [(s * layers_per_step + i) % wl.num_layers for i in range(layers_per_step)]
             list(ex.map(one_layer, layers))
             total_layers += len(layers)
     dt = time.perf_counter() - t0
-    return dt, total_layers * bytes_per_layer, total_layers
+    return dt, total_layers * bytes_per_layer, total_layers, used
 
 
 def cpu_threads():
-    return max(1, min(os.cpu_count() or 1, 16))
+    return max(1, os.cpu_count() or 1)
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(wl, rope=False, seconds=8.0):
+    """The oracle as it stands, timed on this host's cores on a bounded
+    sample of the workload: single-threaded, and on all cores (about
+    `seconds` of wall time each). Returns the cpu_baseline object."""
+    sw = oracle_sample(wl)
+    inputs = oracle_inputs(sw)
+    nproc = cpu_threads()
+    result = {"unit": "GB/s", "kind": "oracle", "nproc": nproc, "cpu_model": cpu_model()}
+    for key, threads in (("single_thread", 1), ("all_cores", nproc)):
+        per_step = min(sw.num_layers, threads) if threads > 1 else 1
+        probe, _, _, _ = time_oracle(sw, per_step, 1, threads, rope, inputs)
+        n_steps = max(1, int(seconds / max(probe, 1e-6)))
+        dt, nbytes, n_layers, used = time_oracle(sw, per_step, n_steps, threads, rope, inputs)
+        result[key] = {"value": round(nbytes / dt / 1e9, 4), "cores": used,
+                       "sample": f"{n_layers} layer-steps of {sw.batch} sequences "
+                                 f"(lengths as the workload's first {sw.batch}), "
+                                 f"{per_step} layer(s) at a time, {dt:.1f} s wall"}
+    result["value"] = result["all_cores"]["value"]
+    result["cores"] = result["all_cores"]["cores"]
+    result["sample"] = result["all_cores"]["sample"]
+    return result
+
+
+def decode_config(wl, args, world=1):
+    return {"workload": f"{wl.name}: {DESCRIPTIONS[wl.name]}",
+            "batch": wl.batch, "layers": wl.num_layers,
+            "seq_lens": "all 2048" if np.all(wl.seq_lens == 2048)
+            else f"mean {float(wl.seq_lens.mean()):.1f}",
+            "rope": f"key and queries rotated in the launch, base {ROPE_BASE:g}" if args.rope
+            else "none (keys arrive rotated)",
+            "l2": "flushed before every step (read of a buffer twice the L2 size, outside the "
+                  "timed events)",
+            "bytes_per_step": step_bytes(wl, args.rope),
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return
     wl = WORKLOADS[args.workload]()
-    threads = min(cpu_threads(), wl.num_layers)
+    sw = oracle_sample(wl)
+    inputs = oracle_inputs(sw)
+    threads = cpu_threads()
+    per_step = min(sw.num_layers, threads)
     # size a step so the whole run stays within about a minute and a half
-    probe_dt, _, probe_layers = time_oracle(wl, threads, 1, threads, args.rope)
-    per_layer = probe_dt / probe_layers * threads   # core-seconds per layer
+    probe_dt, _, probe_layers, _ = time_oracle(sw, per_step, 1, threads, args.rope, inputs)
+    per_layer = probe_dt / probe_layers
     budget = 90.0 / max(1, args.steps + args.warmup)
-    layers = max(1, min(wl.num_layers, int(budget * threads / max(per_layer, 1e-9))))
-    time_oracle(wl, layers, args.warmup, threads, args.rope)
-    dt, nbytes, n_layers = time_oracle(wl, layers, args.steps, threads, args.rope)
+    layers = max(1, min(4 * per_step, int(budget / max(per_layer, 1e-9))))
+    time_oracle(sw, layers, args.warmup, threads, args.rope, inputs)
+    dt, nbytes, n_layers, used = time_oracle(sw, layers, args.steps, threads, args.rope, inputs)
     value = nbytes / dt / 1e9
-    sample = (f"{layers} of {wl.num_layers} layers per step (all {wl.batch} sequences), "
-              f"layers in parallel on {threads} threads, {args.steps} steps")
+    sample = (f"{layers} layer-steps per step, each over {sw.batch} sequences (the workload's "
+              f"first {sw.batch} lengths), on {used} of {threads} host threads, "
+              f"{args.steps} steps")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
-                   "layers_per_step": layers,
-                   "rope": f"key and queries rotated, base {ROPE_BASE:g}" if args.rope
-                   else "none"},
-        "seq_layer_steps_per_s": round(n_layers * wl.batch / dt, 2),
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle", "sample": sample},
+        "config": decode_config(wl, args, world),
+        "seq_layer_steps_per_s": round(n_layers * sw.batch / dt, 2),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used,
+                         "kind": "oracle", "sample": sample, "nproc": threads,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -307,6 +398,173 @@ def make_event():
         return torch.cuda.Event(enable_timing=True), False
 
 
+def nvtx_push(name):
+    try:
+        torch.cuda.nvtx.range_push(name)
+    except Exception:
+        pass
+
+
+def nvtx_pop():
+    try:
+        torch.cuda.nvtx.range_pop()
+    except Exception:
+        pass
+
+
+class DecodeRun:
+    """One workload's decode step on the device: inputs resident in HBM, the
+    pool handle, and CUDA graphs of the step (events around it, and events
+    between its launches)."""
+
+    def __init__(self, pkv, wl, dev, args, stream, flush):
+        self.pkv, self.wl, self.dev, self.args = pkv, wl, dev, args
+        self.stream, self.flush = stream, flush
+        L, B = wl.num_layers, wl.batch
+        self.k_pool, self.v_pool = wl.pools(dev, "zero")
+        self.q = wl.q(dev)
+        self.k_new, self.v_new = wl.k_new(dev), wl.v_new(dev)
+        self.table = torch.from_numpy(wl.block_tables).to(dev)
+        self.lens = torch.from_numpy(wl.seq_lens).to(dev)
+        self.out = torch.zeros((L, B, W.NUM_Q_HEADS, W.HEAD_DIM), device=dev)
+        self.pool = pkv.pkv_pool_create(L, wl.num_pages, B,
+                                        flags=0 if args.no_pdl else pkv.PKV_FLAG_PDL)
+        self.rope_cos, self.rope_sin = (torch.from_numpy(t).to(dev)
+                                        for t in W.rope_tables(base=ROPE_BASE))
+        self.launches = 1 if args.persistent else L
+        made = [make_event() for _ in range(self.launches + 3)]
+        self.external = all(e[1] for e in made)
+        self.events = [e[0] for e in made[:self.launches + 1]]
+        self.t_start, self.t_end = made[self.launches + 1][0], made[self.launches + 2][0]
+        with torch.cuda.stream(stream):
+            self.step()
+        torch.cuda.synchronize()
+        assert pkv.pkv_get_error(self.pool) == pkv.PKV_OK
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            self.step([self.t_start, self.t_end] if self.external else None)
+        self.launch_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.launch_graph, stream=stream):
+            self.step(self.events if self.external else None)
+
+    def plan(self):
+        p = self.pkv.pkv_plan_decode(self.pkv.pkv_pool_device_figures(self.pool), self.wl.batch,
+                                     self.args.splits)
+        shape = {0: "ticket merge", 1: "narrow cluster", 2: "wide cluster"}[p.shape]
+        if self.args.persistent:
+            return "one persistent launch for all layers (cluster per (sequence, kv head))"
+        if p.cluster:
+            return f"{shape}, S = {p.num_splits} ({p.grid_splits * 8 * self.wl.batch} blocks)"
+        ranges = (f"{p.num_splits} ranges" if p.num_splits else
+                  f"ranges of {p.chunk_pages} pages")
+        return (f"{shape}, {ranges}, up to {p.grid_splits * 8 * self.wl.batch} blocks"
+                + (", longest first" if p.longest_first else ""))
+
+    def step(self, marks=None, stream=None):
+        """The 16 launches (or the one multi-layer launch); `marks` = events
+        recorded before, between and after."""
+        pkv, a = self.pkv, self.args
+        s = stream if stream is not None else torch.cuda.current_stream()
+        if marks:
+            marks[0].record(s)
+        if a.persistent:
+            pkv.pkv_append_attend_layers(self.pool, 0, self.q, self.k_new, self.v_new,
+                                         self.k_pool, self.v_pool, self.table, self.lens,
+                                         self.out, stream=s)
+            if marks:
+                marks[-1].record(s)
+            return
+        for layer in range(self.wl.num_layers):
+            if a.rope:
+                pkv.pkv_append_attend_rope(self.pool, layer, self.q[layer], self.k_new[layer],
+                                           self.v_new[layer], self.k_pool, self.v_pool,
+                                           self.table, self.lens, self.rope_cos, self.rope_sin,
+                                           self.out[layer], num_splits=a.splits, stream=s)
+            else:
+                pkv.pkv_append_attend(self.pool, layer, self.q[layer], self.k_new[layer],
+                                      self.v_new[layer], self.k_pool, self.v_pool, self.table,
+                                      self.lens, self.out[layer], num_splits=a.splits, stream=s)
+            if marks and len(marks) > 2:
+                marks[layer + 1].record(s)
+        if marks and len(marks) == 2:
+            marks[1].record(s)
+
+    def replay(self, g, ev0, ev1):
+        with torch.cuda.stream(self.stream):
+            self.flush()
+            if self.external:
+                g.replay()
+            else:
+                ev0.record(self.stream)
+                g.replay()
+                ev1.record(self.stream)
+
+    def time_steps(self, n):
+        """n timed steps (L2 flushed before each), device ms per step."""
+        ms = []
+        for _ in range(n):
+            self.replay(self.graph, self.t_start, self.t_end)
+            self.stream.synchronize()
+            ms.append(self.t_start.elapsed_time(self.t_end))
+        return ms
+
+    def time_launches(self, n):
+        """Per-launch device ms from the graph with events between launches."""
+        out = []
+        if not self.external:
+            return out
+        for _ in range(n):
+            self.replay(self.launch_graph, self.events[0], self.events[self.launches])
+            self.stream.synchronize()
+            out.extend(self.events[i].elapsed_time(self.events[i + 1])
+                       for i in range(self.launches))
+        return out
+
+    def check(self):
+        assert self.pkv.pkv_get_error(self.pool) == self.pkv.PKV_OK
+
+    def close(self):
+        self.pool.close()
+        for name in ("graph", "launch_graph", "k_pool", "v_pool", "q", "k_new", "v_new",
+                     "table", "lens", "out"):
+            setattr(self, name, None)
+
+
+def gbs(nbytes, ms):
+    return nbytes / (ms * 1e-3) / 1e9
+
+
+def per_config_entry(run, hbm_peak, min_seconds, min_steps):
+    """One workload timed over at least `min_seconds` of replays (and at least
+    `min_steps` steps) with its own clock samples."""
+    nbytes = step_bytes(run.wl, run.args.rope)
+    for _ in range(3):
+        run.replay(run.graph, run.t_start, run.t_end)
+    torch.cuda.synchronize()
+    probe = statistics.median(run.time_steps(5))
+    n = max(min_steps, int(min_seconds * 1e3 / max(probe, 1e-3)))
+    sampler = ClockSampler(run.dev)
+    time.sleep(0.2)
+    nvtx_push(f"per-config {run.wl.name}")
+    ms = run.time_steps(n)
+    nvtx_pop()
+    clocks = sampler.stop()
+    launch_ms = run.time_launches(max(3, min(200, n // 4)))
+    run.check()
+    mean = float(np.mean(ms))
+    value = gbs(nbytes, mean)
+    return {"gbs": round(value, 2), "pct_of_measured_hbm": round(100 * value / hbm_peak, 2),
+            "pct_of_nominal_hbm": round(100 * value / NOMINAL_HBM_GBS, 2),
+            "ms_per_step": round(mean, 5),
+            "step_ms_p10_p50_p90": [round(float(np.percentile(ms, p)), 5) for p in (10, 50, 90)],
+            "per_launch_us": round(1e3 * mean / run.launches, 3),
+            "per_launch_us_events_between_launches":
+                round(1e3 * float(np.mean(launch_ms)), 3) if launch_ms else None,
+            "seq_layer_steps_per_s": round(run.wl.batch * run.wl.num_layers / (mean * 1e-3), 1),
+            "steps": n, "timed_s": round(sum(ms) * 1e-3, 3), "plan": run.plan(),
+            "bytes_per_step": nbytes, "clocks": clocks}
+
+
 def run_ours(args, world, rank, local):
     import paged_kv_cache_210_gb300 as pkv
     from paged_kv_cache_210_gb300 import build as lib_build
@@ -315,18 +573,10 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     lib_build.build()
     pkv.load()
-    wl = WORKLOADS[args.workload]()
+    wl = WORKLOADS[args.workload](args.layers)
     L, B = wl.num_layers, wl.batch
-
-    k_pool, v_pool = wl.pools(dev, "zero")
-    q = wl.q(dev)
-    k_new, v_new = wl.k_new(dev), wl.v_new(dev)
-    table = torch.from_numpy(wl.block_tables).to(dev)
-    lens = torch.from_numpy(wl.seq_lens).to(dev)
-    out = torch.zeros((L, B, W.NUM_Q_HEADS, W.HEAD_DIM), device=dev)
-    pool = pkv.pkv_pool_create(L, wl.num_pages, B, flags=0 if args.no_pdl else pkv.PKV_FLAG_PDL)
-    splits = args.splits
-    rope_cos, rope_sin = (torch.from_numpy(t).to(dev) for t in W.rope_tables(base=ROPE_BASE))
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -335,132 +585,89 @@ def run_ours(args, world, rank, local):
         return flush_buf.sum()
 
     stream = torch.cuda.Stream(device=dev)
-    launches = 1 if args.persistent else L        # kernel launches per step
-    made = [make_event() for _ in range(launches + 3)]
-    external = all(e[1] for e in made)
-    events = [e[0] for e in made[:launches + 1]]   # between the launches (per-launch pass)
-    t_start, t_end = made[launches + 1][0], made[launches + 2][0]
+    run = DecodeRun(pkv, wl, dev, args, stream, flush)
+    launches = run.launches
 
-    def step(marks=None):
-        """The 16 launches (or the one multi-layer launch); `marks` = events
-        recorded before, between and after."""
-        s = torch.cuda.current_stream()
-        if marks:
-            marks[0].record(s)
-        if args.persistent:
-            pkv.pkv_append_attend_layers(pool, 0, q, k_new, v_new, k_pool, v_pool, table, lens,
-                                         out, stream=s)
-            if marks:
-                marks[-1].record(s)
-            return
-        for layer in range(L):
-            if args.rope:
-                pkv.pkv_append_attend_rope(pool, layer, q[layer], k_new[layer], v_new[layer],
-                                           k_pool, v_pool, table, lens, rope_cos, rope_sin,
-                                           out[layer], num_splits=splits, stream=s)
-            else:
-                pkv.pkv_append_attend(pool, layer, q[layer], k_new[layer], v_new[layer], k_pool,
-                                      v_pool, table, lens, out[layer], num_splits=splits,
-                                      stream=s)
-            if marks and len(marks) > 2:
-                marks[layer + 1].record(s)
-        if marks and len(marks) == 2:
-            marks[1].record(s)
-
-    with torch.cuda.stream(stream):
-        step()
-    torch.cuda.synchronize()
-    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
-
-    # timed graph: events only before and after the 16 launches
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step([t_start, t_end] if external else None)
-    # per-launch graph: the same launches with an event between each pair
-    launch_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(launch_graph, stream=stream):
-        step(events if external else None)
-
-    # e2e: the same step through the public API with host buffers
-    q_h = q.cpu().pin_memory()
-    kn_h, vn_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-    lens_h = lens.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    # e2e: the same step through the public API with host buffers (pinned),
+    # copies inside the timed region; (a) the step's CUDA graph with the
+    # copies captured in it, (b) direct calls from the host every step
+    q_h = run.q.cpu().pin_memory()
+    kn_h, vn_h = run.k_new.cpu().pin_memory(), run.v_new.cpu().pin_memory()
+    lens_h = run.lens.cpu().pin_memory()
+    out_h = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
     e2e_start, _ = make_event()
     e2e_end, _ = make_event()
+
+    def e2e_body(s):
+        run.q.copy_(q_h, non_blocking=True)
+        run.k_new.copy_(kn_h, non_blocking=True)
+        run.v_new.copy_(vn_h, non_blocking=True)
+        run.lens.copy_(lens_h, non_blocking=True)
+        run.step(stream=s)
+        out_h.copy_(run.out, non_blocking=True)
+
     e2e_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(e2e_graph, stream=stream):
         s = torch.cuda.current_stream()
-        if external:
+        if run.external:
             e2e_start.record(s)
-        q.copy_(q_h, non_blocking=True)
-        k_new.copy_(kn_h, non_blocking=True)
-        v_new.copy_(vn_h, non_blocking=True)
-        lens.copy_(lens_h, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
-        if external:
+        e2e_body(s)
+        if run.external:
             e2e_end.record(s)
     h2d = sum(t.numel() * t.element_size() for t in (q_h, kn_h, vn_h, lens_h))
     d2h = out_h.numel() * out_h.element_size()
 
-    def replay_timed(g, ev0, ev1):
-        with torch.cuda.stream(stream):
-            flush()
-            if external:
-                g.replay()
-            else:
-                ev0.record(stream)
-                g.replay()
-                ev1.record(stream)
-
     # warm-up
     for _ in range(args.warmup):
-        replay_timed(graph, t_start, t_end)
+        run.replay(run.graph, run.t_start, run.t_end)
     torch.cuda.synchronize()
 
-    # timed region
+    # timed region: exactly args.steps steps
     barrier(world)
     torch.cuda.synchronize()
     sampler = ClockSampler(dev)
     time.sleep(0.3)
-    step_ms = []
     wall0 = time.perf_counter()
-    for _ in range(args.steps):
-        replay_timed(graph, t_start, t_end)
-        stream.synchronize()
-        step_ms.append(t_start.elapsed_time(t_end))
+    nvtx_push(f"timed steps {wl.name}")
+    step_ms = run.time_steps(args.steps)
+    nvtx_pop()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(world)
     clocks = sampler.stop()
     total_ms = max_over_ranks(sum(step_ms), world)
-    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    run.check()
 
     # per-launch durations of the dominant kernel (same launches, same flush)
-    launch_ms, launch_step_ms = [], []
-    if external:
-        for _ in range(max(3, min(args.steps, 400))):
-            replay_timed(launch_graph, events[0], events[launches])
-            stream.synchronize()
-            launch_ms.extend(events[i].elapsed_time(events[i + 1]) for i in range(launches))
-            launch_step_ms.append(events[0].elapsed_time(events[launches]))
+    launch_ms = run.time_launches(max(3, min(args.steps, 400)))
 
-    # e2e steps (host buffers, copies inside the timed events)
+    # e2e (a): graph with the copies
     e2e_ms = []
     for _ in range(max(3, args.steps // 4)):
-        replay_timed(e2e_graph, e2e_start, e2e_end)
+        run.replay(e2e_graph, e2e_start, e2e_end)
         stream.synchronize()
         e2e_ms.append(e2e_start.elapsed_time(e2e_end))
-    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    run.check()
     e2e_total = max_over_ranks(sum(e2e_ms), world)
+    # e2e (b): direct C-ABI calls from the host each step, host wall clock
+    direct_s = []
+    for i in range(3 + max(3, args.steps // 4)):
+        with torch.cuda.stream(stream):
+            flush()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            e2e_body(stream)
+        stream.synchronize()
+        if i >= 3:
+            direct_s.append(time.perf_counter() - t0)
+    run.check()
+    direct_ms = max_over_ranks(1e3 * statistics.median(direct_s), world)
 
     nbytes = step_bytes(wl, args.rope)
     ms_per_step = total_ms / args.steps
     value = whole_job_gbs(world, nbytes, args.steps, total_ms)
     e2e_value = whole_job_gbs(world, nbytes, len(e2e_ms), e2e_total)
-    peaks, peak_kind = measured_peaks()
-    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
 
     # average launch duration: the timed region's events / launches (includes
     # the graph's gaps between launches, so an upper bound on kernel time)
@@ -480,28 +687,31 @@ def run_ours(args, world, rank, local):
                                    ("-rope" if args.rope else ""))
         step_note = ("16 x fused append+attend (one launch per layer), CUDA graph" +
                      ("" if args.no_pdl else ", programmatic dependent launch between layers"))
+    plan = run.plan()
+    run.close()
+    del run
+
+    # every other workload of the set, each timed over at least a second
+    per_config = {}
+    if not args.no_per_config:
+        for name in PER_CONFIG:
+            torch.cuda.empty_cache()
+            other = DecodeRun(pkv, WORKLOADS[name](args.layers), dev, args, stream, flush)
+            per_config[name] = per_config_entry(other, hbm_peak, args.per_config_seconds,
+                                                args.steps)
+            other.close()
+            del other
 
     if rank != 0:
         return
-    chunk_note = "library's choice" if splits == 0 else f"{splits} splits per sequence"
+    chunk_note = "library's choice" if args.splits == 0 else f"{args.splits} splits per sequence"
+    config = decode_config(wl, args, world)
+    config.update({"step": step_note, "splits": chunk_note, "plan": plan})
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "storage_dtype": "bf16", "data": "synthetic",
-        "config": {
-            "workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
-            "batch": B, "layers": L, "seq_lens": "all 2048" if np.all(wl.seq_lens == 2048)
-            else f"mean {float(wl.seq_lens.mean()):.1f}",
-            "step": step_note,
-            "splits": chunk_note,
-            "rope": f"key and queries rotated in the launch, base {ROPE_BASE:g}" if args.rope
-                    else "none (keys arrive rotated)",
-            "l2": "flushed before every step (read of a buffer twice the L2 size, outside the "
-                  "timed events)",
-            "bytes_per_step": nbytes,
-            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-        },
+        "storage_dtype": "bf16", "data": "synthetic", "config": config,
         "seq_layer_steps_per_s": round(world * B * L * args.steps / (total_ms * 1e-3), 1),
         "pct_of_measured_hbm": round(100 * value / world / hbm_peak, 2),
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
@@ -509,7 +719,14 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_total / len(e2e_ms), 5)},
+                "ms_per_step": round(e2e_total / len(e2e_ms), 5),
+                "how": "step's CUDA graph replayed with the pinned host->device input copies "
+                       "and the device->host output copy captured in it (device events)",
+                "ms_per_step_direct_calls": round(direct_ms, 5),
+                "gbs_direct_calls": round(world * gbs(nbytes, direct_ms), 2),
+                "direct_calls_how": f"{launches} C-ABI calls issued from Python each step "
+                                    "(ctypes binding, argument checks, launch) plus the same "
+                                    "copies, host wall clock around the step, median"},
         "gpu_launches": launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
@@ -521,17 +738,10 @@ def run_ours(args, world, rank, local):
                      "bytes_per_launch": nbytes // launches},
         "wall_s_timed_loop": round(wall, 3),
     }
-    if not args.no_cpu_baseline:
-        threads = min(cpu_threads(), L)
-        probe_dt, _, probe_layers = time_oracle(wl, threads, 1, threads, args.rope)
-        # about 20 s of CPU work (core-seconds) in total
-        n_steps = max(1, int(20.0 / max(probe_dt * threads, 1e-6)))
-        dt, cbytes, n_layers = time_oracle(wl, threads, n_steps, threads, args.rope)
-        line["cpu_baseline"] = {
-            "value": round(cbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
-            "kind": "oracle",
-            "sample": f"{n_layers} layer-steps ({threads} layers at a time in parallel, all "
-                      f"{B} sequences each), {dt:.1f} s wall"}
+    if per_config:
+        line["per_config"] = per_config
+    if not args.no_cpu_baseline and rank == 0:
+        line["cpu_baseline"] = cpu_baseline(wl, args.rope)
     print(json.dumps(line), flush=True)
 
 
@@ -791,7 +1001,15 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOADS), default="llama-b2-2048")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="ragged-b256",
+                    help="the headline workload (default: the largest configuration)")
+    ap.add_argument("--layers", type=int, default=16,
+                    help="layers per step (16, the model's; fewer only for profiling captures "
+                         "on a smaller pool: the per-layer launches are the same)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the other workloads beside the headline")
+    ap.add_argument("--per-config-seconds", type=float, default=1.0,
+                    help="minimum timed seconds per workload in per_config")
     ap.add_argument("--splits", type=int, default=0, help="0: the library chooses")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rope", action="store_true",
@@ -811,6 +1029,8 @@ def main():
         ap.error("--persistent plans its own clusters; drop --splits")
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if not 1 <= args.layers <= 16:
+        ap.error("--layers must be in 1..16")
     if args.component == "scheduler":
         run_scheduler_bench(args)
         return

@@ -200,44 +200,44 @@ def tiny(alt_lengths=False) -> Workload:
                     note="1 layer, batch 2, 8-page pool")
 
 
-def llama_default() -> Workload:
+def llama_default(num_layers=16) -> Workload:
     seed = BASE_SEED + 2
     lens = np.full(2, MAX_SEQ_LEN, np.int32)
     num_pages = pages_for_pool_mib(128)
-    table = assign_pages(lens, 16, num_pages, _rng(seed, "pages"))
-    return Workload("llama-b2-2048", 16, num_pages, lens, table, seed,
+    table = assign_pages(lens, num_layers, num_pages, _rng(seed, "pages"))
+    return Workload("llama-b2-2048", num_layers, num_pages, lens, table, seed,
                     note="16 layers, batch 2 at 2048, 128 MiB pool")
 
 
-def continuous_mix(batch=64) -> Workload:
+def continuous_mix(batch=64, num_layers=16) -> Workload:
     seed = BASE_SEED + 3
     r = _rng(seed, "lengths")
     u = r.uniform(np.log(16), np.log(MAX_SEQ_LEN), size=batch)
     lens = np.clip(np.round(np.exp(u)), 16, MAX_SEQ_LEN).astype(np.int32)
-    num_pages = pages_for_pool_mib(4096)
-    table = assign_pages(lens, 16, num_pages, _rng(seed, "pages"), hole_every=3)
-    return Workload("mix-b64", 16, num_pages, lens, table, seed,
+    num_pages = pages_for_pool_mib(4096) * num_layers // 16
+    table = assign_pages(lens, num_layers, num_pages, _rng(seed, "pages"), hole_every=3)
+    return Workload("mix-b64", num_layers, num_pages, lens, table, seed,
                     note="16 layers, batch 64 log-uniform lengths, 4 GiB pool, fragmented")
 
 
-def large_ragged(batch=256) -> Workload:
+def large_ragged(batch=256, num_layers=16) -> Workload:
     seed = BASE_SEED + 4
     r = _rng(seed, "lengths")
     lens = r.integers(1, MAX_SEQ_LEN + 1, size=batch).astype(np.int32)
     forced = [1, 16, 32, 2048, 17, 1024]
     lens[:len(forced)] = forced[:batch]
-    n_pages = int(((lens.astype(np.int64) + PAGE_SIZE - 1) // PAGE_SIZE).sum()) * 16
-    table = assign_pages(lens, 16, n_pages, _rng(seed, "pages"))
-    return Workload("ragged-b256", 16, n_pages, lens, table, seed, k_scale=4.0,
+    n_pages = int(((lens.astype(np.int64) + PAGE_SIZE - 1) // PAGE_SIZE).sum()) * num_layers
+    table = assign_pages(lens, num_layers, n_pages, _rng(seed, "pages"))
+    return Workload("ragged-b256", num_layers, n_pages, lens, table, seed, k_scale=4.0,
                     note="16 layers, batch 256 uniform lengths, K x 4")
 
 
-def long_context(batch=1) -> Workload:
+def long_context(batch=1, num_layers=16) -> Workload:
     seed = BASE_SEED + 5
     lens = np.full(batch, MAX_SEQ_LEN, np.int32)
-    num_pages = pages_for_pool_mib(1024)
-    table = assign_pages(lens, 16, num_pages, _rng(seed, "pages"))
-    return Workload(f"long-b{batch}", 16, num_pages, lens, table, seed,
+    num_pages = pages_for_pool_mib(1024) * num_layers // 16
+    table = assign_pages(lens, num_layers, num_pages, _rng(seed, "pages"))
+    return Workload(f"long-b{batch}", num_layers, num_pages, lens, table, seed,
                     note=f"16 layers, batch {batch} at 2048, 1 GiB pool")
 
 
