@@ -111,7 +111,9 @@ typedef struct pkv_pool* pkv_pool_t;
  * copies of max_batch x 32 x max_splits x (64 + 2) floats), one ticket
  * counter per (sequence, kv head) and parity, one layer counter per sequence
  * (pkv_append_attend_layers) and the sticky error flag.
- * It does not own the pools, tables or tensors. Returns INVALID_ARG for a
+ * It does not own the pools, tables or tensors. A handle's launches share
+ * that scratch, so they must be ordered in one stream (calls issued to
+ * several streams at once need a handle each). Returns INVALID_ARG for a
  * null argument, UNSUPPORTED for a geometry other than the one above, CUDA
  * if an allocation fails. */
 pkv_status pkv_pool_create(const pkv_pool_config* config, pkv_pool_t* out);

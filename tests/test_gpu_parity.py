@@ -568,3 +568,92 @@ def test_large_batch_fused_chain_matches_oracle(pdl):
     keep = np.ones(wl.batch, bool)
     keep[9] = False
     assert_close(got[keep], ref[0][keep], "large batch, one invalid length")
+
+
+# ------------------------------------------------------------ large-batch plans
+@pytest.mark.parametrize("case", ["mix", "equal-lengths", "2048-short"])
+@pytest.mark.parametrize("fused", [True, False])
+def test_large_batch_plans_match_oracle(case, fused):
+    """Batches the library splits into page ranges merged by ticket and hands
+    out longest sequence first: a log-uniform length mix with page-boundary
+    lengths, many sequences of equal length (ranks among equals), and 2048
+    short sequences; two layers chained with programmatic dependent launch in
+    a CUDA graph, replayed twice (the tickets must come back to zero),
+    against the oracle."""
+    rng = np.random.default_rng(480)
+    if case == "mix":
+        lens = np.clip(np.round(np.exp(rng.uniform(np.log(16), np.log(2048), 72))), 1, 2048)
+        lens[:8] = [1, 16, 17, 512, 513, 2047, 2048, 33]
+    elif case == "equal-lengths":
+        lens = np.array([300] * 50 + [16] * 30 + [2048] * 5 + [1] * 10)
+    else:
+        lens = rng.integers(1, 40, 2048)
+    wl = W.custom(lens.astype(np.int32), num_layers=2, seed=481, hole_every=3, name=case)
+    st = DeviceState(wl)
+    ref, ok, ov = oracle_step(wl, st.host_k, st.host_v, *_host_inputs(st), threads=16)
+    pool = _pool(wl, flags=pkv.PKV_FLAG_PDL)
+    plan = pkv.pkv_plan_decode(pkv.pkv_pool_device_figures(pool), wl.batch, 0)
+    assert plan.cluster == 0 and plan.longest_first == 1
+    kp, vp = st.k_pool.clone(), st.v_pool.clone()
+    out = torch.full_like(st.out, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for layer in range(wl.num_layers):
+            cs = torch.cuda.current_stream()
+            if fused:
+                pkv.pkv_append_attend(pool, layer, st.q[layer], st.k_new[layer], st.v_new[layer],
+                                      kp, vp, st.table, st.lens, out[layer], stream=cs)
+            else:
+                pkv.pkv_append(pool, layer, st.k_new[layer], st.v_new[layer], kp, vp, st.table,
+                               st.positions, stream=cs)
+                pkv.pkv_decode_attention(pool, layer, st.q[layer], kp, vp, st.table, st.lens,
+                                         out[layer], stream=cs)
+    for replay in range(2):
+        out.fill_(float("nan"))
+        kp.copy_(st.k_pool)
+        vp.copy_(st.v_pool)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            g.replay()
+        s.synchronize()
+        assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+        assert np.array_equal(bits(kp), ok) and np.array_equal(bits(vp), ov)
+        assert_close(out.cpu().numpy(), ref, f"{case} fused={fused} replay {replay}")
+
+
+def test_large_batch_launch_flags_bad_data_and_recovers():
+    """Invalid lengths are flagged and their rows left untouched; a page id
+    out of range is flagged and skipped; the next launch on the same handle
+    is correct (the tickets were reset)."""
+    rng = np.random.default_rng(490)
+    lens = rng.integers(1, 2049, 100).astype(np.int32)
+    wl = W.custom(lens, num_layers=1, seed=491, name="large-batch-errors")
+    st = DeviceState(wl)
+    ref, _, _ = oracle_step(wl, st.host_k, st.host_v, *_host_inputs(st), threads=16)
+    pool = _pool(wl)
+    kp, vp = st.k_pool.clone(), st.v_pool.clone()
+    bad_lens = st.lens.clone()
+    bad_lens[3] = 0
+    bad_lens[50] = 4096
+    out = torch.full_like(st.out[0], float("nan"))
+    pkv.pkv_append_attend(pool, 0, st.q[0], st.k_new[0], st.v_new[0], kp, vp, st.table,
+                          bad_lens, out)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_ERR_OUT_OF_RANGE
+    got = out.cpu().numpy()
+    assert np.all(np.isnan(got[3])) and np.all(np.isnan(got[50]))
+    keep = np.ones(wl.batch, bool)
+    keep[[3, 50]] = False
+    assert_close(got[keep], ref[0][keep], "others beside invalid lengths")
+    bad_table = st.table.clone()
+    bad_table[0, 7, 0] = wl.num_pages + 3
+    pkv.pkv_decode_attention(pool, 0, st.q[0], kp, vp, bad_table, st.lens, out)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_ERR_OUT_OF_RANGE
+    # a clean launch afterwards
+    kp, vp = st.k_pool.clone(), st.v_pool.clone()
+    out.fill_(float("nan"))
+    pkv.pkv_append_attend(pool, 0, st.q[0], st.k_new[0], st.v_new[0], kp, vp, st.table, st.lens,
+                          out)
+    assert pkv.pkv_get_error(pool) == pkv.PKV_OK
+    assert_close(out.cpu().numpy(), ref[0], "after the flagged launches")
