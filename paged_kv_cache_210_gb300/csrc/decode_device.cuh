@@ -37,6 +37,7 @@ constexpr int kTicketWarps = 4;
 constexpr int kTicketStages = 3;
 constexpr int kClusterWarps = 4;
 constexpr int kNarrowStages = 3;
+constexpr int kWideWarps = 4;
 constexpr int kWideStages = 2;
 constexpr int kMergeThreads = 128;               // one thread per (head, dim pair)
 constexpr int kDefaultMaxSplits = 64;
@@ -69,6 +70,18 @@ struct ClusterInbox {
   float l[kInboxSlots];
 };
 
+// A head leader's inbox for the asynchronous cluster merge (decode_kernel):
+// every block of the cluster delivers its (o, m, l) for the heads this block
+// leads with st.async stores that complete on `bar` in transaction bytes, so
+// the leader wakes as soon as its parts have landed, with no cluster-wide
+// barrier at the end. Slot of block r for head g: (g / S) * S + r.
+struct alignas(16) AsyncInbox {
+  float o[kInboxSlots][kDim];
+  float2 ml[kInboxSlots];
+  unsigned long long bar;
+};
+constexpr uint32_t kPartBytes = (kDim + 2) * sizeof(float);   // one (o, m, l) part: 264 B
+
 template <int kWarps, int kStages>
 struct alignas(16) BlockSmem {
   WarpSmem<kStages> warp[kWarps];
@@ -88,21 +101,24 @@ struct alignas(16) BlockSmem {
 
 using TicketSmem = BlockSmem<kTicketWarps, kTicketStages>;
 using NarrowSmem = BlockSmem<kClusterWarps, kNarrowStages>;
-using WideSmem = BlockSmem<kClusterWarps, kWideStages>;
+using WideSmem = BlockSmem<kWideWarps, kWideStages>;
 static_assert(sizeof(WarpSmem<kTicketStages>) % 16 == 0 &&
                   sizeof(WarpSmem<kWideStages>) % 16 == 0,
               "warp slabs keep 16-byte alignment");
 static_assert(sizeof(NarrowSmem) % 16 == 0 && sizeof(WideSmem) % 16 == 0,
               "the cluster inbox follows BlockSmem 16-byte aligned");
-static_assert(sizeof(ClusterInbox) % 16 == 0, "inbox size keeps 16-byte alignment");
+static_assert(sizeof(ClusterInbox) % 16 == 0 && sizeof(AsyncInbox) % 16 == 0,
+              "inbox sizes keep 16-byte alignment");
+static_assert(sizeof(AsyncInbox) <= sizeof(ClusterInbox) + 16, "the inboxes take the same room");
 // residency the kernels are shaped for: 228 KiB of shared memory per SM, 1 KiB
 // of it reserved per block; 4 ticket blocks or 3 cluster blocks per SM
 constexpr size_t kSmemPerSm = 228 * 1024;
 static_assert(4 * (sizeof(TicketSmem) + 1024) <= kSmemPerSm, "4 ticket blocks per SM");
-static_assert(3 * (sizeof(NarrowSmem) + sizeof(ClusterInbox) + 1024) <= kSmemPerSm,
+static_assert(3 * (sizeof(NarrowSmem) + sizeof(AsyncInbox) + 1024) <= kSmemPerSm,
               "3 narrow cluster blocks per SM");
-static_assert(4 * (sizeof(WideSmem) + sizeof(ClusterInbox) + 1024) <= kSmemPerSm,
-              "4 wide cluster blocks per SM");
+static_assert((16 / kWideWarps) * (sizeof(WideSmem) + sizeof(AsyncInbox) + 1024) <=
+                  kSmemPerSm,
+              "16 warps of wide cluster blocks per SM");
 
 struct DecodeParams {
   const uint16_t* q;          // [B][32][64]
@@ -152,6 +168,53 @@ __device__ __forceinline__ void st_cluster2(float* p, uint32_t rank, float2 v) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(p)), "r"(rank));
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
                : "memory");
+}
+
+// Shared-memory address of the same offset in cluster block `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t addr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(p)), "r"(rank));
+  return addr;
+}
+
+// Asynchronous store of two floats into another block's shared memory,
+// completing 8 transaction bytes on that block's mbarrier `rbar`.
+__device__ __forceinline__ void st_async2(uint32_t raddr, float2 v, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+      ::"r"(raddr), "f"(v.x), "f"(v.y), "r"(rbar)
+      : "memory");
+}
+
+// Bounded wait on an mbarrier phase whose transactions come from other
+// blocks of the cluster (acquire at cluster scope): false after ~2 s.
+__device__ __forceinline__ bool mbar_wait_cluster(unsigned long long* bar, uint32_t parity) {
+  constexpr uint32_t kSuspendHintNs = 10000000;
+  auto try_once = [&]() {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return done != 0;
+  };
+  if (try_once()) return true;
+  const long long start = clock64();
+  while (!try_once()) {
+    if (clock64() - start > kWaitCycles) return false;
+  }
+  return true;
+}
+
+// Heads g < 4 that cluster block `rank` leads (g mod S == rank).
+__device__ __forceinline__ int heads_led(int rank, int S) {
+  int n = 0;
+  #pragma unroll
+  for (int g = 0; g < kGroup; ++g) n += g % S == rank ? 1 : 0;
+  return n;
 }
 
 // Pull a 128-byte line into L2 (no register result; L2 is coherent, so this
@@ -502,19 +565,21 @@ __device__ __forceinline__ void cluster_merge(BlockSmem<kWarps, kStages>& sm,
                                               ClusterInbox& inbox, const WarpState& st,
                                               const LaneRoles& rl, int warp, int lane,
                                               float* out_kv, bool wait_always) {
-  static_assert(kWarps == kGroup, "one merging thread per (head, dim pair)");
+  static_assert(kWarps % kGroup == 0, "threads 0..127 hold one (head, dim pair) each");
   float M, L;
   float2 O;
   block_merge(sm, st, rl, warp, M, L, O);
   const int S = gridDim.x;
   const int rank = static_cast<int>(cluster_rank());
-  const int g = warp;               // thread t: head t / 32, dims 2 (t % 32), + 1
+  const int g = warp;               // thread t < 128: head t / 32, dims 2 (t % 32), + 1
   const int d0 = 2 * lane;
-  const int at = (g / S) * S + rank;
-  st_cluster2(&inbox.o[at][d0], g % S, O);
-  if (lane == 0) {
-    st_cluster(&inbox.m[at], g % S, M);
-    st_cluster(&inbox.l[at], g % S, L);
+  if (g < kGroup) {
+    const int at = (g / S) * S + rank;
+    st_cluster2(&inbox.o[at][d0], g % S, O);
+    if (lane == 0) {
+      st_cluster(&inbox.m[at], g % S, M);
+      st_cluster(&inbox.l[at], g % S, L);
+    }
   }
   cluster_arrive_release();
   if (rank >= kGroup) {   // leads no head
@@ -546,6 +611,78 @@ __device__ __forceinline__ void cluster_merge(BlockSmem<kWarps, kStages>& sm,
     const float inv = lw > 0.f ? 1.f / lw : 0.f;
     *reinterpret_cast<float2*>(out_kv + hg * kDim + d0) = make_float2(acc.x * inv, acc.y * inv);
   }
+}
+
+// The leader's inbox barrier, before any block of the cluster sends: thread 0
+// of a leader initialises it and arms it for the S parts of every head it
+// leads; then every thread of the cluster meets on the cluster barrier, so
+// no part can arrive at an uninitialised barrier. Called by every thread.
+__device__ __forceinline__ void async_inbox_setup(AsyncInbox& inbox) {
+  const int S = static_cast<int>(gridDim.x);
+  const int rank = static_cast<int>(cluster_rank());
+  const int led = heads_led(rank, S);
+  if (threadIdx.x == 0 && led > 0) {
+    mbar_init(&inbox.bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&inbox.bar, static_cast<uint32_t>(led * S) * kPartBytes);
+  }
+  cluster_arrive_release();
+  cluster_wait_acquire();
+}
+
+// Cluster merge without a closing cluster barrier: each block merges its
+// warps (block_merge), then threads 0..127 send the block's (o, m, l) part of
+// head t / 32 to the head's leader (block g mod S) with st.async stores; a
+// block that leads no head is then done. In a leader, warp w waits until the
+// parts of head rank + w S have landed and combines them into out_kv.
+template <int kWarps, int kStages>
+__device__ __forceinline__ void cluster_merge_async(BlockSmem<kWarps, kStages>& sm,
+                                                    AsyncInbox& inbox, const WarpState& st,
+                                                    const LaneRoles& rl, int warp, int lane,
+                                                    float* out_kv, int* err) {
+  static_assert(kWarps % kGroup == 0, "threads 0..127 hold one (head, dim pair) each");
+  float M, L;
+  float2 O;
+  block_merge(sm, st, rl, warp, M, L, O);
+  const int S = gridDim.x;
+  const int rank = static_cast<int>(cluster_rank());
+  const int d0 = 2 * lane;
+  if (warp < kGroup) {
+    const int g = warp;
+    const uint32_t dst = static_cast<uint32_t>(g % S);
+    const int at = (g / S) * S + rank;
+    const uint32_t rbar = cluster_addr(&inbox.bar, dst);
+    st_async2(cluster_addr(&inbox.o[at][d0], dst), O, rbar);
+    if (lane == 0) st_async2(cluster_addr(&inbox.ml[at], dst), make_float2(M, L), rbar);
+  }
+  if (rank >= kGroup) return;                  // leads no head
+  const int hg = rank + warp * S;             // head of this leader warp
+  if (hg >= kGroup) return;
+  if (!__all_sync(0xffffffffu, mbar_wait_cluster(&inbox.bar, 0))) {
+    if (lane == 0) set_error(err, kErrTimeout);
+    return;
+  }
+  const int base = warp * S;                  // its parts: slots base .. base + S - 1
+  const float2 mlp = lane < S ? inbox.ml[base + lane] : make_float2(-INFINITY, 0.f);
+  float mx = mlp.x;
+  #pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float w = mlp.x == -INFINITY ? 0.f : fast_exp2(mlp.x - mx);
+  float lw = w * mlp.y;
+  #pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+  float2 acc = make_float2(0.f, 0.f);
+  #pragma unroll
+  for (int p = 0; p < kMaxClusterSize; ++p) {
+    if (p < S) {
+      const float wp = __shfl_sync(0xffffffffu, w, p);
+      const float2 op = *reinterpret_cast<const float2*>(&inbox.o[base + p][d0]);
+      acc.x += wp * op.x;
+      acc.y += wp * op.y;
+    }
+  }
+  const float inv = lw > 0.f ? 1.f / lw : 0.f;
+  *reinterpret_cast<float2*>(out_kv + hg * kDim + d0) = make_float2(acc.x * inv, acc.y * inv);
 }
 
 // ---------------------------------------------------------------- dispatch order

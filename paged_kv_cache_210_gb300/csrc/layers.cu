@@ -58,7 +58,7 @@ struct LayersParams {
 };
 
 struct alignas(16) LayersSmem {
-  WideSmem blk;
+  BlockSmem<kClusterWarps, kWideStages> blk;
   ClusterInbox inbox;
   int ptab[kLayerTab];        // physical page of (layer j, page o of the block's range): j * span + o
   int flag;                   // thread 0's wait verdict for the block
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 4) decode_layers_kernel(co
   constexpr int kThreads = kWarps * 32;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   LayersSmem& ls = *reinterpret_cast<LayersSmem*>(smem_raw);
-  WideSmem& sm = ls.blk;
+  auto& sm = ls.blk;
 
   const int S = static_cast<int>(gridDim.x);
   const int split = blockIdx.x;

@@ -154,6 +154,7 @@ decode_kernel(const DecodeParams prm) {
   const int new_slot = (len - 1) % kPage;               // slot of the appended token
 
   WarpSmem<kStages>& ws = sm.warp[warp];
+  AsyncInbox& inbox = *reinterpret_cast<AsyncInbox*>(smem_raw + sizeof(Smem));
   // pages of this warp: page_begin + warp + 4 i
   const int mine = page_begin + warp < page_end
                        ? (page_end - (page_begin + warp) + kWarps - 1) / kWarps
@@ -163,6 +164,9 @@ decode_kernel(const DecodeParams prm) {
     for (int s = 0; s < kStages; ++s) mbar_init(&ws.bar[s], 1);
     fence_mbar_init();
   }
+  // the leaders' inbox barriers are armed before any part is sent (every
+  // block of the cluster takes this branch: it depends on the length only)
+  if (kCluster && n_splits > 1) async_inbox_setup(inbox);
   __syncthreads();   // the block-table row is in shared memory
 
   // Physical page of this warp's i-th page (i < mine <= 32) sits in lane i:
@@ -349,8 +353,9 @@ decode_kernel(const DecodeParams prm) {
   }
   if constexpr (kCluster) {
     if (n_splits > 1) {
-      cluster_merge(sm, *reinterpret_cast<ClusterInbox*>(smem_raw + sizeof(Smem)), st, rl, warp,
-                    lane, prm.out + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim, false);
+      cluster_merge_async(sm, inbox, st, rl, warp, lane,
+                          prm.out + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim,
+                          prm.err);
       return;
     }
   }
@@ -392,18 +397,20 @@ constexpr auto ticket_kernel = decode_kernel<kFused, false, kTicketWarps, kTicke
 template <bool kFused, bool kRope = false>
 constexpr auto narrow_kernel = decode_kernel<kFused, true, kClusterWarps, kNarrowStages, kRope>;
 template <bool kFused, bool kRope = false>
-constexpr auto wide_kernel = decode_kernel<kFused, true, kClusterWarps, kWideStages, kRope>;
+constexpr auto wide_kernel = decode_kernel<kFused, true, kWideWarps, kWideStages, kRope>;
 
 size_t smem_bytes(Shape shape) {
   switch (shape) {
-    case kNarrowShape: return sizeof(NarrowSmem) + sizeof(ClusterInbox);
-    case kWideShape: return sizeof(WideSmem) + sizeof(ClusterInbox);
+    case kNarrowShape: return sizeof(NarrowSmem) + sizeof(AsyncInbox);
+    case kWideShape: return sizeof(WideSmem) + sizeof(AsyncInbox);
     default: return sizeof(TicketSmem);
   }
 }
 
 int block_threads(Shape shape) {
-  return 32 * (shape == kTicketShape ? kTicketWarps : kClusterWarps);
+  return 32 * (shape == kTicketShape ? kTicketWarps
+               : shape == kWideShape ? kWideWarps
+                                     : kClusterWarps);
 }
 
 template <typename Kernel>
