@@ -454,17 +454,23 @@ int auto_chunk_pages(const pkv_device_figures& d, int batch) {
 }
 
 // The launch plan for a batch. Cluster plans when the library chooses: the
-// split count S (16, 8, 4, 2) and the block shape, from a sweep on a 152-SM
-// GB300 with full-length sequences (GB/s per 16-layer step):
+// split count S (16, 12, 8, 4, 2) and the block shape, from sweeps on a
+// 152-SM GB300 with full-length sequences (GB/s per 16-layer step; the
+// first sweep with the barrier-based cluster merge, the second with the
+// asynchronous one):
 //   batch 2:  narrow S = 16 (256 blocks) 1522; wide S = 16 1453; S = 8 1337;
+//             async: narrow S = 12 (192) 1720, S = 16 1574, S = 14 1495,
+//             S = 10 1565; wide S = 16 1677;
 //   batch 4:  narrow S = 8 (256) 2304; narrow S = 16 1404; wide S = 8 2015;
+//             async: narrow S = 8 2374, S = 7 2216, S = 6 2282; wide S = 16 1950;
 //   batch 8:  wide S = 8 (512) 3462; narrow S = 4 (256) 2680; wide S = 16 2016;
 //   batch 16: wide S = 4 (512) 4214; narrow S = 2 (256) 3187; wide S = 8 3443.
-// So: the narrow shape with the largest S whose blocks take at most 9/16 of
-// its resident slots (256 of 456, leaving room for the next launch), if that
-// S is at least 8; else the wide shape with the largest S <= 8 whose blocks
-// take at most 27/32 of its slots (512 of 608); else (large batches) the
-// ticket merge over page ranges.
+// So: the narrow shape with S = 16 or 12 when the blocks of two consecutive
+// launches fit its resident slots at once (the next layer's blocks then
+// become resident and prefetch during this one), else S = 8 when one
+// launch's blocks take at most 9/16 of the slots (256 of 456); else the wide
+// shape with the largest S <= 8 whose blocks take at most 27/32 of its slots
+// (512 of 608); else (large batches) the ticket merge over page ranges.
 pkv_plan plan_decode(const pkv_device_figures& d, int batch, int num_splits) {
   const int max_pages = d.max_seq_len / kPage;
   const long long narrow = static_cast<long long>(d.narrow_blocks_per_sm) * d.num_sms;
@@ -475,11 +481,15 @@ pkv_plan plan_decode(const pkv_device_figures& d, int batch, int num_splits) {
     auto usable = [&](int s) {
       return s <= d.max_cluster && s <= d.max_splits && s <= max_pages;
     };
-    for (int s = kMaxClusterSize; s >= 8 && !p.cluster; s /= 2) {
-      if (usable(s) && 16 * static_cast<long long>(batch) * kHkv * s <= 9 * narrow) {
+    for (const int s : {16, 12}) {
+      if (!p.cluster && usable(s) && 2 * static_cast<long long>(batch) * kHkv * s <= narrow) {
         p.cluster = s;
         p.shape = kNarrowShape;
       }
+    }
+    if (!p.cluster && usable(8) && 16 * static_cast<long long>(batch) * kHkv * 8 <= 9 * narrow) {
+      p.cluster = 8;
+      p.shape = kNarrowShape;
     }
     for (int s = 8; s >= 2 && !p.cluster; s /= 2) {
       if (usable(s) && 32 * static_cast<long long>(batch) * kHkv * s <= 27 * wide) {
