@@ -12,42 +12,43 @@
 // attention; here it reads keys through the block table, so a chunk can
 // continue a prompt whose earlier pages are already cached.
 //
-// Attention kernel, one CTA per (sequence, kv head, 32-token query tile),
+// Attention kernel, one CTA per (sequence, kv head, 64-token query tile),
 // warp-specialised:
-//  * the 128 rows of the MMA are the tile's 32 tokens x the 4 query heads
-//    of the kv head (row = token * 4 + head), so every K/V page tile is
-//    shared by the group, as in decode;
-//  * a loader warp brings Q (16 KiB) and per step 4 pages of K and of V
+//  * the 256 rows of the tile are its 64 tokens x the 4 query heads of the
+//    kv head (row = token * 4 + head), so every K/V page tile is shared by
+//    the group, as in decode; they are two row halves of 128, each the M of
+//    its own tensor-core products (M 128 is the largest a single CTA issues);
+//  * a loader warp brings Q (32 KiB) and per step 4 pages of K and of V
 //    (64 keys, 8 KiB each) by TMA tensor copies (cp.async.bulk.tensor) with
-//    the 128-byte swizzle, one page per lane, K in a 4-stage and V in a
-//    3-stage ring, so loads run two to three steps ahead; a page's tile is
-//    addressed by its id in the block table, nothing is gathered into a
-//    contiguous buffer;
-//  * a score warp (one thread) issues S = Q K^T (M 128, N 64, K 64) up to
-//    three steps ahead into three tensor-memory tiles, and a value warp (one
-//    thread) issues O += P V (M 128, N 64, K 64) into an FP32 accumulator
-//    that stays in tensor memory, as tcgen05.mma kind::f16 completed on
-//    mbarriers through tcgen05.commit, which also tell the loader when a
-//    stage is free and the score warp when a tile is;
-//  * eight softmax warps, two per tensor-memory lane quarter: each thread
-//    reads its half (32 keys) of its row's scores; online softmax in base 2
-//    whose max moves only when a row's max grows by more than 2^8 (then the
-//    two halves agree on it through shared memory, and O is rescaled in
-//    tensor memory by the warps whose rows grew); the probabilities go back
-//    into tensor memory over the scores they came from, as a BF16 high part
-//    (truncated) and a BF16 low part, and the value product reads them from
-//    there (A operand in tensor memory; ~16 significant bits for P from two
-//    MMAs). With three score tiles P is triple-buffered too: the softmax
-//    warps never wait for the previous value product, except to rescale O.
-//    An mbarrier with one arrival per softmax thread hands P over; the
-//    only block-level syncs in the step loop are two votes among the
-//    softmax warps;
-//  * tiles run heaviest first (the last tile of a prompt sees the most keys).
+//    the 128-byte swizzle, one page per lane, K in a 6-stage and V in a
+//    5-stage ring; a page's tile is addressed by its id in the block table,
+//    nothing is gathered into a contiguous buffer;
+//  * a score warp (one thread) issues S = Q K^T (two M 128 x N 64 x K 64
+//    products, one per row half) up to three steps ahead into three pairs of
+//    tensor-memory tiles, and a value warp (one thread) issues O += P V (two
+//    M 128 x N 64 x K 64 products) into FP32 accumulators that stay in
+//    tensor memory, as tcgen05.mma kind::f16 completed on mbarriers through
+//    tcgen05.commit, which also tell the loader when a stage is free and the
+//    score warp when a tile is;
+//  * eight softmax warps, one per (tensor-memory lane quarter, row half):
+//    each thread owns one row and reads all 64 keys of the step, so no
+//    thread needs another's maximum or sum and the step loop has no block
+//    barrier; online softmax in base 2 whose max moves only when the row's
+//    max grows by more than 2^8 (O is then rescaled in tensor memory by that
+//    thread); the probabilities go back into tensor memory over the scores
+//    they came from, as a BF16 high part (truncated) and a BF16 low part,
+//    and the value product reads them from there (A operand in tensor
+//    memory; ~16 significant bits for P from two MMAs). With three score
+//    tiles P is triple-buffered too: the softmax warps wait for a value
+//    product only to rescale O. An mbarrier with one arrival per softmax
+//    thread hands P over;
+//  * one CTA per SM (it holds all 512 tensor-memory columns); tiles run
+//    heaviest first (the last tile of a prompt sees the most keys).
 //
-// What bounds it (measured on an earlier version): per step a softmax
-// thread spent ~1,100 cycles on its 32 exponentials and the surrounding
-// arithmetic, so the step, not the tensor cores, sets the pace; 128-row x
-// 64-key steps keep every product small (M 128, N 64).
+// What bounds it (measured with clock counters in an instrumented copy):
+// a step takes ~2,100 cycles, set by the loader: each TMA tensor copy of a
+// 2 KiB page takes the copy engine ~250 cycles, eight per step; the softmax
+// threads need ~1,350 cycles of a step.
 //
 // Every mbarrier wait is bounded (about two seconds of SM clock); a timeout
 // sets the error flag, the CTA waits (bounded) for its own copies and
@@ -69,39 +70,45 @@ using namespace pkv_dev;
 
 namespace {
 
-constexpr int kTileTokens = 32;                      // query tokens per CTA
-constexpr int kRows = kTileTokens * kGroup;          // 128: the MMA's M
+constexpr int kRowHalves = 2;                        // MMAs of M = 128 rows per CTA
+constexpr int kHalfRows = 128;                       // rows of one MMA (its M): 32 tokens
+constexpr int kRows = kRowHalves * kHalfRows;        // 256 rows: token x head
+constexpr int kTileTokens = kRows / kGroup;          // 64 query tokens per CTA
+constexpr int kCtasPerSm = 2 / kRowHalves;           // tensor memory: 256 columns per row half
 constexpr int kStepKeys = 64;                        // keys per step: the S MMA's N
 constexpr int kStepPages = kStepKeys / kPage;        // 4
-constexpr int kSoftmaxWarps = 8;                     // two per tensor-memory lane quarter
+constexpr int kSoftmaxWarps = 4 * kRowHalves;        // one per (lane quarter, row half)
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kLoadWarp = kSoftmaxWarps;             // TMA copies
 constexpr int kScoreWarp = kSoftmaxWarps + 1;        // S = Q K^T products
 constexpr int kValueWarp = kSoftmaxWarps + 2;        // O += P V products
 constexpr int kThreads = kSoftmaxThreads + 96;
-constexpr int kKStages = 4;                          // K ring
-constexpr int kVStages = 3;                          // V ring
+constexpr int kKStages = kRowHalves == 2 ? 6 : 4;     // K ring
+constexpr int kVStages = kRowHalves == 2 ? 5 : 3;     // V ring
 constexpr int kSTiles = 3;                           // score (then P) tiles in tensor memory
-constexpr uint32_t kTmemCols = 256;                  // S/P tiles: 0..191, O: 192..255
-constexpr uint32_t kTmemO = kSTiles * 64;
+constexpr uint32_t kTmemCols = 256 * kRowHalves;     // S/P tiles, then O
+constexpr uint32_t kTmemO = kSTiles * kRowHalves * kStepKeys;   // O of row half h at + 64 h
 constexpr float kRescaleLog2 = 8.f;                  // lazy max: p <= 2^8
 
 struct PrefillSmem {                                 // every tile 1024-byte aligned
-  uint8_t q[kRows * kRowBytes];                      // 16 KiB
-  uint8_t k[kKStages][kStepKeys * kRowBytes];        // 4 x 8 KiB
-  uint8_t v[kVStages][kStepKeys * kRowBytes];        // 3 x 8 KiB
+  uint8_t q[kRows * kRowBytes];                      // 32 KiB
+  uint8_t k[kKStages][kStepKeys * kRowBytes];        // 6 x 8 KiB
+  uint8_t v[kVStages][kStepKeys * kRowBytes];        // 5 x 8 KiB
   unsigned long long bar_q, bar_k[kKStages], bar_v[kVStages], bar_s[kSTiles], bar_p[kSTiles];
   unsigned long long bar_o[kSTiles];   // P(j) V(j) (and every earlier product) done, per tile
   unsigned long long p_free[kSTiles];                // tile (S, then P) read by its value product
   unsigned long long k_free[kKStages], v_free[kVStages];   // stage read by its product
   uint32_t tmem_base;
   int abort_flag;
-  float lsum[2][kRows];                              // the two halves' row sums
-  float pmax[2][kRows];                              // the two halves' step maxima
   int pages[kMaxPages];                              // block-table row, -1 = not loadable
 };
-static_assert(offsetof(PrefillSmem, k) % 1024 == 0 && offsetof(PrefillSmem, v) % 1024 == 0,
-              "swizzled tiles start on 1024-byte boundaries");
+static_assert(offsetof(PrefillSmem, k) % 1024 == 0 && offsetof(PrefillSmem, v) % 1024 == 0 &&
+                  (kHalfRows * kRowBytes) % 1024 == 0,
+              "swizzled tiles (and Q's second row half) start on 1024-byte boundaries");
+// kCtasPerSm CTAs share an SM's 512 tensor-memory columns (the registers
+// of their threads admit no more)
+static_assert(kCtasPerSm * (sizeof(PrefillSmem) + 2048) <= 228 * 1024,
+              "shared memory holds kCtasPerSm prefill CTAs per SM");
 constexpr size_t kSmemBytes = sizeof(PrefillSmem) + 1024;   // + room to align the base
 
 struct PrefillParams {
@@ -229,25 +236,6 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Barrier among the softmax warps that also ORs a flag over them.
-__device__ __forceinline__ bool softmax_warps_any(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(pred ? 1u : 0u), "n"(kSoftmaxThreads)
-      : "memory");
-  return r != 0;
-}
-
-// Barrier among the softmax warps only (named barrier 1).
-__device__ __forceinline__ void softmax_warps_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-}
-
 // Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
 // and stride byte offsets (>> 4), descriptor version 1, layout SWIZZLE_128B.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -306,7 +294,7 @@ __global__ void __launch_bounds__(128) prefill_fill_kernel(
 }
 
 // ---------------------------------------------------------------- attention
-__global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_attention_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v, const PrefillParams prm) {
   extern __shared__ uint8_t smem_raw[];
@@ -458,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
       int issued = 0;
       bool ok = true;
       if (scores) {
-        const uint32_t idesc_s = instr_desc(kRows, kStepKeys, false);
+        const uint32_t idesc_s = instr_desc(kHalfRows, kStepKeys, false);
         const uint64_t q_desc = smem_desc_sw128(smem_u32(sm.q), 16, 1024);
         ok = mbar_wait(&sm.bar_q, 0);
         for (int j = 0; ok && j < n_steps; ++j) {
@@ -472,17 +460,22 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
           }
           tc_fence_after();
           const uint64_t k_desc = smem_desc_sw128(smem_u32(sm.k[j % kKStages]), 16, 1024);
-          // the descriptor's start address counts 16-byte units: + bytes >> 4
+          // the descriptor's start address counts 16-byte units: + bytes >> 4;
+          // row half h reads Q rows 128 h .. 128 h + 127 into its own S tile
           #pragma unroll
-          for (int kk = 0; kk < kDim / 16; ++kk)
-            mma_bf16(tmem + (j % kSTiles) * kStepKeys, q_desc + kk * 2, k_desc + kk * 2, idesc_s,
-                     kk > 0);
+          for (int h = 0; h < kRowHalves; ++h) {
+            #pragma unroll
+            for (int kk = 0; kk < kDim / 16; ++kk)
+              mma_bf16(tmem + ((j % kSTiles) * kRowHalves + h) * kStepKeys,
+                       q_desc + h * (kHalfRows * kRowBytes >> 4) + kk * 2, k_desc + kk * 2,
+                       idesc_s, kk > 0);
+          }
           mma_commit(&sm.bar_s[j % kSTiles]);
           mma_commit(&sm.k_free[j % kKStages]);
           ++issued;
         }
       } else {
-        const uint32_t idesc_o = instr_desc(kRows, kDim, true);
+        const uint32_t idesc_o = instr_desc(kHalfRows, kDim, true);
         for (int j = 0; ok && j < n_steps; ++j) {
           // O += P(j) V(j): P from tensor memory (tile j % 3: high part in
           // columns 0..31, low part in 32..63, 16 keys per 8 columns), once
@@ -494,15 +487,19 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
           }
           tc_fence_after();
           const uint64_t v_desc = smem_desc_sw128(smem_u32(sm.v[j % kVStages]), 8192, 1024);
-          const uint32_t p_tile = tmem + (j % kSTiles) * kStepKeys;
           #pragma unroll
-          for (int kk = 0; kk < kStepKeys / 16; ++kk)
-            mma_bf16_tmem_a(tmem + kTmemO, p_tile + kk * 8, v_desc + kk * (16 * kRowBytes >> 4),
-                            idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-          #pragma unroll
-          for (int kk = 0; kk < kStepKeys / 16; ++kk)
-            mma_bf16_tmem_a(tmem + kTmemO, p_tile + 32 + kk * 8,
-                            v_desc + kk * (16 * kRowBytes >> 4), idesc_o, 1u);
+          for (int h = 0; h < kRowHalves; ++h) {
+            const uint32_t p_tile = tmem + ((j % kSTiles) * kRowHalves + h) * kStepKeys;
+            const uint32_t o_tile = tmem + kTmemO + h * kDim;
+            #pragma unroll
+            for (int kk = 0; kk < kStepKeys / 16; ++kk)
+              mma_bf16_tmem_a(o_tile, p_tile + kk * 8, v_desc + kk * (16 * kRowBytes >> 4),
+                              idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            #pragma unroll
+            for (int kk = 0; kk < kStepKeys / 16; ++kk)
+              mma_bf16_tmem_a(o_tile, p_tile + 32 + kk * 8,
+                              v_desc + kk * (16 * kRowBytes >> 4), idesc_o, 1u);
+          }
           mma_commit(&sm.bar_o[j % kSTiles]);
           mma_commit(&sm.v_free[j % kVStages]);
           mma_commit(&sm.p_free[j % kSTiles]);
@@ -526,54 +523,60 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int half = warp >> 2;                         // key columns 32*half .. +31
-    const int r = (warp & 3) * 32 + (tid & 31);         // the MMA row = tensor-memory lane
-    const int tok = r >> 2;                             // token of the tile, head r & 3
+    // One thread per row: warp w reads tensor-memory lanes 32 (w % 4) ..
+    // + 31 of row half w / 4, all 64 keys of the step, so no thread needs
+    // another's maximum or sum and the step loop has no block barrier.
+    const int rh = warp >> 2;                           // row half: tokens 32 rh .. 32 rh + 31
+    const int r = (warp & 3) * 32 + (tid & 31);         // its MMA row = tensor-memory lane
+    const int tok = (rh * kHalfRows + r) >> 2;          // token of the tile, head r & 3
+    const uint32_t s_col = rh * kStepKeys;              // the row half's S/P tile columns
+    const uint32_t o_col = kTmemO + rh * kDim;          // ... and its O columns
     const int pos = p_first + min(tok, t_valid - 1);    // rows past the chunk mirror its last token
     const float c = 1.4426950408889634f * 0.125f;       // log2(e) / sqrt(64)
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float m_run = -INFINITY, l_half = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_steps; ++j) {
-      // (a failed wait is voted on with the other softmax threads below, so
-      // that every one of them leaves the loop at the same step)
-      bool failed = *abort_flag != 0 ||
-                    !mbar_wait(&sm.bar_s[j % kSTiles], (j / kSTiles) & 1);
+      // one verdict per warp (the tensor-memory accesses below are warp-wide)
+      if (!__all_sync(0xffffffffu, *abort_flag == 0 &&
+                                       mbar_wait(&sm.bar_s[j % kSTiles], (j / kSTiles) & 1))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      uint32_t sv[32];                                   // this half's 32 keys of the step
-      tmem_ld32(tmem + lane_addr + (j % kSTiles) * kStepKeys + half * 32, sv);
-
-      const int key0 = j * kStepKeys + half * 32;
-      if (key0 + 31 > p_first) {                         // some key hidden from some row
+      const uint32_t st_tile = tmem + lane_addr + (j % kSTiles) * kRowHalves * kStepKeys + s_col;
+      uint32_t sv[64];                                   // the row's 64 keys of the step
+      {
+        uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+        uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+        tmem_ld32(st_tile, a);
+        tmem_ld32(st_tile + 32, b);
+      }
+      const int key0 = j * kStepKeys;
+      if (key0 + kStepKeys - 1 > p_first) {              // some key hidden from some row
         #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 64; ++i)
           if (key0 + i > pos) sv[i] = __float_as_uint(-INFINITY);
       }
       float mx8[8];
       #pragma unroll
       for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(sv[e]);
       #pragma unroll
-      for (int i = 8; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
-      const float half_max = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      // The max used for the exponentials moves only when a row's max grows
-      // by more than 2^8. Usually no row's does; when one does, the two
-      // halves of every row agree on the step's row max through shared memory.
+      for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
+      const float m_step = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
+      // The max used for the exponentials moves only when the row's max
+      // grows by more than 2^8 (so every p <= 2^8).
       float alpha = 1.f;
-      bool grow = false;
-      if (softmax_warps_any(half_max * c > m_run + kRescaleLog2)) {
-        sm.pmax[half][r] = half_max;
-        softmax_warps_sync();
-        const float m_step = fmaxf(sm.pmax[0][r], sm.pmax[1][r]) * c;
-        grow = m_step > m_run + kRescaleLog2;
-        if (grow) {
-          alpha = fast_exp2(m_run - m_step);
-          m_run = m_step;
-          l_half *= alpha;
-        }
+      const bool grow = m_step > m_run + kRescaleLog2;
+      if (grow) {
+        alpha = fast_exp2(m_run - m_step);
+        m_run = m_step;
+        l_run *= alpha;
       }
-      // this half's 32 probabilities, their sum, BF16 high / low parts
-      uint32_t hi[16], lo[16];
+      // the 64 probabilities, their sum, BF16 high / low parts, in two
+      // halves of 32 keys written over the scores they came from (high
+      // parts in columns 0..31, low parts in 32..63)
       {
         const float2 c2 = make_float2(c, c);
         const float2 nm2 = make_float2(-m_run, -m_run);
@@ -581,39 +584,53 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
         #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
-                                      c2, nm2);
-          const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          acc[(i >> 1) & 3] = __fadd2_rn(acc[(i >> 1) & 3], pp);
-          const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
-          hi[i / 2] = __byte_perm(b0, b1, 0x7632);
-          const float2 h = make_float2(__uint_as_float(b0 & 0xffff0000u),
-                                       __uint_as_float(b1 & 0xffff0000u));
-          const float2 rest = __ffma2_rn(h, neg1, pp);
-          lo[i / 2] = float2_to_bf16x2(rest.x, rest.y);
+        for (int kh = 0; kh < 2; ++kh) {
+          uint32_t hi[16], lo[16];
+          #pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int k = kh * 32 + i;
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), c2, nm2);
+            const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            acc[(i >> 1) & 3] = __fadd2_rn(acc[(i >> 1) & 3], pp);
+            const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
+            hi[i / 2] = __byte_perm(b0, b1, 0x7632);
+            const float2 h = make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                         __uint_as_float(b1 & 0xffff0000u));
+            const float2 rest = __ffma2_rn(h, neg1, pp);
+            lo[i / 2] = float2_to_bf16x2(rest.x, rest.y);
+          }
+          // the scores of both halves are in registers already: P may overwrite them
+          tmem_st16(st_tile + kh * 16, hi);
+          tmem_st16(st_tile + 32 + kh * 16, lo);
         }
         const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        l_half += a.x + a.y;
+        l_run += a.x + a.y;
       }
 
-      // a row that grew its max rescales O, once P(j - 1) V(j - 1) is done
-      // (P(j) V(j) cannot start before this thread hands over P(j))
+      // a row that grew its max rescales its O, once P(j - 1) V(j - 1) is
+      // done (P(j) V(j) cannot start before this thread hands over P(j))
+      bool failed = false;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        failed |= !mbar_wait(&sm.bar_o[(j - 1) % kSTiles], ((j - 1) / kSTiles) & 1);
+        failed = !__all_sync(0xffffffffu,
+                             mbar_wait(&sm.bar_o[(j - 1) % kSTiles], ((j - 1) / kSTiles) & 1));
         tc_fence_after();
         if (!failed) {
-          uint32_t ov[32];
-          tmem_ld32(tmem + lane_addr + kTmemO + half * 32, ov);
           #pragma unroll
-          for (int d = 0; d < 32; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
-          tmem_st32(tmem + lane_addr + kTmemO + half * 32, ov);
+          for (int dh = 0; dh < 2; ++dh) {
+            uint32_t ov[32];
+            tmem_ld32(tmem + lane_addr + o_col + dh * 32, ov);
+            #pragma unroll
+            for (int d = 0; d < 32; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
+            tmem_st32(tmem + lane_addr + o_col + dh * 32, ov);
+          }
         }
       }
       // V rows the product must not see: keys past the tile's last token and
-      // pages not loaded (zero, so that p = 0 times them stays 0)
-      if (any_bad_page || (j + 1) * kStepKeys > n_keys) {
-        if (mbar_wait(&sm.bar_v[j % kVStages], (j / kVStages) & 1)) {
+      // pages not loaded (zero, so that p = 0 times them stays 0); every
+      // softmax thread zeroes its share before it hands over P(j)
+      if (!failed && (any_bad_page || (j + 1) * kStepKeys > n_keys)) {
+        if (__all_sync(0xffffffffu, mbar_wait(&sm.bar_v[j % kVStages], (j / kVStages) & 1))) {
           for (int idx = tid; idx < kStepKeys * 8; idx += kSoftmaxThreads) {
             const int key_row = idx >> 3;
             const int key = j * kStepKeys + key_row;
@@ -627,41 +644,35 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_attention_kernel(
           failed = true;
         }
       }
-      // both halves of every row have read S(j): P(j) may overwrite it
-      tc_fence_before();
-      if (softmax_warps_any(failed)) {
+      if (failed) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const uint32_t p_tile = tmem + lane_addr + (j % kSTiles) * kStepKeys;
-      tmem_st16(p_tile + half * 16, hi);
-      tmem_st16(p_tile + 32 + half * 16, lo);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&sm.bar_p[j % kSTiles]);
     }
     if (!ok) {
       *abort_flag = 1;
-      if (tid == 0) set_error(prm.err, PKV_DEV_ERR_TIMEOUT);
+      set_error(prm.err, PKV_DEV_ERR_TIMEOUT);
     }
-    // the two halves' sums of each row meet in shared memory
-    sm.lsum[half][r] = l_half;
-    softmax_warps_sync();
     if (ok && !*abort_flag &&
         mbar_wait(&sm.bar_o[(n_steps - 1) % kSTiles], ((n_steps - 1) / kSTiles) & 1)) {
       tc_fence_after();
-      uint32_t ov[32];
-      tmem_ld32(tmem + lane_addr + kTmemO + half * 32, ov);
-      if (tok < t_valid) {
-        const float inv = 1.f / (sm.lsum[0][r] + sm.lsum[1][r]);
-        float* dst = prm.out + ((static_cast<size_t>(row0) + tile * kTileTokens + tok) * kHq +
-                                g * kGroup + (r & 3)) * kDim + half * 32;
-        #pragma unroll
-        for (int d = 0; d < 32; d += 4)
-          *reinterpret_cast<float4*>(dst + d) =
-              make_float4(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv,
-                          __uint_as_float(ov[d + 2]) * inv, __uint_as_float(ov[d + 3]) * inv);
+      const float inv = 1.f / l_run;
+      float* dst = prm.out + ((static_cast<size_t>(row0) + tile * kTileTokens + tok) * kHq +
+                              g * kGroup + (r & 3)) * kDim;
+      #pragma unroll
+      for (int dh = 0; dh < 2; ++dh) {
+        uint32_t ov[32];
+        tmem_ld32(tmem + lane_addr + o_col + dh * 32, ov);
+        if (tok < t_valid) {
+          #pragma unroll
+          for (int d = 0; d < 32; d += 4)
+            *reinterpret_cast<float4*>(dst + dh * 32 + d) =
+                make_float4(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv,
+                            __uint_as_float(ov[d + 2]) * inv, __uint_as_float(ov[d + 3]) * inv);
+        }
       }
     }
   }
