@@ -20,16 +20,18 @@
 //    its own tensor-core products (M 128 is the largest a single CTA issues);
 //  * a loader warp brings Q (32 KiB) and per step 4 pages of K and of V
 //    (64 keys, 8 KiB each) by TMA tensor copies (cp.async.bulk.tensor) with
-//    the 128-byte swizzle, one page per lane, K in a 6-stage and V in a
-//    5-stage ring; a page's tile is addressed by its id in the block table,
-//    nothing is gathered into a contiguous buffer;
+//    the 128-byte swizzle, K in a 6-stage and V in a 5-stage ring, all 8
+//    pages of a step in one round (one wait for the free stages, one copy
+//    instruction across lanes 0..7); a page's tile is addressed by its id in
+//    the block table, nothing is gathered into a contiguous buffer;
 //  * a score warp (one thread) issues S = Q K^T (two M 128 x N 64 x K 64
-//    products, one per row half) up to three steps ahead into three pairs of
-//    tensor-memory tiles, and a value warp (one thread) issues O += P V (two
-//    M 128 x N 64 x K 64 products) into FP32 accumulators that stay in
-//    tensor memory, as tcgen05.mma kind::f16 completed on mbarriers through
+//    products, one per row half, their K 16 slices interleaved) up to three
+//    steps ahead into three pairs of tensor-memory tiles, and two value
+//    warps (one thread each, one per row half) issue O += P V (M 128 x N 64
+//    x K 64, high and low parts) into FP32 accumulators that stay in tensor
+//    memory, as tcgen05.mma kind::f16 completed on mbarriers through
 //    tcgen05.commit, which also tell the loader when a stage is free and the
-//    score warp when a tile is;
+//    score warp when a tile is (the value barriers count both halves);
 //  * eight softmax warps, one per (tensor-memory lane quarter, row half):
 //    each thread owns one row and reads all 64 keys of the step, so no
 //    thread needs another's maximum or sum and the step loop has no block
@@ -46,9 +48,14 @@
 //    heaviest first (the last tile of a prompt sees the most keys).
 //
 // What bounds it (measured with clock counters in an instrumented copy):
-// a step takes ~2,100 cycles, set by the loader: each TMA tensor copy of a
-// 2 KiB page takes the copy engine ~250 cycles, eight per step; the softmax
-// threads need ~1,350 cycles of a step.
+// a step takes ~1,850 cycles. A copy round costs the loader warp ~1,800
+// cycles (the free-stage waits ~400, the 8-lane copy instruction ~1,300:
+// the SM's copy engine takes a page tile at a time), so K(j) lands just as
+// the score product wants it; the softmax threads need ~1,350 cycles of a
+// step and wait the rest for S. With the copies out of the way (one 8 KiB
+// box per tensor and step, timed in an experiment) the step is ~1,650
+// cycles, set by the hand-offs between the warps: each mbarrier wait that
+// ends a dependency costs its waiter ~200-500 cycles.
 //
 // Every mbarrier wait is bounded (about two seconds of SM clock); a timeout
 // sets the error flag, the CTA waits (bounded) for its own copies and
@@ -81,8 +88,8 @@ constexpr int kSoftmaxWarps = 4 * kRowHalves;        // one per (lane quarter, r
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kLoadWarp = kSoftmaxWarps;             // TMA copies
 constexpr int kScoreWarp = kSoftmaxWarps + 1;        // S = Q K^T products
-constexpr int kValueWarp = kSoftmaxWarps + 2;        // O += P V products
-constexpr int kThreads = kSoftmaxThreads + 96;
+constexpr int kValueWarp0 = kSoftmaxWarps + 2;       // O += P V products, one warp per row half
+constexpr int kThreads = kSoftmaxThreads + 64 + 32 * kRowHalves;
 constexpr int kKStages = kRowHalves == 2 ? 6 : 4;     // K ring
 constexpr int kVStages = kRowHalves == 2 ? 5 : 3;     // V ring
 constexpr int kSTiles = 3;                           // score (then P) tiles in tensor memory
@@ -352,10 +359,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_attention_kernel
     // one per tile as well: the softmax warps may be two value products
     // ahead, and a parity wait on a single barrier could then return for an
     // older product
-    for (int i = 0; i < kSTiles; ++i) mbar_init(&sm.bar_o[i], 1);
-    for (int i = 0; i < kSTiles; ++i) mbar_init(&sm.p_free[i], 1);
+    // the value barriers complete once both row halves' issuers committed
+    for (int i = 0; i < kSTiles; ++i) mbar_init(&sm.bar_o[i], kRowHalves);
+    for (int i = 0; i < kSTiles; ++i) mbar_init(&sm.p_free[i], kRowHalves);
     for (int i = 0; i < kKStages; ++i) mbar_init(&sm.k_free[i], 1);
-    for (int i = 0; i < kVStages; ++i) mbar_init(&sm.v_free[i], 1);
+    for (int i = 0; i < kVStages; ++i) mbar_init(&sm.v_free[i], kRowHalves);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -368,8 +376,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_attention_kernel
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ copy engine
-    // Lanes 0..3 each copy one page of a step; lane 0 waits for the stage to
-    // be free (its product committed) and sets the expected bytes first.
     const int lane = lane_of(tid);
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
@@ -378,47 +384,49 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_attention_kernel
       mbar_arrive_expect_tx(&sm.bar_q, kRows * kRowBytes);
       tma_load_3d(sm.q, &tmap_q, 0, g * kGroup, row0 + tile * kTileTokens, &sm.bar_q);
     }
-    int k_issued = 0, v_issued = 0;
-    auto issue_tile = [&](uint8_t* dst, const CUtensorMap* map, unsigned long long* bar,
-                          unsigned long long* free_bar, int j, int stages) -> bool {
-      bool ok = true;
+    // One round per step: lane 0 waits until the step's K and V stages are
+    // free (their products committed) and sets both expected byte counts,
+    // then lanes 0..3 copy the step's 4 K pages and lanes 4..7 its 4 V pages
+    // in one instruction. A round costs the warp a few hundred cycles
+    // whatever it copies, so the copies of a step share one.
+    int issued = 0;
+    bool ok = true;
+    for (int j = 0; j < n_steps; ++j) {
+      const int ks = j % kKStages, vs = j % kVStages;
+      bool good = true;
       if (lane == 0) {
-        if (j >= stages) ok = mbar_wait(free_bar, ((j - stages) / stages) & 1);
-        if (ok) {
+        good = *abort_flag == 0;
+        if (good && j >= kKStages) good = mbar_wait(&sm.k_free[ks], ((j - kKStages) / kKStages) & 1);
+        if (good && j >= kVStages) good = mbar_wait(&sm.v_free[vs], ((j - kVStages) / kVStages) & 1);
+        if (good) {
           int valid = 0;
           for (int q = 0; q < kStepPages; ++q) {
             const int lp = j * kStepPages + q;
             valid += (lp < n_pages && sm.pages[lp] >= 0) ? 1 : 0;
           }
-          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(valid) * kPage * kRowBytes);
+          const uint32_t bytes = static_cast<uint32_t>(valid) * kPage * kRowBytes;
+          mbar_arrive_expect_tx(&sm.bar_k[ks], bytes);
+          mbar_arrive_expect_tx(&sm.bar_v[vs], bytes);
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (ok && lane < kStepPages) {
-        const int lp = j * kStepPages + lane;
-        const int page = lp < n_pages ? sm.pages[lp] : -1;
-        // the pool seen as rows of 64 dims: (page, kv head, token) -> row
-        if (page >= 0)
-          tma_load_2d(dst + lane * kPage * kRowBytes, map, 0, (page * kHkv + g) * kPage, bar);
-      }
-      __syncwarp();
-      return ok;
-    };
-    bool ok = true;
-    for (int j = 0; ok && j < n_steps; ++j) {
-      if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) {   // one view per warp
+      if (!__shfl_sync(0xffffffffu, good ? 1 : 0, 0)) {
         ok = false;
         break;
       }
-      ok = issue_tile(sm.k[j % kKStages], &tmap_k, &sm.bar_k[j % kKStages],
-                      &sm.k_free[j % kKStages], j, kKStages);
-      if (!ok) break;
-      ++k_issued;
-      ok = issue_tile(sm.v[j % kVStages], &tmap_v, &sm.bar_v[j % kVStages],
-                      &sm.v_free[j % kVStages], j, kVStages);
-      if (!ok) break;
-      ++v_issued;
+      if (lane < 2 * kStepPages) {
+        const bool is_v = lane >= kStepPages;
+        const int q = lane % kStepPages;
+        const int lp = j * kStepPages + q;
+        const int page = lp < n_pages ? sm.pages[lp] : -1;
+        // the pool seen as rows of 64 dims: (page, kv head, token) -> row
+        if (page >= 0)
+          tma_load_2d((is_v ? sm.v[vs] : sm.k[ks]) + q * kPage * kRowBytes, is_v ? &tmap_v : &tmap_k,
+                      0, (page * kHkv + g) * kPage, is_v ? &sm.bar_v[vs] : &sm.bar_k[ks]);
+      }
+      __syncwarp();
+      ++issued;
     }
+    const int k_issued = issued, v_issued = issued;
     if (lane == 0) {
       if (!ok) {
         *abort_flag = 1;
@@ -436,13 +444,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_attention_kernel
         if (uses > 0) mbar_wait(&sm.bar_v[st], (uses - 1) & 1);
       }
     }
-  } else if (warp == kScoreWarp || warp == kValueWarp) {
+  } else if (warp == kScoreWarp || (warp >= kValueWarp0 && warp < kValueWarp0 + kRowHalves)) {
     // ------------------------------------------------------------ tensor cores
-    // Two issuing threads, one for the score products and one for the value
-    // products (a tcgen05.commit tracks the products of its own thread), so
-    // scores can run ahead while the value products wait for P.
+    // Three issuing threads: one for the score products and one per row half
+    // for the value products (a tcgen05.commit tracks the products of its
+    // own thread), so scores can run ahead while the value products wait for
+    // P, and the two halves' value products, each a chain of accumulations
+    // into its own O, overlap in the tensor pipe.
     if (lane_of(tid) == 0) {
       const bool scores = warp == kScoreWarp;
+      const int half = warp - kValueWarp0;   // the value issuer's row half
       int issued = 0;
       bool ok = true;
       if (scores) {
@@ -462,10 +473,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_attention_kernel
           const uint64_t k_desc = smem_desc_sw128(smem_u32(sm.k[j % kKStages]), 16, 1024);
           // the descriptor's start address counts 16-byte units: + bytes >> 4;
           // row half h reads Q rows 128 h .. 128 h + 127 into its own S tile
+          // the row halves' accumulations interleaved: two independent
+          // chains keep the tensor pipe busy while one waits on its operand
           #pragma unroll
-          for (int h = 0; h < kRowHalves; ++h) {
+          for (int kk = 0; kk < kDim / 16; ++kk) {
             #pragma unroll
-            for (int kk = 0; kk < kDim / 16; ++kk)
+            for (int h = 0; h < kRowHalves; ++h)
               mma_bf16(tmem + ((j % kSTiles) * kRowHalves + h) * kStepKeys,
                        q_desc + h * (kHalfRows * kRowBytes >> 4) + kk * 2, k_desc + kk * 2,
                        idesc_s, kk > 0);
@@ -487,19 +500,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_attention_kernel
           }
           tc_fence_after();
           const uint64_t v_desc = smem_desc_sw128(smem_u32(sm.v[j % kVStages]), 8192, 1024);
+          // this issuer's row half: P tile columns 0..31 high parts, 32..63 low
+          const uint32_t p_tile = tmem + ((j % kSTiles) * kRowHalves + half) * kStepKeys;
+          const uint32_t o_tile = tmem + kTmemO + half * kDim;
           #pragma unroll
-          for (int h = 0; h < kRowHalves; ++h) {
-            const uint32_t p_tile = tmem + ((j % kSTiles) * kRowHalves + h) * kStepKeys;
-            const uint32_t o_tile = tmem + kTmemO + h * kDim;
-            #pragma unroll
-            for (int kk = 0; kk < kStepKeys / 16; ++kk)
-              mma_bf16_tmem_a(o_tile, p_tile + kk * 8, v_desc + kk * (16 * kRowBytes >> 4),
-                              idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-            #pragma unroll
-            for (int kk = 0; kk < kStepKeys / 16; ++kk)
-              mma_bf16_tmem_a(o_tile, p_tile + 32 + kk * 8,
-                              v_desc + kk * (16 * kRowBytes >> 4), idesc_o, 1u);
-          }
+          for (int kk = 0; kk < kStepKeys / 16; ++kk)
+            mma_bf16_tmem_a(o_tile, p_tile + kk * 8, v_desc + kk * (16 * kRowBytes >> 4),
+                            idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          #pragma unroll
+          for (int kk = 0; kk < kStepKeys / 16; ++kk)
+            mma_bf16_tmem_a(o_tile, p_tile + 32 + kk * 8,
+                            v_desc + kk * (16 * kRowBytes >> 4), idesc_o, 1u);
           mma_commit(&sm.bar_o[j % kSTiles]);
           mma_commit(&sm.v_free[j % kVStages]);
           mma_commit(&sm.p_free[j % kSTiles]);
