@@ -174,22 +174,25 @@ decode_kernel(const DecodeParams prm) {
   int my_phys = -1;
   if (lane < mine) my_phys = sm.pages[page_begin + warp + kWarps * lane];
 
-  // Copy engine: rows of this warp's i-th page into stage i % kStages (lane 0
-  // issues). In the fused step the appended row is not copied from the pool.
+  // Copy engine: rows of this warp's i-th page into stage i % kStages. A copy
+  // instruction costs its warp a few hundred cycles whatever its size, so the
+  // K and V copies go out together from lanes 0 and 1. In the fused step the
+  // appended row is not copied from the pool.
   auto issue_copy = [&](int i, int stage, int phys) {
-    if (lane != 0) return;
+    if (lane > 1) return;   // lane 0 copies the K rows, lane 1 the V rows, in one instruction
     const int lp = page_begin + warp + kWarps * i;
     const bool ok = phys >= 0 && phys < prm.num_pages;
     int rows = lp == last_page ? len - lp * kPage : kPage;
     if (kFused && lp == last_page) rows = new_slot;     // the new row comes from k/v
-    if (!ok) set_error(prm.err, kErrPage);
+    if (!ok && lane == 0) set_error(prm.err, kErrPage);
     if (ok && rows > 0) {
       const uint32_t bytes = static_cast<uint32_t>(rows) * kRowBytes;
       const size_t tile = (static_cast<size_t>(phys) * kHkv + kvh) * (kPage * kDim);
-      mbar_arrive_expect_tx(&ws.bar[stage], 2 * bytes);
-      bulk_load(ws.k[stage], prm.k_pool + tile, bytes, &ws.bar[stage]);
-      bulk_load(ws.v[stage], prm.v_pool + tile, bytes, &ws.bar[stage]);
-    } else {
+      if (lane == 0) mbar_arrive_expect_tx(&ws.bar[stage], 2 * bytes);
+      __syncwarp(0x3u);   // the expected bytes are set before either copy can land
+      bulk_load(lane == 0 ? ws.k[stage] : ws.v[stage], (lane == 0 ? prm.k_pool : prm.v_pool) + tile,
+                bytes, &ws.bar[stage]);
+    } else if (lane == 0) {
       mbar_arrive(&ws.bar[stage]);
     }
   };
