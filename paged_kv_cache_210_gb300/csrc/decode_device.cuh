@@ -10,6 +10,7 @@
 #ifndef PKV_DECODE_DEVICE_CUH
 #define PKV_DECODE_DEVICE_CUH
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -51,16 +52,7 @@ constexpr int kErrSeqLen = PKV_DEV_ERR_SEQ_LEN;
 constexpr int kErrTimeout = PKV_DEV_ERR_TIMEOUT;
 
 
-template <int kStages>
-struct alignas(16) WarpSmem {
-  uint8_t k[kStages][kTileBytes];
-  uint8_t v[kStages][kTileBytes];
-  float2 p[kPage][kGroup];   // (p, p) per token and head
-  float2 alpha[kGroup];      // (alpha, alpha) per head
-  unsigned long long bar[kStages];
-};
-
-// A head leader's inbox (placed after BlockSmem, cluster kernels only): every
+// A head leader's inbox (placed after the block's shared memory, cluster kernels only): every
 // block of the cluster stores its (m, l, o) for the heads this block leads.
 // Slot of block r for head g: (g / S) * S + r (at most 16 slots for S <= 16).
 constexpr int kInboxSlots = kMaxClusterSize;
@@ -82,9 +74,22 @@ struct alignas(16) AsyncInbox {
 };
 constexpr uint32_t kPartBytes = (kDim + 2) * sizeof(float);   // one (o, m, l) part: 264 B
 
+// Shared memory of decode_kernel. Each warp's ring of K and V page tiles
+// comes first, as the copy engine writes them with the 128-byte swizzle
+// (16-byte chunk c of row r at chunk c ^ (r mod 8); every tile is
+// 1024-byte aligned, so the rule holds for each tile's own rows), then one
+// mbarrier per stage, then the block merge's slots (aliased by the
+// longest-first order of the prologue) and the block-table row.
+template <int kStages>
+struct alignas(1024) PageRing {
+  uint8_t k[kStages][kTileBytes];
+  uint8_t v[kStages][kTileBytes];
+};
+
 template <int kWarps, int kStages>
-struct alignas(16) BlockSmem {
-  WarpSmem<kStages> warp[kWarps];
+struct alignas(1024) DecodeSmem {
+  PageRing<kStages> warp[kWarps];
+  unsigned long long bar[kWarps][kStages];
   float m[kWarps][kGroup];
   float l[kWarps][kGroup];
   union {
@@ -99,24 +104,23 @@ struct alignas(16) BlockSmem {
   int last;
 };
 
-using TicketSmem = BlockSmem<kTicketWarps, kTicketStages>;
-using NarrowSmem = BlockSmem<kClusterWarps, kNarrowStages>;
-using WideSmem = BlockSmem<kWideWarps, kWideStages>;
-static_assert(sizeof(WarpSmem<kTicketStages>) % 16 == 0 &&
-                  sizeof(WarpSmem<kWideStages>) % 16 == 0,
-              "warp slabs keep 16-byte alignment");
-static_assert(sizeof(NarrowSmem) % 16 == 0 && sizeof(WideSmem) % 16 == 0,
-              "the cluster inbox follows BlockSmem 16-byte aligned");
 static_assert(sizeof(ClusterInbox) % 16 == 0 && sizeof(AsyncInbox) % 16 == 0,
               "inbox sizes keep 16-byte alignment");
 static_assert(sizeof(AsyncInbox) <= sizeof(ClusterInbox) + 16, "the inboxes take the same room");
 // residency the kernels are shaped for: 228 KiB of shared memory per SM, 1 KiB
 // of it reserved per block; 4 ticket blocks or 3 cluster blocks per SM
 constexpr size_t kSmemPerSm = 228 * 1024;
-static_assert(4 * (sizeof(TicketSmem) + 1024) <= kSmemPerSm, "4 ticket blocks per SM");
-static_assert(3 * (sizeof(NarrowSmem) + sizeof(AsyncInbox) + 1024) <= kSmemPerSm,
+using TicketDecodeSmem = DecodeSmem<kTicketWarps, kTicketStages>;
+using NarrowDecodeSmem = DecodeSmem<kClusterWarps, kNarrowStages>;
+using WideDecodeSmem = DecodeSmem<kWideWarps, kWideStages>;
+static_assert(sizeof(NarrowDecodeSmem) % 16 == 0 && sizeof(WideDecodeSmem) % 16 == 0,
+              "the cluster inbox follows DecodeSmem 16-byte aligned");
+// + 1 KiB: the dynamic shared memory base is rounded up to 1024 bytes
+static_assert(4 * (sizeof(TicketDecodeSmem) + 1024 + 1024) <= kSmemPerSm,
+              "4 ticket blocks per SM");
+static_assert(3 * (sizeof(NarrowDecodeSmem) + sizeof(AsyncInbox) + 1024 + 1024) <= kSmemPerSm,
               "3 narrow cluster blocks per SM");
-static_assert((16 / kWideWarps) * (sizeof(WideSmem) + sizeof(AsyncInbox) + 1024) <=
+static_assert((16 / kWideWarps) * (sizeof(WideDecodeSmem) + sizeof(AsyncInbox) + 1024 + 1024) <=
                   kSmemPerSm,
               "16 warps of wide cluster blocks per SM");
 
@@ -238,15 +242,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Bulk copy global -> shared (the copy engine), completion counted in bytes
-// on `bar`. dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          unsigned long long* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // BF16 pair (low half = element 0) -> two FP32 values, exact.
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
@@ -290,248 +285,232 @@ __device__ __forceinline__ uint4 shfl_xor_uint4(uint4 v, int m) {
                     __shfl_xor_sync(0xffffffffu, v.z, m), __shfl_xor_sync(0xffffffffu, v.w, m));
 }
 
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  return __ffma2_rn(a, b, c);
+// ---------------------------------------------------------------- page computation on tensor cores
+// decode_kernel's page math: warp-wide mma.sync m16n8k16 (BF16 operands,
+// FP32 accumulate). The rows of every product are the 4 query heads of the
+// kv head, padded to 16 with zero rows, so lane L sees head g = L / 4 in its
+// row fragments (lanes 16..31: padding rows 4..7) and column pair 2 q, 2 q + 1
+// with q = L % 4.
+//   scores: S = Q K^T, columns = the page's 16 tokens (two 8-token tiles),
+//           contraction over the 64 dims in 4 slices of 16;
+//   values: O += P V, columns = the 64 dims (eight 8-dim tiles), contraction
+//           over the 16 tokens, P as a BF16 high part (truncated) plus a
+//           BF16 low part (two products, ~16 significant bits of P).
+// The order of the dims inside a contraction slice does not change the sum
+// as long as Q and K agree on it: slice s, lane q takes dims 16 q + 4 s ..
+// + 3, so each lane's K fragments come from one 32-byte span of one token
+// row (two 16-byte loads, bank-conflict free on the swizzled tile).
+
+constexpr float kRescaleLog2 = 8.f;   // lazy max: a head's p stay <= 2^8
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a2,
+                                               uint32_t b0, uint32_t b1) {
+  // rows 8..15 of A (a1, a3) are the zero padding
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+// Copy of one (page, kv head) tile by the tensor copy engine: 16 token rows
+// of 64 dims from a pool seen as [page][kv head * 16 + token][dim] (the
+// tensor map), with the 128-byte swizzle, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_tile(void* dst, const CUtensorMap* map, int row,
+                                              int page, unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(page),
+        "r"(smem_u32(bar))
+      : "memory");
+}
 
-// ---------------------------------------------------------------- page computation
-// Lane roles, fixed per lane. QK: a lane owns tokens tp and tp + 8 and the
-// 16-byte dim chunks qd and qd + 4 (read in a row-parity-dependent order so
-// the shared loads are bank-conflict-free); after the reduce-scatter it owns
-// head gh. PV: a lane owns dims 4 dq .. 4 dq + 3 of the tokens 2 i + tpar.
-struct LaneRoles {
-  int tp, qd, cA, cB, gh, dq, tpar;
-  __device__ explicit LaneRoles(int lane) {
-    tp = lane >> 2;
-    qd = lane & 3;
-    const int par = tp & 1;
-    cA = qd + 4 * par;
-    cB = qd + 4 * (1 - par);
-    gh = 2 * (qd & 1) + ((qd >> 1) & 1);
-    dq = lane & 15;
-    tpar = lane >> 4;
-  }
-};
+// The tensor map's descriptor into the cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 
-// Online-softmax state of one warp for the 4 heads of a kv head.
-struct WarpState {
-  float m_run;              // running max (base 2) of head gh
-  float l_run;              // this lane's share of the running sum of head gh
-  float2 acc[kGroup][2];    // PV accumulators: dims (4dq, 4dq+1), (4dq+2, 4dq+3)
+// This thread's earlier generic-proxy writes to shared memory are ordered
+// before later copy-engine (async proxy) accesses to it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Four transposed 8x8 BF16 matrices from shared memory, one row address per lane.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// Online-softmax state of one warp on tensor cores (head g = lane / 4).
+struct MmaState {
+  float o[8][4];   // O tile j: [0..1] = O[g][8 j + 2 q, + 1]; [2..3] padding rows (zero)
+  float m_run;     // base-2 max the exponentials of head g are taken against
+  float l_run;     // this lane's share of head g's sum (its 4 columns)
   __device__ void reset() {
+    #pragma unroll
+    for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
     m_run = -INFINITY;
     l_run = 0.f;
-    #pragma unroll
-    for (int g = 0; g < kGroup; ++g) acc[g][0] = acc[g][1] = make_float2(0.f, 0.f);
   }
 };
 
-// q of the 4 heads at qrow ([4][64] BF16) for this lane's chunks, scaled by
-// log2(e) / sqrt(64) so that scores come out in base 2. kRope: q is first
-// rotated in FP32 by the angles cs, sn of pairs 8 qd .. 8 qd + 7 at the
-// query's position; the lane's chunks qd and qd + 4 are exactly the two
-// halves of those pairs. With the scale folded into the angles and the sign
-// of the rotation folded into sin (chunk A is the low half when cA < 4):
-//   A' = A c' + B s_A,  B' = B c' - A s_A,  c' = c scale, s_A = -/+ s scale.
+// q of the 4 heads as the A fragments of the score products: lane L < 16
+// holds head L / 4, dims 16 (L % 4) .. + 15 as 8 BF16 pairs; slice s uses
+// pairs 2 s and 2 s + 1. Lanes 16..31 hold zeros. kRope: q is first rotated
+// in FP32 by the angles of its position (cos_row, sin_row: the 32 pair
+// angles; dim d < 32 pairs with d + 32, the partner half coming from lane
+// L ^ 2) and kept as BF16 high (qh) and low (ql) parts; otherwise q is exact
+// in BF16 and ql is zero.
 template <bool kRope>
-__device__ __forceinline__ void load_q(const uint16_t* qrow, const LaneRoles& r,
-                                       float2 (&qa)[kGroup][4], float2 (&qb)[kGroup][4],
-                                       const float (&cs)[8], const float (&sn)[8]) {
-  const float qscale = 1.4426950408889634f * 0.125f;
-  float2 cq[4], sa[4], sb[4];
-  if (kRope) {
-    const float sgn = r.cA < 4 ? -qscale : qscale;
+__device__ __forceinline__ void load_q_mma(const uint16_t* qrow, int lane, const float* cos_row,
+                                           const float* sin_row, uint32_t (&qh)[8],
+                                           uint32_t (&ql)[8]) {
+  const int g = lane >> 2;
+  const int qq = lane & 3;
+  uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+  if (lane < 16) {
+    const uint4* src = reinterpret_cast<const uint4*>(qrow + g * kDim + 16 * qq);
+    a = __ldg(src);
+    b = __ldg(src + 1);
+  }
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  if constexpr (!kRope) {
     #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      cq[j] = make_float2(cs[2 * j] * qscale, cs[2 * j + 1] * qscale);
-      sa[j] = make_float2(sn[2 * j] * sgn, sn[2 * j + 1] * sgn);
-      sb[j] = make_float2(-sa[j].x, -sa[j].y);
+    for (int i = 0; i < 8; ++i) {
+      qh[i] = w[i];
+      ql[i] = 0u;
     }
-  }
-  #pragma unroll
-  for (int g = 0; g < kGroup; ++g) {
-    const uint4* pa = reinterpret_cast<const uint4*>(qrow + g * kDim + r.cA * 8);
-    const uint4* pb = reinterpret_cast<const uint4*>(qrow + g * kDim + r.cB * 8);
-    const uint4 ra = __ldg(pa);
-    const uint4 rb = __ldg(pb);
-    const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
-    const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
-    #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 fa = bf16x2_to_float2(wa[j]);
-      const float2 fb = bf16x2_to_float2(wb[j]);
-      if (kRope) {
-        qa[g][j] = ffma2(fb, sa[j], fmul2(fa, cq[j]));
-        qb[g][j] = ffma2(fa, sb[j], fmul2(fb, cq[j]));
-      } else {
-        qa[g][j] = make_float2(fa.x * qscale, fa.y * qscale);
-        qb[g][j] = make_float2(fb.x * qscale, fb.y * qscale);
-      }
-    }
-  }
-}
-
-// Scores of one page for this lane: tokens tp and tp + 8 of K tile kt, all 4
-// heads over the lane's 16 dims, then a reduce-scatter over the 4 lanes of a
-// token pair so that the lane keeps head gh's full scores (base 2, scaled).
-// Tokens at or past `live` get -inf.
-__device__ __forceinline__ void page_scores(const uint8_t* kt, int live,
-                                            const float2 (&qa)[kGroup][4],
-                                            const float2 (&qb)[kGroup][4], const LaneRoles& r,
-                                            float (&sc)[2]) {
-  float s[kGroup][2];
-  #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint8_t* krow = kt + (r.tp + 8 * j) * kRowBytes;
-    const uint4 ka = *reinterpret_cast<const uint4*>(krow + r.cA * 16);
-    const uint4 kb = *reinterpret_cast<const uint4*>(krow + r.cB * 16);
-    const float2 fa[4] = {bf16x2_to_float2(ka.x), bf16x2_to_float2(ka.y),
-                          bf16x2_to_float2(ka.z), bf16x2_to_float2(ka.w)};
-    const float2 fb[4] = {bf16x2_to_float2(kb.x), bf16x2_to_float2(kb.y),
-                          bf16x2_to_float2(kb.z), bf16x2_to_float2(kb.w)};
-    #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-      float2 d = make_float2(0.f, 0.f);
-      #pragma unroll
-      for (int c = 0; c < 4; ++c) d = ffma2(qa[g][c], fa[c], d);
-      #pragma unroll
-      for (int c = 0; c < 4; ++c) d = ffma2(qb[g][c], fb[c], d);
-      s[g][j] = d.x + d.y;
-    }
-  }
-  const bool hi1 = r.qd & 1;
-  const bool hi2 = r.qd & 2;
-  #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const float send0 = hi1 ? s[0][j] : s[2][j];
-    const float send1 = hi1 ? s[1][j] : s[3][j];
-    float keep0 = hi1 ? s[2][j] : s[0][j];
-    float keep1 = hi1 ? s[3][j] : s[1][j];
-    keep0 += __shfl_xor_sync(0xffffffffu, send0, 1);
-    keep1 += __shfl_xor_sync(0xffffffffu, send1, 1);
-    const float send = hi2 ? keep0 : keep1;
-    float kept = hi2 ? keep1 : keep0;
-    kept += __shfl_xor_sync(0xffffffffu, send, 2);
-    sc[j] = kept;
-  }
-  sc[0] = r.tp < live ? sc[0] : -INFINITY;
-  sc[1] = r.tp + 8 < live ? sc[1] : -INFINITY;
-}
-
-// Rescale of the accumulators by the per-head factors in alpha_s.
-__device__ __forceinline__ void rescale_acc(const float2* alpha_s, WarpState& st) {
-  const float4 a01 = *reinterpret_cast<const float4*>(&alpha_s[0]);
-  const float4 a23 = *reinterpret_cast<const float4*>(&alpha_s[2]);
-  const float2 al[kGroup] = {make_float2(a01.x, a01.y), make_float2(a01.z, a01.w),
-                             make_float2(a23.x, a23.y), make_float2(a23.z, a23.w)};
-  #pragma unroll
-  for (int g = 0; g < kGroup; ++g) {
-    st.acc[g][0] = fmul2(st.acc[g][0], al[g]);
-    st.acc[g][1] = fmul2(st.acc[g][1], al[g]);
-  }
-}
-
-// P V of one page: this lane's 4 dims over its tokens 2 i + tpar of V tile vt
-// (the first `live`), with the probabilities of the 4 heads from p ([16][4],
-// each duplicated as a pair).
-__device__ __forceinline__ void page_pv(const uint8_t* vt, int live, const float2 (*p)[kGroup],
-                                        const LaneRoles& r, WarpState& st) {
-  auto pv_token = [&](int t) {
-    const uint2 vv = *reinterpret_cast<const uint2*>(vt + t * kRowBytes + r.dq * 8);
-    const float2 v01 = bf16x2_to_float2(vv.x);
-    const float2 v23 = bf16x2_to_float2(vv.y);
-    const float4 pa = *reinterpret_cast<const float4*>(&p[t][0]);
-    const float4 pb = *reinterpret_cast<const float4*>(&p[t][2]);
-    const float2 pg[kGroup] = {make_float2(pa.x, pa.y), make_float2(pa.z, pa.w),
-                               make_float2(pb.x, pb.y), make_float2(pb.z, pb.w)};
-    #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-      st.acc[g][0] = ffma2(pg[g], v01, st.acc[g][0]);
-      st.acc[g][1] = ffma2(pg[g], v23, st.acc[g][1]);
-    }
-  };
-  if (live == kPage) {
-    #pragma unroll
-    for (int t2 = 0; t2 < kPage / 2; ++t2) pv_token(2 * t2 + r.tpar);
   } else {
-    #pragma unroll
-    for (int t2 = 0; t2 < kPage / 2; ++t2) {
-      if (2 * t2 + r.tpar < live) pv_token(2 * t2 + r.tpar);
-    }
+  float cs[16], sn[16];
+  #pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 c4 = __ldg(reinterpret_cast<const float4*>(cos_row + 16 * (qq & 1)) + i);
+    const float4 s4 = __ldg(reinterpret_cast<const float4*>(sin_row + 16 * (qq & 1)) + i);
+    cs[4 * i] = c4.x; cs[4 * i + 1] = c4.y; cs[4 * i + 2] = c4.z; cs[4 * i + 3] = c4.w;
+    sn[4 * i] = s4.x; sn[4 * i + 1] = s4.y; sn[4 * i + 2] = s4.z; sn[4 * i + 3] = s4.w;
+  }
+  // dims < 32: x' = x cos - y sin; dims >= 32: y' = y cos + x sin
+  const float sgn = qq < 2 ? -1.f : 1.f;
+  #pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t pw = __shfl_xor_sync(0xffffffffu, w[i], 2);
+    const float2 own = bf16x2_to_float2(w[i]);
+    const float2 par = bf16x2_to_float2(pw);
+    const float r0 = fmaf(own.x, cs[2 * i], sgn * par.x * sn[2 * i]);
+    const float r1 = fmaf(own.y, cs[2 * i + 1], sgn * par.y * sn[2 * i + 1]);
+    const uint32_t hi = float2_to_bf16x2(r0, r1);
+    const float2 hf = bf16x2_to_float2(hi);
+    qh[i] = lane < 16 ? hi : 0u;
+    ql[i] = lane < 16 ? float2_to_bf16x2(r0 - hf.x, r1 - hf.y) : 0u;
+  }
   }
 }
 
-// One page: K tile kt and V tile vt in shared memory, `live` valid tokens
-// (the rest are masked by select, so stale data never leaks). p and alpha
-// are the warp's shared slots for the probabilities and the rescale factors.
-__device__ __forceinline__ void attend_page(const uint8_t* kt, const uint8_t* vt, int live,
-                                            const float2 (&qa)[kGroup][4],
-                                            const float2 (&qb)[kGroup][4],
-                                            float2 (*p)[kGroup], float2* alpha_s,
-                                            const LaneRoles& r, WarpState& st) {
-  float sc[2];
-  page_scores(kt, live, qa, qb, r, sc);
-
-  // online softmax, base 2, per head over the page's 16 tokens
-  float pm = fmaxf(sc[0], sc[1]);
-  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-  const float m_new = fmaxf(st.m_run, pm);
-  const float m_use = m_new == -INFINITY ? 0.f : m_new;
-  const float alpha = fast_exp2(st.m_run - m_use);
-  const float p0 = fast_exp2(sc[0] - m_use);
-  const float p1 = fast_exp2(sc[1] - m_use);
-  st.l_run = st.l_run * alpha + p0 + p1;
-  st.m_run = m_new;
-  p[r.tp][r.gh] = make_float2(p0, p0);
-  p[r.tp + 8][r.gh] = make_float2(p1, p1);
-  if (r.tp == 0) alpha_s[r.gh] = make_float2(alpha, alpha);
-  __syncwarp();
-
-  // PV: rescale, then accumulate this lane's tokens
-  rescale_acc(alpha_s, st);
-  page_pv(vt, live, p, r, st);
-  __syncwarp();
-}
-
-// End of a warp's pages: the running sum over the 8 token-pair lanes of each
-// head, the accumulators over the two token-parity halves.
-__device__ __forceinline__ void reduce_warp_state(WarpState& st) {
-  st.l_run += __shfl_xor_sync(0xffffffffu, st.l_run, 4);
-  st.l_run += __shfl_xor_sync(0xffffffffu, st.l_run, 8);
-  st.l_run += __shfl_xor_sync(0xffffffffu, st.l_run, 16);
+// One page on tensor cores: K tile kt and V tile vt (swizzled, in shared
+// memory), `live` valid tokens (the scores of the rest are masked by select;
+// V rows at or past `live` must hold finite values, the caller zeroes them).
+template <bool kRope>
+__device__ __forceinline__ void attend_page_mma(const uint8_t* kt, const uint8_t* vt, int live,
+                                                int lane, const uint32_t (&qh)[8],
+                                                const uint32_t (&ql)[8], MmaState& st) {
+  const int g = lane >> 2;
+  const int qq = lane & 3;
+  // ---- S = Q K^T: lane q of row group g loads token 8 nt + g, dims 16 q .. + 15
+  float s[4];
   #pragma unroll
-  for (int g = 0; g < kGroup; ++g) {
+  for (int nt = 0; nt < 2; ++nt) {
+    const uint8_t* row = kt + (8 * nt + g) * kRowBytes;
+    const uint4 k0 = *reinterpret_cast<const uint4*>(row + (((2 * qq) ^ g) << 4));
+    const uint4 k1 = *reinterpret_cast<const uint4*>(row + (((2 * qq + 1) ^ g) << 4));
+    const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
     #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      st.acc[g][h].x += __shfl_xor_sync(0xffffffffu, st.acc[g][h].x, 16);
-      st.acc[g][h].y += __shfl_xor_sync(0xffffffffu, st.acc[g][h].y, 16);
+    for (int sl = 0; sl < 4; ++sl) {
+      mma_bf16_16816(d, qh[2 * sl], qh[2 * sl + 1], kw[2 * sl], kw[2 * sl + 1]);
+      if (kRope) mma_bf16_16816(d, ql[2 * sl], ql[2 * sl + 1], kw[2 * sl], kw[2 * sl + 1]);
     }
+    s[2 * nt] = d[0];
+    s[2 * nt + 1] = d[1];
+  }
+  // ---- online softmax of head g over its tokens 2 q, 2 q + 1, 8 + 2 q, 9 + 2 q
+  const float c = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
+  float x[4];
+  #pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = 8 * (i >> 1) + 2 * qq + (i & 1);
+    x[i] = t < live ? s[i] * c : -INFINITY;
+  }
+  float pm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+  // the max used moves only when the head's max grows by more than 2^8
+  const bool grow = pm > st.m_run + kRescaleLog2;
+  if (__any_sync(0xffffffffu, grow)) {
+    const float alpha = grow ? fast_exp2(st.m_run - pm) : 1.f;   // 0 on the first valid page
+    if (grow) st.m_run = pm;
+    st.l_run *= alpha;
+    #pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      st.o[j][0] *= alpha;
+      st.o[j][1] *= alpha;
+    }
+  }
+  const float mu = st.m_run == -INFINITY ? 0.f : st.m_run;
+  float p[4];
+  #pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - mu);
+  st.l_run += (p[0] + p[1]) + (p[2] + p[3]);
+  // P as the A fragments of the value products: tokens 2 q, 2 q + 1 (pair 0)
+  // and 8 + 2 q, 9 + 2 q (pair 2), high parts truncated, low parts rounded
+  uint32_t ah[2], al[2];
+  #pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t b0 = __float_as_uint(p[2 * h]), b1 = __float_as_uint(p[2 * h + 1]);
+    ah[h] = __byte_perm(b0, b1, 0x7632);
+    al[h] = float2_to_bf16x2(p[2 * h] - __uint_as_float(b0 & 0xffff0000u),
+                             p[2 * h + 1] - __uint_as_float(b1 & 0xffff0000u));
+  }
+  // ---- O += P V: lane L addresses row L % 8 of matrix L / 8 (tokens 0..7 or
+  // 8..15, dim chunk 2 jj or 2 jj + 1), the transposed loads giving the
+  // B fragments of dim tiles 2 jj and 2 jj + 1
+  const int mrow = lane & 7;
+  const int mat = lane >> 3;
+  const uint32_t vrow = smem_u32(vt) + (mrow + 8 * (mat & 1)) * kRowBytes;
+  #pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    uint32_t bv[4];
+    ldsm_x4_trans(bv, vrow + (((2 * jj + (mat >> 1)) ^ mrow) << 4));
+    mma_bf16_16816(st.o[2 * jj], ah[0], ah[1], bv[0], bv[1]);
+    mma_bf16_16816(st.o[2 * jj], al[0], al[1], bv[0], bv[1]);
+    mma_bf16_16816(st.o[2 * jj + 1], ah[0], ah[1], bv[2], bv[3]);
+    mma_bf16_16816(st.o[2 * jj + 1], al[0], al[1], bv[2], bv[3]);
   }
 }
 
 // ---------------------------------------------------------------- merges
-// The block's warps merged in shared memory: thread t < 128 gets the
-// log-sum-exp state of head g = (t / 32) % 4 for dims d0 = 2 (t % 32), d0 + 1
-// (M: max, L: sum, O: unnormalised output); the rest of an 8-warp block
-// computes an alias.
-template <int kWarps, int kStages>
-__device__ __forceinline__ void block_merge(BlockSmem<kWarps, kStages>& sm, const WarpState& st,
-                                            const LaneRoles& rl, int warp, float& M, float& L,
-                                            float2& O) {
-  if (rl.tp == 0) {
-    sm.m[warp][rl.gh] = st.m_run;
-    sm.l[warp][rl.gh] = st.l_run;
-  }
-  if (rl.tpar == 0) {
-    #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-      *reinterpret_cast<float4*>(&sm.acc[warp][g][4 * rl.dq]) =
-          make_float4(st.acc[g][0].x, st.acc[g][0].y, st.acc[g][1].x, st.acc[g][1].y);
+// The block's warps merged in shared memory: lanes 0..15 of each warp store
+// head lane / 4's max, sum (summed over the lane quad) and output tiles;
+// then thread t < 128 gets the log-sum-exp state of head g = (t / 32) % 4
+// for dims d0 = 2 (t % 32), d0 + 1 (M: max, L: sum, O: unnormalised output).
+template <int kWarps, class Smem>
+__device__ __forceinline__ void block_merge_mma(Smem& sm, MmaState& st, int warp, int lane,
+                                                float& M, float& L, float2& O) {
+  st.l_run += __shfl_xor_sync(0xffffffffu, st.l_run, 1);
+  st.l_run += __shfl_xor_sync(0xffffffffu, st.l_run, 2);
+  if (lane < 16) {
+    const int g = lane >> 2;
+    const int qq = lane & 3;
+    if (qq == 0) {
+      sm.m[warp][g] = st.m_run;
+      sm.l[warp][g] = st.l_run;
     }
+    #pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float2*>(&sm.acc[warp][g][8 * j + 2 * qq]) =
+          make_float2(st.o[j][0], st.o[j][1]);
   }
   __syncthreads();
   const int g = (threadIdx.x >> 5) & (kGroup - 1);
@@ -552,23 +531,19 @@ __device__ __forceinline__ void block_merge(BlockSmem<kWarps, kStages>& sm, cons
   }
 }
 
+
 // Cluster merge of the S blocks of one (sequence, kv head) (S = the cluster
-// size): each block first merges its warps (block_merge), then sends one
-// (m, l, o) part per head straight into the inbox of the head's leader,
-// block g mod S of the cluster; every thread arrives on the cluster barrier,
-// and in each leader warp w combines the S parts of head rank + w S into
-// out_kv ([4][64], the kv head's query heads). A block that leads no head
-// returns after its arrival, or, with `wait_always` (blocks that go on to use
-// the cluster barrier again), after the wait as well.
-template <int kWarps, int kStages>
-__device__ __forceinline__ void cluster_merge(BlockSmem<kWarps, kStages>& sm,
-                                              ClusterInbox& inbox, const WarpState& st,
-                                              const LaneRoles& rl, int warp, int lane,
-                                              float* out_kv, bool wait_always) {
-  static_assert(kWarps % kGroup == 0, "threads 0..127 hold one (head, dim pair) each");
-  float M, L;
-  float2 O;
-  block_merge(sm, st, rl, warp, M, L, O);
+// size), after each block merged its warps (M, L, O of thread t < 128: head
+// t / 32, dims 2 (t % 32), + 1): threads 0..127 send one (m, l, o) part per
+// head straight into the inbox of the head's leader, block g mod S of the
+// cluster; every thread arrives on the cluster barrier, and in each leader
+// warp w combines the S parts of head rank + w S into out_kv ([4][64], the
+// kv head's query heads). A block that leads no head returns after its
+// arrival, or, with `wait_always` (blocks that go on to use the cluster
+// barrier again), after the wait as well.
+__device__ __forceinline__ void cluster_merge(ClusterInbox& inbox, float M, float L, float2 O,
+                                              int warp, int lane, float* out_kv,
+                                              bool wait_always) {
   const int S = gridDim.x;
   const int rank = static_cast<int>(cluster_rank());
   const int g = warp;               // thread t < 128: head t / 32, dims 2 (t % 32), + 1
@@ -630,20 +605,14 @@ __device__ __forceinline__ void async_inbox_setup(AsyncInbox& inbox) {
   cluster_wait_acquire();
 }
 
-// Cluster merge without a closing cluster barrier: each block merges its
-// warps (block_merge), then threads 0..127 send the block's (o, m, l) part of
-// head t / 32 to the head's leader (block g mod S) with st.async stores; a
-// block that leads no head is then done. In a leader, warp w waits until the
-// parts of head rank + w S have landed and combines them into out_kv.
-template <int kWarps, int kStages>
-__device__ __forceinline__ void cluster_merge_async(BlockSmem<kWarps, kStages>& sm,
-                                                    AsyncInbox& inbox, const WarpState& st,
-                                                    const LaneRoles& rl, int warp, int lane,
-                                                    float* out_kv, int* err) {
-  static_assert(kWarps % kGroup == 0, "threads 0..127 hold one (head, dim pair) each");
-  float M, L;
-  float2 O;
-  block_merge(sm, st, rl, warp, M, L, O);
+// Cluster merge without a closing cluster barrier: after the block merge
+// (M, L, O of thread t < 128: head t / 32, dims 2 (t % 32), + 1), threads
+// 0..127 send the block's (o, m, l) part of head t / 32 to the head's leader
+// (block g mod S) with st.async stores; a block that leads no head is then
+// done. In a leader, warp w waits until the parts of head rank + w S have
+// landed and combines them into out_kv.
+__device__ __forceinline__ void cluster_merge_async(AsyncInbox& inbox, float M, float L, float2 O,
+                                                    int warp, int lane, float* out_kv, int* err) {
   const int S = gridDim.x;
   const int rank = static_cast<int>(cluster_rank());
   const int d0 = 2 * lane;
@@ -700,9 +669,9 @@ __device__ __forceinline__ int page_count(int len) {
 
 // Returns -1 without the second pass when `useful(pages)` says a block of
 // that rank has no work (split slots past the sequence's last range).
-template <int kWarps, int kStages, class Useful>
-__device__ int longest_first_sequence(int z, int batch, const int32_t* seq_lens,
-                                      BlockSmem<kWarps, kStages>& sm, Useful useful) {
+template <int kWarps, class Smem, class Useful>
+__device__ int longest_first_sequence(int z, int batch, const int32_t* seq_lens, Smem& sm,
+                                      Useful useful) {
   constexpr int kThreads = kWarps * 32;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;

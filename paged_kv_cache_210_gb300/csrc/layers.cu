@@ -6,6 +6,7 @@
 // batched decode bullet]; this kernel keeps each sequence's layer order with
 // device-side waits instead of one launch per layer.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -57,14 +58,16 @@ struct LayersParams {
   int wait_extra;             // added to every wait's target: 0, or 1 from the timeout test hook
 };
 
-struct alignas(16) LayersSmem {
-  BlockSmem<kClusterWarps, kWideStages> blk;
+struct alignas(1024) LayersSmem {
+  DecodeSmem<kClusterWarps, kWideStages> blk;
   ClusterInbox inbox;
   int ptab[kLayerTab];        // physical page of (layer j, page o of the block's range): j * span + o
   int flag;                   // thread 0's wait verdict for the block
 };
+// + 1 KiB: the kernel rounds the dynamic shared memory base up to 1024 bytes
+constexpr size_t kLayersSmemBytes = sizeof(LayersSmem) + 1024;
 
-static_assert(4 * (sizeof(LayersSmem) + 1024) <= kSmemPerSm, "4 multi-layer blocks per SM");
+static_assert(4 * (kLayersSmemBytes + 1024) <= kSmemPerSm, "4 multi-layer blocks per SM");
 
 // Bounded wait until *ctr >= target (acquire, GPU scope): false after about
 // two seconds.
@@ -82,12 +85,18 @@ __device__ __forceinline__ bool wait_count(const int* ctr, int target) {
   return true;
 }
 
-__global__ void __launch_bounds__(kClusterWarps * 32, 4) decode_layers_kernel(const LayersParams prm) {
+// tmap_k, tmap_v: the K and V pools as the copy engine's 3-D tensors (dim,
+// kv head x 16 + token, page), boxes of one (page, kv head) tile.
+__global__ void __launch_bounds__(kClusterWarps * 32, 4)
+decode_layers_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const LayersParams prm) {
   constexpr int kWarps = kClusterWarps;
   constexpr int kStages = kWideStages;
   constexpr int kThreads = kWarps * 32;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  LayersSmem& ls = *reinterpret_cast<LayersSmem*>(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled tiles need a 1024-byte aligned base (the launch adds 1 KiB)
+  LayersSmem& ls = *reinterpret_cast<LayersSmem*>(
+      smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   auto& sm = ls.blk;
 
   const int S = static_cast<int>(gridDim.x);
@@ -125,14 +134,19 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 4) decode_layers_kernel(co
     ls.ptab[e] = prm.tables[static_cast<size_t>(j) * prm.table_layer_stride +
                             static_cast<size_t>(b) * prm.table_stride + page_begin + (e - j * span)];
   }
-  WarpSmem<kStages>& ws = sm.warp[warp];
+  PageRing<kStages>& ws = sm.warp[warp];
+  unsigned long long* bars = sm.bar[warp];
   // this warp's pages of the range: warp, warp + 4, ...; its items run over
   // the layers: item k is page i = k % mine of layer j = k / mine
   const int mine = warp < span ? (span - warp + kWarps - 1) / kWarps : 0;
   const int total = mine * J;
   if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&ws.bar[s], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
+    if (warp == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
   }
   __syncthreads();
 
@@ -145,23 +159,24 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 4) decode_layers_kernel(co
     const int j = k / mine;
     return ls.ptab[j * span + warp + kWarps * (k - j * mine)];
   };
-  // Copy engine: item k into `stage` (lane 0 issues); the last page's copy
-  // stops before the appended row, which comes from k/v after the wait
+  // Copy engine: item k into `stage`, whole 16-row tiles (rows past the
+  // sequence are masked or zeroed after they land), K by lane 0 and V by
+  // lane 1 in one instruction. A last page whose only row is the appended
+  // one is not copied: that row comes from k/v after the wait.
   auto issue_copy = [&](int k, int stage) {
-    if (lane != 0) return;
+    if (lane > 1) return;
     const int lp = page_begin + warp + kWarps * (k % mine);
     const int phys = phys_of(k);
     const bool ok = phys >= 0 && phys < prm.num_pages;
-    const int rows = lp == last_page ? new_slot : kPage;
-    if (!ok) set_error(prm.err, kErrPage);
-    if (ok && rows > 0) {
-      const uint32_t bytes = static_cast<uint32_t>(rows) * kRowBytes;
-      const size_t tile = (static_cast<size_t>(phys) * kHkv + kvh) * (kPage * kDim);
-      mbar_arrive_expect_tx(&ws.bar[stage], 2 * bytes);
-      bulk_load(ws.k[stage], prm.k_pool + tile, bytes, &ws.bar[stage]);
-      bulk_load(ws.v[stage], prm.v_pool + tile, bytes, &ws.bar[stage]);
-    } else {
-      mbar_arrive(&ws.bar[stage]);
+    const bool rows = !(lp == last_page && new_slot == 0);
+    if (!ok && lane == 0) set_error(prm.err, kErrPage);
+    if (ok && rows) {
+      if (lane == 0) mbar_arrive_expect_tx(&bars[stage], 2 * kTileBytes);
+      __syncwarp(0x3u);   // the expected bytes are set before either copy can land
+      tma_load_tile(lane == 0 ? ws.k[stage] : ws.v[stage], lane == 0 ? &tmap_k : &tmap_v,
+                    kvh * kPage, phys, &bars[stage]);
+    } else if (lane == 0) {
+      mbar_arrive(&bars[stage]);
     }
   };
   // the appended row of layer j: lanes 0..7 K, 8..15 V, one 16-byte chunk each
@@ -175,23 +190,36 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 4) decode_layers_kernel(co
     }
     return val;
   };
-  // ... written to the pool and to the stage tile of its page
-  auto place_new_row = [&](int stage, int phys, uint4 val) {
+  // ... written to the pool now, and into its stage tile once that tile has landed
+  auto store_new_row = [&](int phys, uint4 val) {
     if (lane >= 16 || phys < 0 || phys >= prm.num_pages) return;
     const bool is_v = lane >= 8;
     const int c = lane & 7;
     uint16_t* pool = is_v ? prm.v_pool : prm.k_pool;
     *reinterpret_cast<uint4*>(pool + ((static_cast<size_t>(phys) * kHkv + kvh) * kPage +
                                       new_slot) * kDim + c * 8) = val;
-    uint8_t* tile = is_v ? ws.v[stage] : ws.k[stage];
-    *reinterpret_cast<uint4*>(tile + new_slot * kRowBytes + c * 16) = val;
+  };
+  uint4 new_val = make_uint4(0u, 0u, 0u, 0u);
+  // A landed stage holding fewer than 16 live tokens or the appended row: V
+  // rows at or past `live` zeroed, the appended row into its slot; the
+  // stores reach the copy engine's view before the stage is refilled.
+  auto patch_stage = [&](int stage, int live, bool with_new) {
+    uint8_t* vt = ws.v[stage];
+    for (int idx = live * 8 + lane; idx < kPage * 8; idx += 32)
+      *reinterpret_cast<uint4*>(vt + (idx >> 3) * kRowBytes + (idx & 7) * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
+    if (with_new && lane < 16) {
+      uint8_t* t = lane >= 8 ? ws.v[stage] : ws.k[stage];
+      const int c = lane & 7;
+      *reinterpret_cast<uint4*>(t + new_slot * kRowBytes + ((c ^ (new_slot & 7)) << 4)) = new_val;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
   };
 
   int issued = min(total, kStages);
   for (int k = 0; k < issued; ++k) issue_copy(k, k);
 
-  const LaneRoles rl(lane);
-  const float no_angles[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   int k = 0;                 // next item to consume
   int consumed = 0;
   bool broken = false;       // a page wait gave up: this warp copies and computes no more
@@ -216,15 +244,14 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 4) decode_layers_kernel(co
     }
     const int item_new = i_new >= 0 ? j * mine + i_new : -1;   // this layer's appended-row item
     const bool place_now = item_new >= 0 && item_new < issued && !broken;
-    uint4 new_val = make_uint4(0u, 0u, 0u, 0u);
     if (place_now) new_val = load_new_row(j);
-    float2 qa[kGroup][4], qb[kGroup][4];
-    load_q<false>(prm.q + ((static_cast<size_t>(j) * prm.batch + b) * kHq + kvh * kGroup) * kDim,
-                  rl, qa, qb, no_angles, no_angles);
-    if (place_now) place_new_row(item_new % kStages, phys_of(item_new), new_val);
-    __syncwarp();
+    uint32_t qh[8], ql[8];
+    load_q_mma<false>(prm.q + ((static_cast<size_t>(j) * prm.batch + b) * kHq + kvh * kGroup) *
+                                  kDim,
+                      lane, nullptr, nullptr, qh, ql);
+    if (place_now) store_new_row(phys_of(item_new), new_val);
 
-    WarpState st;
+    MmaState st;
     st.reset();
     bool lost = false;       // this layer's pages are incomplete
     // tokens of item k (page i of this layer) that count
@@ -240,37 +267,40 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 4) decode_layers_kernel(co
       if (kn < total) {
         issue_copy(kn, k % kStages);
         // a later item of this layer holding the appended slot: its row now
-        if (kn == item_new) place_new_row(k % kStages, phys_of(kn), load_new_row(j));
-        __syncwarp();
+        if (kn == item_new) {
+          new_val = load_new_row(j);
+          store_new_row(phys_of(kn), new_val);
+        }
         issued = kn + 1;
       }
     };
     for (int i = 0; i < mine && !broken; ++i, ++k) {
       // one verdict per warp: the page work below shuffles across all lanes
-      if (!__all_sync(0xffffffffu, mbar_wait(&ws.bar[k % kStages], (k / kStages) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[k % kStages], (k / kStages) & 1))) {
         broken = true;
         if (lane == 0) set_error(prm.err, kErrTimeout);
         break;
       }
       consumed = k + 1;
-      attend_page(ws.k[k % kStages], ws.v[k % kStages], live_of(k, i), qa, qb, ws.p, ws.alpha,
-                  rl, st);
+      const int live = live_of(k, i);
+      if (live < kPage || k == item_new) patch_stage(k % kStages, live, k == item_new && live > 0);
+      attend_page_mma<false>(ws.k[k % kStages], ws.v[k % kStages], live, lane, qh, ql, st);
+      __syncwarp();   // every lane's reads of the stage are done before it is refilled
       refill(k);
     }
     lost |= broken;
     k = (j + 1) * mine;      // the next layer's first item (also after a break)
-    reduce_warp_state(st);
     if (lost) {
       st.m_run = -INFINITY;
       st.l_run = 0.f;
     }
     float* out_kv = prm.out + ((static_cast<size_t>(j) * prm.batch + b) * kHq + kvh * kGroup) * kDim;
+    float M, L;
+    float2 O;
+    block_merge_mma<kWarps>(sm, st, warp, lane, M, L, O);
     if (n_splits > 1) {
-      cluster_merge(sm, ls.inbox, st, rl, warp, lane, out_kv, true);
+      cluster_merge(ls.inbox, M, L, O, warp, lane, out_kv, true);
     } else {
-      float M, L;
-      float2 O;
-      block_merge(sm, st, rl, warp, M, L, O);
       const int g = (threadIdx.x >> 5) & (kGroup - 1);
       const int d0 = 2 * (threadIdx.x & 31);
       const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -286,7 +316,7 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 4) decode_layers_kernel(co
   if (broken) {
     // let this warp's copies still in flight land before the block exits
     // (each wait bounded again)
-    for (int kk = consumed; kk < issued; ++kk) mbar_wait(&ws.bar[kk % kStages], (kk / kStages) & 1);
+    for (int kk = consumed; kk < issued; ++kk) mbar_wait(&bars[kk % kStages], (kk / kStages) & 1);
   }
 }
 
@@ -344,6 +374,10 @@ pkv_status launch_layers(pkv_pool_t pool, int layer_begin, int num_layers, const
     return PKV_OK;
   }
 
+  CUtensorMap tk, tv;
+  if (!pkv_pool_tensor_map(k_pool, c.num_pages, &tk) ||
+      !pkv_pool_tensor_map(v_pool, c.num_pages, &tv))
+    return PKV_ERR_CUDA;
   const int max_pages = c.max_seq_len / kPage;
   const int chunk_max = (max_pages + S - 1) / S;
   const int per_launch = kLayerTab / chunk_max;   // >= 4: chunk_max <= 64
@@ -375,7 +409,7 @@ pkv_status launch_layers(pkv_pool_t pool, int layer_begin, int num_layers, const
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, kHkv, batch);
     cfg.blockDim = dim3(kClusterWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = sizeof(LayersSmem);
+    cfg.dynamicSmemBytes = kLayersSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -384,7 +418,8 @@ pkv_status launch_layers(pkv_pool_t pool, int layer_begin, int num_layers, const
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, decode_layers_kernel, prm) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, decode_layers_kernel, tk, tv, prm) != cudaSuccess)
+      return PKV_ERR_CUDA;
   }
   return pkv_check_launch();
 }
@@ -393,7 +428,7 @@ pkv_status launch_layers(pkv_pool_t pool, int layer_begin, int num_layers, const
 
 bool pkv_layers_setup(pkv_pool* pool) {
   bool ok = cudaFuncSetAttribute(decode_layers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(sizeof(LayersSmem))) == cudaSuccess;
+                                 static_cast<int>(kLayersSmemBytes)) == cudaSuccess;
   ok = ok && cudaFuncSetAttribute(decode_layers_kernel,
                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
   // how many clusters of the multi-layer kernel the device holds at once,
@@ -406,7 +441,7 @@ bool pkv_layers_setup(pkv_pool* pool) {
     cudaLaunchConfig_t probe = {};
     probe.gridDim = dim3(size, kHkv, 1);
     probe.blockDim = dim3(kClusterWarps * 32, 1, 1);
-    probe.dynamicSmemBytes = sizeof(LayersSmem);
+    probe.dynamicSmemBytes = kLayersSmemBytes;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = size;

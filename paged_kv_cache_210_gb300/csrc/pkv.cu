@@ -16,22 +16,26 @@
 //    of the group, so each 2 KiB (page, kv head) tile of K and of V is read
 //    from HBM exactly once;
 //  * each of the block's 4 warps owns every 4th page of the split and its own
-//    ring of page stages in shared memory, filled by the bulk-copy engine
-//    (cp.async.bulk, completion counted on an mbarrier), so bytes in flight
-//    do not depend on registers and warps never wait on each other inside
-//    the page loop;
-//  * QK: a lane owns 2 tokens x 16 dims for all 4 heads; packed FP32 FMA
-//    (two lanes of FP32 per instruction) over dim pairs; a 2-step
-//    reduce-scatter leaves each lane with one head's scores for its 2 tokens;
-//  * online softmax per page in base 2 (q is pre-scaled by log2(e)/8);
-//  * PV: a lane owns 4 dims x every other token for all 4 heads; the
-//    probabilities go through a per-warp shared-memory slot, duplicated so
-//    that packed FMAs read them as pairs;
-//  * warps merge in shared memory; splits merge in the same launch: every
-//    split block writes its (o, m, l) partial and takes a ticket, and the
-//    last to arrive merges (no spinning);
-//  * the score scale 1/8 and log2(e) are folded into q once per block.
+//    ring of page stages in shared memory, filled by the tensor copy engine
+//    (cp.async.bulk.tensor with the 128-byte swizzle, the K and V tiles of a
+//    page in one instruction, completion counted on an mbarrier), so bytes in
+//    flight do not depend on registers and warps never wait on each other
+//    inside the page loop;
+//  * the page math runs on the tensor cores, warp-wide (mma.sync m16n8k16,
+//    BF16 in, FP32 accumulate): S = Q K^T with the group's 4 heads as the
+//    rows (padded to 16), then a base-2 online softmax in registers whose
+//    max moves only when a head's max grows by more than 2^8, then O += P V
+//    with P as a BF16 high plus low part; per page and lane about a quarter
+//    of the instructions the same work takes in FP32 FMAs, which leaves the
+//    step bound by HBM rather than by issue;
+//  * warps merge in shared memory; splits merge in the same launch, in a
+//    cluster through st.async stores into the head leaders' shared memory,
+//    or through global partials and a ticket: every split block writes its
+//    (o, m, l) partial and takes a ticket, and the last to arrive merges (no
+//    spinning).
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -99,13 +103,18 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t* __restrict_
 // kCluster: the splits of one (sequence, kv head) form one thread-block
 // cluster (gridDim.x == cluster size) and merge through distributed shared
 // memory; otherwise splits merge through global partials and a ticket.
+// tmap_k, tmap_v: the K and V pools as 3-D tensors (dims, kv head x token,
+// page), boxes of one (page, kv head) tile.
 template <bool kFused, bool kCluster, int kWarps, int kStages, bool kRope>
 __global__ void __launch_bounds__(kWarps * 32, kCluster && kStages == kNarrowStages ? 3 : 16 / kWarps)
-decode_kernel(const DecodeParams prm) {
+decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+              const __grid_constant__ CUtensorMap tmap_v, const DecodeParams prm) {
   constexpr int kThreads = kWarps * 32;
-  using Smem = BlockSmem<kWarps, kStages>;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  using Smem = DecodeSmem<kWarps, kStages>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled tiles need a 1024-byte aligned base (the launch adds 1 KiB)
+  uint8_t* smem_base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Smem& sm = *reinterpret_cast<Smem*>(smem_base);
 
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
@@ -121,8 +130,8 @@ decode_kernel(const DecodeParams prm) {
                                            : prm.chunk_pages;
       return pages > 0 && split < (pages + chunk - 1) / chunk;
     };
-    b = longest_first_sequence(static_cast<int>(blockIdx.z), static_cast<int>(gridDim.z),
-                               prm.seq_lens, sm, useful);
+    b = longest_first_sequence<kWarps>(static_cast<int>(blockIdx.z), static_cast<int>(gridDim.z),
+                                       prm.seq_lens, sm, useful);
     if (b < 0) return;
   }
 
@@ -153,16 +162,21 @@ decode_kernel(const DecodeParams prm) {
   const int last_page = n_pages - 1;
   const int new_slot = (len - 1) % kPage;               // slot of the appended token
 
-  WarpSmem<kStages>& ws = sm.warp[warp];
-  AsyncInbox& inbox = *reinterpret_cast<AsyncInbox*>(smem_raw + sizeof(Smem));
+  PageRing<kStages>& ws = sm.warp[warp];
+  unsigned long long* bars = sm.bar[warp];
+  AsyncInbox& inbox = *reinterpret_cast<AsyncInbox*>(smem_base + sizeof(Smem));
   // pages of this warp: page_begin + warp + 4 i
   const int mine = page_begin + warp < page_end
                        ? (page_end - (page_begin + warp) + kWarps - 1) / kWarps
                        : 0;
 
   if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&ws.bar[s], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
+    if (warp == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
   }
   // the leaders' inbox barriers are armed before any part is sent (every
   // block of the cluster takes this branch: it depends on the length only)
@@ -174,32 +188,31 @@ decode_kernel(const DecodeParams prm) {
   int my_phys = -1;
   if (lane < mine) my_phys = sm.pages[page_begin + warp + kWarps * lane];
 
-  // Copy engine: rows of this warp's i-th page into stage i % kStages. A copy
-  // instruction costs its warp a few hundred cycles whatever its size, so the
-  // K and V copies go out together from lanes 0 and 1. In the fused step the
-  // appended row is not copied from the pool.
+  // Copy engine: the (page, kv head) tiles of this warp's i-th page into
+  // stage i % kStages, whole 16-row tiles (rows past the sequence are masked
+  // or zeroed after they land). A copy instruction costs its warp a few
+  // hundred cycles whatever its size, so the K and V copies go out together
+  // from lanes 0 and 1. A page whose only row is the appended one (fused
+  // step) is not copied: that row comes from k/v.
   auto issue_copy = [&](int i, int stage, int phys) {
-    if (lane > 1) return;   // lane 0 copies the K rows, lane 1 the V rows, in one instruction
+    if (lane > 1) return;
     const int lp = page_begin + warp + kWarps * i;
     const bool ok = phys >= 0 && phys < prm.num_pages;
-    int rows = lp == last_page ? len - lp * kPage : kPage;
-    if (kFused && lp == last_page) rows = new_slot;     // the new row comes from k/v
+    const bool rows = !(kFused && lp == last_page && new_slot == 0);
     if (!ok && lane == 0) set_error(prm.err, kErrPage);
-    if (ok && rows > 0) {
-      const uint32_t bytes = static_cast<uint32_t>(rows) * kRowBytes;
-      const size_t tile = (static_cast<size_t>(phys) * kHkv + kvh) * (kPage * kDim);
-      if (lane == 0) mbar_arrive_expect_tx(&ws.bar[stage], 2 * bytes);
+    if (ok && rows) {
+      if (lane == 0) mbar_arrive_expect_tx(&bars[stage], 2 * kTileBytes);
       __syncwarp(0x3u);   // the expected bytes are set before either copy can land
-      bulk_load(lane == 0 ? ws.k[stage] : ws.v[stage], (lane == 0 ? prm.k_pool : prm.v_pool) + tile,
-                bytes, &ws.bar[stage]);
+      tma_load_tile(lane == 0 ? ws.k[stage] : ws.v[stage], lane == 0 ? &tmap_k : &tmap_v,
+                    kvh * kPage, phys, &bars[stage]);
     } else if (lane == 0) {
-      mbar_arrive(&ws.bar[stage]);
+      mbar_arrive(&bars[stage]);
     }
   };
   // Rotary angles of the position len - 1 for pairs 8 (lane & 3) .. + 7: the
-  // query rotation uses them, and so does the key rotation in lanes 0..7
-  // (chunk c = lane, c & 3 == lane & 3). The tables are constant inputs, read
-  // ahead of the wait for the previous launch.
+  // key rotation of the appended row uses them in lanes 0..7 (chunk c = lane,
+  // c & 3 == lane & 3). The tables are constant inputs, read ahead of the
+  // wait for the previous launch.
   float rcs[8], rsn[8];
   if (kRope) {
     load_angles(prm.rope_cos + static_cast<size_t>(len - 1) * (kDim / 2), lane & 3, rcs);
@@ -207,9 +220,10 @@ decode_kernel(const DecodeParams prm) {
   }
 
   // Fused step: the warp whose i_new-th page is the sequence's last page
-  // writes the appended token's K/V row to the pool and to the stage tile.
-  // Lanes 0..15 load one 16-byte chunk each (K for lanes 0..7, V for 8..15),
-  // only after the wait: k/v may come from the previous kernel.
+  // writes the appended token's K/V row to the pool, and into the stage tile
+  // once that tile has landed. Lanes 0..15 load one 16-byte chunk each (K for
+  // lanes 0..7, V for 8..15), only after the wait: k/v may come from the
+  // previous kernel.
   const int new_off = last_page - page_begin - warp;
   const int i_new = kFused && new_off >= 0 && new_off % kWarps == 0 && new_off / kWarps < mine
                         ? new_off / kWarps
@@ -223,37 +237,22 @@ decode_kernel(const DecodeParams prm) {
     }
     return val;
   };
-  // Stores the loaded chunk `val` (page i_new, in stage `stage`). With rotary
-  // tables lanes 0..7 rotate the key first, the partner chunk coming from
-  // lane ^ 4, with the angles above (`preloaded`) or loaded again (in the
-  // page loop, where rcs/rsn are no longer kept). Called by the whole warp.
-  auto place_new_row = [&](int stage, int phys, bool preloaded, uint4 val) {
-    if (phys < 0 || phys >= prm.num_pages) return;
+  // The loaded chunk `val` of the appended row into the pool (page phys);
+  // with rotary tables lanes 0..7 rotate the key first, the partner chunk
+  // coming from lane ^ 4. Returns the chunk as stored. Called by the whole warp.
+  auto store_new_row = [&](int phys, uint4 val) {
     const bool is_v = lane >= 8;
     const int c = lane & 7;
     if (kRope) {
       const uint4 partner = shfl_xor_uint4(val, 4);
-      if (lane < 8) {
-        float cs[8], sn[8];
-        if (preloaded) {
-          #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            cs[e] = rcs[e];
-            sn[e] = rsn[e];
-          }
-        } else {
-          load_angles(prm.rope_cos + static_cast<size_t>(len - 1) * (kDim / 2), c & 3, cs);
-          load_angles(prm.rope_sin + static_cast<size_t>(len - 1) * (kDim / 2), c & 3, sn);
-        }
-        val = rope_key_chunk(val, partner, c >= 4, cs, sn);
-      }
+      if (lane < 8) val = rope_key_chunk(val, partner, c >= 4, rcs, rsn);
     }
-    if (lane >= 16) return;
-    uint16_t* pool = is_v ? prm.v_pool : prm.k_pool;
-    *reinterpret_cast<uint4*>(pool + ((static_cast<size_t>(phys) * kHkv + kvh) * kPage +
-                                      new_slot) * kDim + c * 8) = val;
-    uint8_t* tile = is_v ? ws.v[stage] : ws.k[stage];
-    *reinterpret_cast<uint4*>(tile + new_slot * kRowBytes + c * 16) = val;
+    if (lane < 16 && phys >= 0 && phys < prm.num_pages) {
+      uint16_t* pool = is_v ? prm.v_pool : prm.k_pool;
+      *reinterpret_cast<uint4*>(pool + ((static_cast<size_t>(phys) * kHkv + kvh) * kPage +
+                                        new_slot) * kDim + c * 8) = val;
+    }
+    return val;
   };
 
   // prefetch; the unfused kernel defers the page holding the appended slot,
@@ -294,14 +293,14 @@ decode_kernel(const DecodeParams prm) {
   if (deferred >= 0) issue_copy(deferred, deferred, __shfl_sync(0xffffffffu, my_phys, deferred));
   int issued = n_prefetch;
 
-  const LaneRoles rl(lane);
-  float2 qa[kGroup][4], qb[kGroup][4];
-  load_q<kRope>(prm.q + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim, rl, qa, qb, rcs,
-                rsn);
-  if (new_in_prologue) place_new_row(i_new, __shfl_sync(0xffffffffu, my_phys, i_new), true, new_val);
-  __syncwarp();   // the appended row written by lanes 0..15 is read by every lane
+  uint32_t qh[8], ql[8];
+  load_q_mma<kRope>(prm.q + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim, lane,
+                    kRope ? prm.rope_cos + static_cast<size_t>(len - 1) * (kDim / 2) : nullptr,
+                    kRope ? prm.rope_sin + static_cast<size_t>(len - 1) * (kDim / 2) : nullptr,
+                    qh, ql);
+  if (new_in_prologue) new_val = store_new_row(__shfl_sync(0xffffffffu, my_phys, i_new), new_val);
 
-  WarpState st;
+  MmaState st;
   st.reset();
 
   bool timed_out = false;
@@ -312,13 +311,30 @@ decode_kernel(const DecodeParams prm) {
     const int valid = lp == last_page ? len - lp * kPage : kPage;
     return phys >= 0 && phys < prm.num_pages ? valid : 0;
   };
+  // A landed stage holding fewer than 16 live tokens or the appended row: V
+  // rows at or past `live` are zeroed (p = 0 times them must stay 0 whatever
+  // the pool held there), and the appended row goes into its slot (over
+  // what the copy brought, which may predate this step's write). The stores
+  // reach the copy engine's view (async proxy) before the stage is refilled.
+  auto patch_stage = [&](int stage, int live, bool with_new) {
+    uint8_t* vt = ws.v[stage];
+    for (int idx = live * 8 + lane; idx < kPage * 8; idx += 32)
+      *reinterpret_cast<uint4*>(vt + (idx >> 3) * kRowBytes + (idx & 7) * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
+    if (with_new && lane < 16) {
+      uint8_t* t = lane >= 8 ? ws.v[stage] : ws.k[stage];
+      const int c = lane & 7;
+      *reinterpret_cast<uint4*>(t + new_slot * kRowBytes + ((c ^ (new_slot & 7)) << 4)) = new_val;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+  };
   // after page i is consumed: the copy of page i + kStages into its stage
   auto refill = [&](int i, int stage) {
     if (i + kStages < mine) {
       const int next_phys = __shfl_sync(0xffffffffu, my_phys, i + kStages);
       issue_copy(i + kStages, stage, next_phys);
-      if (i + kStages == i_new) place_new_row(stage, next_phys, false, load_new_row());
-      __syncwarp();
+      if (i + kStages == i_new) new_val = store_new_row(next_phys, load_new_row());
       issued = i + kStages + 1;
     }
   };
@@ -327,12 +343,15 @@ decode_kernel(const DecodeParams prm) {
   for (int i = 0; i < mine; ++i) {
     const int phys = __shfl_sync(0xffffffffu, my_phys, i);
     // one verdict per warp: the page work below shuffles across all lanes
-    if (!__all_sync(0xffffffffu, mbar_wait(&ws.bar[stage], phase))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars[stage], phase))) {
       timed_out = true;
       break;
     }
     consumed = i + 1;
-    attend_page(ws.k[stage], ws.v[stage], live_of(i, phys), qa, qb, ws.p, ws.alpha, rl, st);
+    const int live = live_of(i, phys);
+    if (live < kPage || i == i_new) patch_stage(stage, live, i == i_new && live > 0);
+    attend_page_mma<kRope>(ws.k[stage], ws.v[stage], live, lane, qh, ql, st);
+    __syncwarp();   // every lane's reads of the stage are done before it is refilled
     refill(i, stage);
     if (++stage == kStages) {
       stage = 0;
@@ -342,32 +361,30 @@ decode_kernel(const DecodeParams prm) {
   if (timed_out) {
     // let this warp's copies still in flight land before the block exits
     // (each wait bounded again)
-    for (int j = consumed; j < issued; ++j) mbar_wait(&ws.bar[j % kStages], (j / kStages) & 1);
+    for (int j = consumed; j < issued; ++j) mbar_wait(&bars[j % kStages], (j / kStages) & 1);
   }
 
   if (!prm.early_trigger) pdl_launch_dependents();
 
-  // ---- warp state
-  reduce_warp_state(st);
+  // ---- block merge
   if (timed_out) {
     if (lane == 0) set_error(prm.err, kErrTimeout);
     st.m_run = -INFINITY;
     st.l_run = 0.f;
   }
+  float M, L;
+  float2 O;
+  block_merge_mma<kWarps>(sm, st, warp, lane, M, L, O);
   if constexpr (kCluster) {
     if (n_splits > 1) {
-      cluster_merge_async(sm, inbox, st, rl, warp, lane,
+      cluster_merge_async(inbox, M, L, O, warp, lane,
                           prm.out + (static_cast<size_t>(b) * kHq + kvh * kGroup) * kDim,
                           prm.err);
       return;
     }
   }
 
-  // ---- block merge (every ticket-mode block; a cluster whose sequence has
-  // a single split)
-  float M, L;
-  float2 O;
-  block_merge(sm, st, rl, warp, M, L, O);
+  // every ticket-mode block; a cluster whose sequence has a single split
   const bool merger = threadIdx.x < kMergeThreads;
   const int g = (threadIdx.x >> 5) & (kGroup - 1);
   const int d0 = 2 * (threadIdx.x & 31);
@@ -402,13 +419,73 @@ constexpr auto narrow_kernel = decode_kernel<kFused, true, kClusterWarps, kNarro
 template <bool kFused, bool kRope = false>
 constexpr auto wide_kernel = decode_kernel<kFused, true, kWideWarps, kWideStages, kRope>;
 
+// + 1 KiB: the kernel rounds the dynamic shared memory base up to 1024 bytes
 size_t smem_bytes(Shape shape) {
   switch (shape) {
-    case kNarrowShape: return sizeof(NarrowSmem) + sizeof(AsyncInbox);
-    case kWideShape: return sizeof(WideSmem) + sizeof(AsyncInbox);
-    default: return sizeof(TicketSmem);
+    case kNarrowShape: return sizeof(NarrowDecodeSmem) + sizeof(AsyncInbox) + 1024;
+    case kWideShape: return sizeof(WideDecodeSmem) + sizeof(AsyncInbox) + 1024;
+    default: return sizeof(TicketDecodeSmem) + 1024;
   }
 }
+
+// ---------------------------------------------------------------- pool tensor maps
+// The K or V pool of num_pages pages as a 3-D BF16 tensor for the copy
+// engine: (dim, kv head x 16 + token, page), rows of 128 B, pages of 16 KiB;
+// a box is one (page, kv head) tile of 16 x 64, written with the 128-byte
+// swizzle. Encoding is host work only; the last maps are kept per base
+// address (the map depends on nothing else).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool pkv_pool_tensor_map(const void* pool, int num_pages, CUtensorMap* map) {
+  constexpr int kCacheSlots = 64;
+  struct Slot {
+    const void* base;
+    int num_pages;
+    CUtensorMap map;
+  };
+  static std::mutex lock;
+  static Slot cache[kCacheSlots] = {};
+  const size_t slot = (reinterpret_cast<uintptr_t>(pool) >> 8) % kCacheSlots;
+  {
+    std::lock_guard<std::mutex> guard(lock);
+    if (cache[slot].base == pool && cache[slot].num_pages == num_pages) {
+      *map = cache[slot].map;
+      return true;
+    }
+  }
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {kDim, static_cast<cuuint64_t>(kHkv) * kPage,
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[2] = {kRowBytes, static_cast<cuuint64_t>(kHkv) * kPage * kRowBytes};
+  const cuuint32_t box[3] = {kDim, kPage, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  if (fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box,
+         elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> guard(lock);
+  cache[slot].base = pool;
+  cache[slot].num_pages = num_pages;
+  cache[slot].map = *map;
+  return true;
+}
+
+namespace {
 
 int block_threads(Shape shape) {
   return 32 * (shape == kTicketShape ? kTicketWarps
@@ -620,15 +697,19 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   }
   cfg.attrs = attrs;
   cfg.numAttrs = n_attrs;
+  CUtensorMap tk, tv;
+  if (!pkv_pool_tensor_map(k_pool, c.num_pages, &tk) ||
+      !pkv_pool_tensor_map(v_pool, c.num_pages, &tv))
+    return PKV_ERR_CUDA;
   cudaError_t e;
   if (rope) {
-    e = shape == kNarrowShape ? cudaLaunchKernelEx(&cfg, narrow_kernel<kFused, true>, prm)
-        : shape == kWideShape ? cudaLaunchKernelEx(&cfg, wide_kernel<kFused, true>, prm)
-                              : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused, true>, prm);
+    e = shape == kNarrowShape ? cudaLaunchKernelEx(&cfg, narrow_kernel<kFused, true>, tk, tv, prm)
+        : shape == kWideShape ? cudaLaunchKernelEx(&cfg, wide_kernel<kFused, true>, tk, tv, prm)
+                              : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused, true>, tk, tv, prm);
   } else {
-    e = shape == kNarrowShape ? cudaLaunchKernelEx(&cfg, narrow_kernel<kFused>, prm)
-        : shape == kWideShape ? cudaLaunchKernelEx(&cfg, wide_kernel<kFused>, prm)
-                              : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused>, prm);
+    e = shape == kNarrowShape ? cudaLaunchKernelEx(&cfg, narrow_kernel<kFused>, tk, tv, prm)
+        : shape == kWideShape ? cudaLaunchKernelEx(&cfg, wide_kernel<kFused>, tk, tv, prm)
+                              : cudaLaunchKernelEx(&cfg, ticket_kernel<kFused>, tk, tv, prm);
   }
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return pkv_check_launch();
@@ -726,9 +807,13 @@ pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_
   prm.longest_first = 0;
   prm.rope_cos = nullptr;
   prm.rope_sin = nullptr;
+  CUtensorMap tk, tv;
+  if (!pkv_pool_tensor_map(k_pool, num_pages, &tk) ||
+      !pkv_pool_tensor_map(v_pool, num_pages, &tv))
+    return PKV_ERR_CUDA;
   ticket_kernel<false><<<dim3(num_splits, kHkv, batch), block_threads(kTicketShape),
                          smem_bytes(kTicketShape),
-                         s>>>(prm);
+                         s>>>(tk, tv, prm);
   return pkv_check_launch();
 }
 

@@ -3,6 +3,7 @@
 #ifndef PKV_POOL_INTERNAL_H
 #define PKV_POOL_INTERNAL_H
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,6 +40,11 @@ inline bool pkv_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p
 inline pkv_status pkv_check_launch() {
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
+
+// pkv.cu: a K or V pool of num_pages pages as the copy engine's 3-D tensor
+// map (dim, kv head x 16 + token, page), boxes of one (page, kv head) tile
+// with the 128-byte swizzle; false if the driver refuses it.
+bool pkv_pool_tensor_map(const void* pool, int num_pages, CUtensorMap* map);
 
 // layers.cu: the multi-layer kernel's attributes and, per cluster size, how
 // many of its clusters the device holds at once (pool->layer_clusters).
