@@ -269,9 +269,11 @@ pkv_status pkv_test_layers_wait_timeout(pkv_pool_t pool, int layer_begin, int nu
  * the launches call.
  *
  * Plans (num_splits = 0): for up to 32 sequences a thread-block cluster of S
- * blocks per (sequence, kv head) in the narrow shape (3 page stages per
- * warp) with S = 16 or 8 while its blocks take at most 9/16 of the narrow
- * shape's resident slots, else the wide shape (2 stages, 4 blocks per SM)
+ * blocks per (sequence, kv head): the narrow shape (3 page stages per warp)
+ * with S = 16 or 12 while the blocks of two consecutive launches fit its
+ * resident slots, else the wide shape (2 stages, 4 blocks per SM) with S = 8
+ * while two launches fit its slots, else the narrow shape with S = 8 while
+ * one launch's blocks take at most 9/16 of its slots, else the wide shape
  * with the largest S <= 8 whose blocks take at most 27/32 of its slots;
  * larger batches take the ticket merge with ranges of 128, 64, 32 or 16
  * pages (the largest leaving >= 3 blocks per resident ticket slot for

@@ -544,11 +544,18 @@ int auto_chunk_pages(const pkv_device_figures& d, int batch) {
 //   batch 4:  narrow S = 8 (256) 2304; narrow S = 16 1404; wide S = 8 2015;
 //             async: narrow S = 8 2374, S = 7 2216, S = 6 2282; wide S = 16 1950;
 //   batch 8:  wide S = 8 (512) 3462; narrow S = 4 (256) 2680; wide S = 16 2016;
-//   batch 16: wide S = 4 (512) 4214; narrow S = 2 (256) 3187; wide S = 8 3443.
+//   batch 16: wide S = 4 (512) 4214; narrow S = 2 (256) 3187; wide S = 8 3443;
+// and with the page math on the tensor cores:
+//   batch 2:  narrow S = 12 1855; wide S = 16 1766;
+//   batch 4:  wide S = 8 (256) 2972-2974; narrow S = 8 2627-2630;
+//   batch 8:  wide S = 8 (512) 4024; wide S = 4 (256) 3886;
+//   batch 16: wide S = 4 (512) 5079; wide S = 2 (256) 4379.
 // So: the narrow shape with S = 16 or 12 when the blocks of two consecutive
 // launches fit its resident slots at once (the next layer's blocks then
-// become resident and prefetch during this one), else S = 8 when one
-// launch's blocks take at most 9/16 of the slots (256 of 456); else the wide
+// become resident and prefetch during this one); else the wide shape with
+// S = 8 when two consecutive launches fit its slots (batch 3-4); else the
+// narrow S = 8 when one launch's blocks take at most 9/16 of its slots (a
+// device with fewer wide slots); else the wide
 // shape with the largest S <= 8 whose blocks take at most 27/32 of its slots
 // (512 of 608); else (large batches) the ticket merge over page ranges.
 pkv_plan plan_decode(const pkv_device_figures& d, int batch, int num_splits) {
@@ -566,6 +573,10 @@ pkv_plan plan_decode(const pkv_device_figures& d, int batch, int num_splits) {
         p.cluster = s;
         p.shape = kNarrowShape;
       }
+    }
+    if (!p.cluster && usable(8) && 2 * static_cast<long long>(batch) * kHkv * 8 <= wide) {
+      p.cluster = 8;
+      p.shape = kWideShape;
     }
     if (!p.cluster && usable(8) && 16 * static_cast<long long>(batch) * kHkv * 8 <= 9 * narrow) {
       p.cluster = 8;

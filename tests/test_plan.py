@@ -30,7 +30,7 @@ def plan(lib, batch, num_splits=0, **kw):
 
 
 @pytest.mark.parametrize("batch,shape,splits", [
-    (1, N, 16), (2, N, 12), (3, N, 8), (4, N, 8),
+    (1, N, 16), (2, N, 12), (3, WD, 8), (4, WD, 8),
     (5, WD, 8), (8, WD, 8), (9, WD, 4), (16, WD, 4), (17, WD, 2), (32, WD, 2),
 ])
 def test_cluster_plans_by_batch(lib, batch, shape, splits):
