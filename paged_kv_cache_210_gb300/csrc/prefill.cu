@@ -18,12 +18,13 @@
 //    kv head (row = token * 4 + head), so every K/V page tile is shared by
 //    the group, as in decode; they are two row halves of 128, each the M of
 //    its own tensor-core products (M 128 is the largest a single CTA issues);
-//  * a loader warp brings Q (32 KiB) and per step 4 pages of K and of V
+//  * two loader warps bring Q (32 KiB) and per step 4 pages of K and of V
 //    (64 keys, 8 KiB each) by TMA tensor copies (cp.async.bulk.tensor) with
-//    the 128-byte swizzle, K in a 6-stage and V in a 5-stage ring, all 8
-//    pages of a step in one round (one wait for the free stages, one copy
-//    instruction across lanes 0..7); a page's tile is addressed by its id in
-//    the block table, nothing is gathered into a contiguous buffer;
+//    the 128-byte swizzle, K in a 6-stage and V in a 5-stage ring; each warp
+//    copies one tensor, a step's 4 pages in one round (one wait for the free
+//    stage, one copy instruction across lanes 0..3); a page's tile is
+//    addressed by its id in the block table, nothing is gathered into a
+//    contiguous buffer;
 //  * a score warp (one thread) issues S = Q K^T (two M 128 x N 64 x K 64
 //    products, one per row half, their K 16 slices interleaved) up to three
 //    steps ahead into three pairs of tensor-memory tiles, and two value
@@ -48,14 +49,13 @@
 //    heaviest first (the last tile of a prompt sees the most keys).
 //
 // What bounds it (measured with clock counters in an instrumented copy):
-// a step takes ~1,850 cycles. A copy round costs the loader warp ~1,800
-// cycles (the free-stage waits ~400, the 8-lane copy instruction ~1,300:
-// the SM's copy engine takes a page tile at a time), so K(j) lands just as
-// the score product wants it; the softmax threads need ~1,350 cycles of a
-// step and wait the rest for S. With the copies out of the way (one 8 KiB
-// box per tensor and step, timed in an experiment) the step is ~1,650
-// cycles, set by the hand-offs between the warps: each mbarrier wait that
-// ends a dependency costs its waiter ~200-500 cycles.
+// with one loader warp for both tensors a step took ~1,850 cycles, a copy
+// round costing that warp ~1,800 (the free-stage waits ~400, the 8-lane copy
+// instruction ~1,300), so K(j) landed just as the score product wanted it.
+// With the tensors split over two loader warps the copies keep ahead, and
+// the step (~1,650 cycles) is set by the hand-offs between the warps: each
+// mbarrier wait that ends a dependency costs its waiter ~200-500 cycles;
+// the softmax threads need ~1,350 cycles of a step.
 //
 // Every mbarrier wait is bounded (about two seconds of SM clock); a timeout
 // sets the error flag, the CTA waits (bounded) for its own copies and
@@ -86,10 +86,10 @@ constexpr int kStepKeys = 64;                        // keys per step: the S MMA
 constexpr int kStepPages = kStepKeys / kPage;        // 4
 constexpr int kSoftmaxWarps = 4 * kRowHalves;        // one per (lane quarter, row half)
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kLoadWarp = kSoftmaxWarps;             // TMA copies
-constexpr int kScoreWarp = kSoftmaxWarps + 1;        // S = Q K^T products
-constexpr int kValueWarp0 = kSoftmaxWarps + 2;       // O += P V products, one warp per row half
-constexpr int kThreads = kSoftmaxThreads + 64 + 32 * kRowHalves;
+constexpr int kLoadWarp = kSoftmaxWarps;             // TMA copies: Q and K, then V (+ 1)
+constexpr int kScoreWarp = kSoftmaxWarps + 2;        // S = Q K^T products
+constexpr int kValueWarp0 = kSoftmaxWarps + 3;       // O += P V products, one warp per row half
+constexpr int kThreads = kSoftmaxThreads + 96 + 32 * kRowHalves;
 constexpr int kKStages = kRowHalves == 2 ? 6 : 4;     // K ring
 constexpr int kVStages = kRowHalves == 2 ? 5 : 3;     // V ring
 constexpr int kSTiles = 3;                           // score (then P) tiles in tensor memory
@@ -374,59 +374,59 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_attention_kernel
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
 
-  if (warp == kLoadWarp) {
+  if (warp == kLoadWarp || warp == kLoadWarp + 1) {
     // ------------------------------------------------------------ copy engine
+    // Two loader warps, one for K (and Q), one for V: a copy round costs its
+    // warp a few hundred cycles whatever it copies, so the two tensors' rounds
+    // run side by side. Each round: lane 0 waits until the step's stage is
+    // free (its products committed) and sets the expected bytes, then lanes
+    // 0..3 copy the step's 4 pages in one instruction.
     const int lane = lane_of(tid);
+    const bool is_v = warp != kLoadWarp;
+    const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
+    const int stages = is_v ? kVStages : kKStages;
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
-      mbar_arrive_expect_tx(&sm.bar_q, kRows * kRowBytes);
-      tma_load_3d(sm.q, &tmap_q, 0, g * kGroup, row0 + tile * kTileTokens, &sm.bar_q);
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+      if (!is_v) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
+        mbar_arrive_expect_tx(&sm.bar_q, kRows * kRowBytes);
+        tma_load_3d(sm.q, &tmap_q, 0, g * kGroup, row0 + tile * kTileTokens, &sm.bar_q);
+      }
     }
-    // One round per step: lane 0 waits until the step's K and V stages are
-    // free (their products committed) and sets both expected byte counts,
-    // then lanes 0..3 copy the step's 4 K pages and lanes 4..7 its 4 V pages
-    // in one instruction. A round costs the warp a few hundred cycles
-    // whatever it copies, so the copies of a step share one.
     int issued = 0;
     bool ok = true;
     for (int j = 0; j < n_steps; ++j) {
-      const int ks = j % kKStages, vs = j % kVStages;
+      const int st = j % stages;
+      unsigned long long* full = is_v ? &sm.bar_v[st] : &sm.bar_k[st];
       bool good = true;
       if (lane == 0) {
         good = *abort_flag == 0;
-        if (good && j >= kKStages) good = mbar_wait(&sm.k_free[ks], ((j - kKStages) / kKStages) & 1);
-        if (good && j >= kVStages) good = mbar_wait(&sm.v_free[vs], ((j - kVStages) / kVStages) & 1);
+        if (good && j >= stages)
+          good = mbar_wait(is_v ? &sm.v_free[st] : &sm.k_free[st], ((j - stages) / stages) & 1);
         if (good) {
           int valid = 0;
           for (int q = 0; q < kStepPages; ++q) {
             const int lp = j * kStepPages + q;
             valid += (lp < n_pages && sm.pages[lp] >= 0) ? 1 : 0;
           }
-          const uint32_t bytes = static_cast<uint32_t>(valid) * kPage * kRowBytes;
-          mbar_arrive_expect_tx(&sm.bar_k[ks], bytes);
-          mbar_arrive_expect_tx(&sm.bar_v[vs], bytes);
+          mbar_arrive_expect_tx(full, static_cast<uint32_t>(valid) * kPage * kRowBytes);
         }
       }
       if (!__shfl_sync(0xffffffffu, good ? 1 : 0, 0)) {
         ok = false;
         break;
       }
-      if (lane < 2 * kStepPages) {
-        const bool is_v = lane >= kStepPages;
-        const int q = lane % kStepPages;
-        const int lp = j * kStepPages + q;
+      if (lane < kStepPages) {
+        const int lp = j * kStepPages + lane;
         const int page = lp < n_pages ? sm.pages[lp] : -1;
         // the pool seen as rows of 64 dims: (page, kv head, token) -> row
         if (page >= 0)
-          tma_load_2d((is_v ? sm.v[vs] : sm.k[ks]) + q * kPage * kRowBytes, is_v ? &tmap_v : &tmap_k,
-                      0, (page * kHkv + g) * kPage, is_v ? &sm.bar_v[vs] : &sm.bar_k[ks]);
+          tma_load_2d((is_v ? sm.v[st] : sm.k[st]) + lane * kPage * kRowBytes, map, 0,
+                      (page * kHkv + g) * kPage, full);
       }
       __syncwarp();
       ++issued;
     }
-    const int k_issued = issued, v_issued = issued;
     if (lane == 0) {
       if (!ok) {
         *abort_flag = 1;
@@ -434,14 +434,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_attention_kernel
       }
       // every copy issued lands before the CTA frees its memory (last phase
       // of each barrier; every wait bounded)
-      mbar_wait(&sm.bar_q, 0);
-      for (int st = 0; st < kKStages; ++st) {
-        const int uses = (k_issued - st + kKStages - 1) / kKStages;
-        if (uses > 0) mbar_wait(&sm.bar_k[st], (uses - 1) & 1);
-      }
-      for (int st = 0; st < kVStages; ++st) {
-        const int uses = (v_issued - st + kVStages - 1) / kVStages;
-        if (uses > 0) mbar_wait(&sm.bar_v[st], (uses - 1) & 1);
+      if (!is_v) mbar_wait(&sm.bar_q, 0);
+      for (int s = 0; s < stages; ++s) {
+        const int uses = (issued - s + stages - 1) / stages;
+        if (uses > 0) mbar_wait(is_v ? &sm.bar_v[s] : &sm.bar_k[s], (uses - 1) & 1);
       }
     }
   } else if (warp == kScoreWarp || (warp >= kValueWarp0 && warp < kValueWarp0 + kRowHalves)) {
