@@ -460,9 +460,10 @@ class DecodeRun:
         return (f"{shape}, {ranges}, up to {p.grid_splits * 8 * self.wl.batch} blocks"
                 + (", longest first" if p.longest_first else ""))
 
-    def step(self, marks=None, stream=None):
+    def step(self, marks=None, stream=None, before=None, after=None):
         """The 16 launches (or the one multi-layer launch); `marks` = events
-        recorded before, between and after."""
+        recorded before, between and after; `before(layer)` / `after(layer)`
+        run around each per-layer launch (stream work such as event waits)."""
         pkv, a = self.pkv, self.args
         s = stream if stream is not None else torch.cuda.current_stream()
         if marks:
@@ -475,6 +476,8 @@ class DecodeRun:
                 marks[-1].record(s)
             return
         for layer in range(self.wl.num_layers):
+            if before:
+                before(layer)
             if a.rope:
                 pkv.pkv_append_attend_rope(self.pool, layer, self.q[layer], self.k_new[layer],
                                            self.v_new[layer], self.k_pool, self.v_pool,
@@ -484,6 +487,8 @@ class DecodeRun:
                 pkv.pkv_append_attend(self.pool, layer, self.q[layer], self.k_new[layer],
                                       self.v_new[layer], self.k_pool, self.v_pool, self.table,
                                       self.lens, self.out[layer], num_splits=a.splits, stream=s)
+            if after:
+                after(layer)
             if marks and len(marks) > 2:
                 marks[layer + 1].record(s)
         if marks and len(marks) == 2:
@@ -598,13 +603,55 @@ def run_ours(args, world, rank, local):
     e2e_start, _ = make_event()
     e2e_end, _ = make_event()
 
+    # With large layers the copies overlap the layers: the inputs go over on
+    # a copy stream in two parts, layer 0's (which the first launch waits
+    # for) and then the other layers' (which the second launch waits for,
+    # copied while layer 0 runs); layer l's output comes back on a second
+    # copy stream once layer l is done, while the later layers run. With
+    # small layers (under 1 MiB of output each) the fixed cost of the extra
+    # copies and, in the direct calls, of issuing them exceeds what they
+    # hide, so all inputs go first and all outputs come back at the end, as
+    # with the one multi-layer launch.
+    h2d_stream = torch.cuda.Stream(device=dev)
+    d2h_stream = torch.cuda.Stream(device=dev)
+    n_layers = wl.num_layers
+    in_ev = [torch.cuda.Event() for _ in range(2)]
+    out_ev = [torch.cuda.Event() for _ in range(n_layers)]
+
+    pipelined = (not args.persistent and
+                 run.out[0].numel() * run.out.element_size() >= (1 << 20))
+
     def e2e_body(s):
-        run.q.copy_(q_h, non_blocking=True)
-        run.k_new.copy_(kn_h, non_blocking=True)
-        run.v_new.copy_(vn_h, non_blocking=True)
-        run.lens.copy_(lens_h, non_blocking=True)
-        run.step(stream=s)
-        out_h.copy_(run.out, non_blocking=True)
+        if not pipelined:
+            run.q.copy_(q_h, non_blocking=True)
+            run.k_new.copy_(kn_h, non_blocking=True)
+            run.v_new.copy_(vn_h, non_blocking=True)
+            run.lens.copy_(lens_h, non_blocking=True)
+            run.step(stream=s)
+            out_h.copy_(run.out, non_blocking=True)
+            return
+        h2d_stream.wait_stream(s)
+        d2h_stream.wait_stream(s)
+        with torch.cuda.stream(h2d_stream):
+            run.lens.copy_(lens_h, non_blocking=True)
+            for part, rows in enumerate((slice(0, 1), slice(1, n_layers))):
+                run.q[rows].copy_(q_h[rows], non_blocking=True)
+                run.k_new[rows].copy_(kn_h[rows], non_blocking=True)
+                run.v_new[rows].copy_(vn_h[rows], non_blocking=True)
+                in_ev[part].record(h2d_stream)
+
+        def before(layer):
+            if layer < 2:
+                s.wait_event(in_ev[layer])
+
+        def after(layer):
+            out_ev[layer].record(s)
+            d2h_stream.wait_event(out_ev[layer])
+            with torch.cuda.stream(d2h_stream):
+                out_h[layer].copy_(run.out[layer], non_blocking=True)
+
+        run.step(stream=s, before=before, after=after)
+        s.wait_stream(d2h_stream)
 
     e2e_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(e2e_graph, stream=stream):
@@ -720,8 +767,12 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_total / len(e2e_ms), 5),
-                "how": "step's CUDA graph replayed with the pinned host->device input copies "
-                       "and the device->host output copy captured in it (device events)",
+                "how": ("step's CUDA graph replayed with the pinned host->device input copies "
+                        "and the device->host output copies captured in it (device events)"
+                        + ("" if not pipelined else
+                           "; inputs on a copy stream in two parts (layer 0, then the "
+                           "rest while layer 0 runs), each layer's output back on a second "
+                           "copy stream while the later layers run")),
                 "ms_per_step_direct_calls": round(direct_ms, 5),
                 "gbs_direct_calls": round(world * gbs(nbytes, direct_ms), 2),
                 "direct_calls_how": f"{launches} C-ABI calls issued from Python each step "
