@@ -362,8 +362,10 @@ struct MmaState {
 // pairs 2 s and 2 s + 1. Lanes 16..31 hold zeros. kRope: q is first rotated
 // in FP32 by the angles of its position (cos_row, sin_row: the 32 pair
 // angles; dim d < 32 pairs with d + 32, the partner half coming from lane
-// L ^ 2) and kept as BF16 high (qh) and low (ql) parts; otherwise q is exact
-// in BF16 and ql is zero.
+// L ^ 2) and kept as a BF16 high part in rows 0..3 and a BF16 low part in
+// the otherwise empty rows 4..7 (lanes 16..31), so one set of products
+// gives both halves' scores; otherwise q is exact in BF16. ql is zero
+// (kept for the signature).
 template <bool kRope>
 __device__ __forceinline__ void load_q_mma(const uint16_t* qrow, int lane, const float* cos_row,
                                            const float* sin_row, uint32_t (&qh)[8],
@@ -403,8 +405,12 @@ __device__ __forceinline__ void load_q_mma(const uint16_t* qrow, int lane, const
     const float r1 = fmaf(own.y, cs[2 * i + 1], sgn * par.y * sn[2 * i + 1]);
     const uint32_t hi = float2_to_bf16x2(r0, r1);
     const float2 hf = bf16x2_to_float2(hi);
-    qh[i] = lane < 16 ? hi : 0u;
-    ql[i] = lane < 16 ? float2_to_bf16x2(r0 - hf.x, r1 - hf.y) : 0u;
+    const uint32_t lo = float2_to_bf16x2(r0 - hf.x, r1 - hf.y);
+    // the low parts ride in the padding rows 4..7 (lanes 16..31) of the same
+    // products; the scores of the two halves are added after them
+    const uint32_t lo_of_head = __shfl_xor_sync(0xffffffffu, lo, 16);
+    qh[i] = lane < 16 ? hi : lo_of_head;
+    ql[i] = 0u;
   }
   }
 }
@@ -430,7 +436,10 @@ __device__ __forceinline__ void attend_page_mma(const uint8_t* kt, const uint8_t
     #pragma unroll
     for (int sl = 0; sl < 4; ++sl) {
       mma_bf16_16816(d, qh[2 * sl], qh[2 * sl + 1], kw[2 * sl], kw[2 * sl + 1]);
-      if (kRope) mma_bf16_16816(d, ql[2 * sl], ql[2 * sl + 1], kw[2 * sl], kw[2 * sl + 1]);
+    }
+    if (kRope) {   // rows g and g + 4: the high and low parts of head g's q
+      d[0] += __shfl_xor_sync(0xffffffffu, d[0], 16);
+      d[1] += __shfl_xor_sync(0xffffffffu, d[1], 16);
     }
     s[2 * nt] = d[0];
     s[2 * nt + 1] = d[1];
