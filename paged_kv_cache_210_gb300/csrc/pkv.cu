@@ -240,12 +240,21 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // The loaded chunk `val` of the appended row into the pool (page phys);
   // with rotary tables lanes 0..7 rotate the key first, the partner chunk
   // coming from lane ^ 4. Returns the chunk as stored. Called by the whole warp.
-  auto store_new_row = [&](int phys, uint4 val) {
+  auto store_new_row = [&](int phys, uint4 val, bool preloaded) {
     const bool is_v = lane >= 8;
     const int c = lane & 7;
     if (kRope) {
       const uint4 partner = shfl_xor_uint4(val, 4);
-      if (lane < 8) val = rope_key_chunk(val, partner, c >= 4, rcs, rsn);
+      if (lane < 8) {
+        if (preloaded) {
+          val = rope_key_chunk(val, partner, c >= 4, rcs, rsn);
+        } else {   // in the page loop the angles are read again (from cache)
+          float cs[8], sn[8];
+          load_angles(prm.rope_cos + static_cast<size_t>(len - 1) * (kDim / 2), c & 3, cs);
+          load_angles(prm.rope_sin + static_cast<size_t>(len - 1) * (kDim / 2), c & 3, sn);
+          val = rope_key_chunk(val, partner, c >= 4, cs, sn);
+        }
+      }
     }
     if (lane < 16 && phys >= 0 && phys < prm.num_pages) {
       uint16_t* pool = is_v ? prm.v_pool : prm.k_pool;
@@ -298,7 +307,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     kRope ? prm.rope_cos + static_cast<size_t>(len - 1) * (kDim / 2) : nullptr,
                     kRope ? prm.rope_sin + static_cast<size_t>(len - 1) * (kDim / 2) : nullptr,
                     qh, ql);
-  if (new_in_prologue) new_val = store_new_row(__shfl_sync(0xffffffffu, my_phys, i_new), new_val);
+  if (new_in_prologue)
+    new_val = store_new_row(__shfl_sync(0xffffffffu, my_phys, i_new), new_val, true);
 
   MmaState st;
   st.reset();
@@ -334,7 +344,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (i + kStages < mine) {
       const int next_phys = __shfl_sync(0xffffffffu, my_phys, i + kStages);
       issue_copy(i + kStages, stage, next_phys);
-      if (i + kStages == i_new) new_val = store_new_row(next_phys, load_new_row());
+      if (i + kStages == i_new) new_val = store_new_row(next_phys, load_new_row(), false);
       issued = i + kStages + 1;
     }
   };
