@@ -455,10 +455,13 @@ class DecodeRun:
             return "one persistent launch for all layers (cluster per (sequence, kv head))"
         if p.cluster:
             return f"{shape}, S = {p.num_splits} ({p.grid_splits * 8 * self.wl.batch} blocks)"
+        if p.longest_first:
+            return (f"{shape}, (sequence, range) units longest first, ranges of at least "
+                    f"{p.chunk_pages} pages sized to the batch (pages / {p.range_div}), "
+                    f"{p.grid_units * 8} blocks")
         ranges = (f"{p.num_splits} ranges" if p.num_splits else
                   f"ranges of {p.chunk_pages} pages")
-        return (f"{shape}, {ranges}, up to {p.grid_splits * 8 * self.wl.batch} blocks"
-                + (", longest first" if p.longest_first else ""))
+        return f"{shape}, {ranges}, {p.grid_splits * 8 * self.wl.batch} blocks"
 
     def step(self, marks=None, stream=None, before=None, after=None):
         """The 16 launches (or the one multi-layer launch); `marks` = events

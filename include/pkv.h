@@ -275,9 +275,18 @@ pkv_status pkv_test_layers_wait_timeout(pkv_pool_t pool, int layer_begin, int nu
  * while two launches fit its slots, else the narrow shape with S = 8 while
  * one launch's blocks take at most 9/16 of its slots, else the wide shape
  * with the largest S <= 8 whose blocks take at most 27/32 of its slots;
- * larger batches take the ticket merge with ranges of 128, 64, 32 or 16
- * pages (the largest leaving >= 3 blocks per resident ticket slot for
- * full-length sequences, at least max_seq_len / 16 / max_splits). A chosen
+ * larger batches take the ticket merge with ranges of at least chunk_pages
+ * = max(16, ceil(max_seq_len / 16 / max_splits)) pages. When the blocks of
+ * full-length sequences would exceed one wave of resident ticket blocks,
+ * the launch has the grid (1, 8, grid_units), its blocks taking (sequence,
+ * range) units longest sequence first. Up to two waves of sequences
+ * (batch x 8 <= 2 x resident ticket blocks) it sizes the ranges from the
+ * lengths it reads: max(chunk_pages, min(128, ceil(T / range_div))) pages,
+ * T the batch's total page count (one kv head), range_div = resident
+ * ticket blocks x 5 / 72 (about 1.8 times the pages per resident block
+ * slot), grid_units = batch + range_div. Past two waves every sequence is
+ * one unit (chunk_pages = max_seq_len / 16, grid_units = batch). Otherwise
+ * the grid is (grid_splits, 8, batch). A chosen
  * num_splits = S takes a cluster for 2 <= S <= max_cluster (narrow while its
  * blocks fit one wave of it, else wide), the ticket merge otherwise. */
 typedef struct {
@@ -298,10 +307,15 @@ typedef struct {
   int shape;          /* PKV_SHAPE_* */
   int cluster;        /* blocks per cluster (the split count) for the cluster shapes, else 0 */
   int num_splits;     /* splits per sequence (cluster plans, chosen counts), else 0 */
-  int chunk_pages;    /* pages per range when num_splits == 0, else 0 */
-  int grid_splits;    /* blocks per (sequence, kv head) in the grid */
+  int chunk_pages;    /* pages per range when num_splits == 0 (the least, with range_div), else 0 */
+  int range_div;      /* longest first: ranges of max(chunk_pages, min(128, ceil(T / range_div)))
+                         pages, T the batch's pages; else 0 */
+  int grid_splits;    /* blocks per (sequence, kv head) in the grid (longest first: the most
+                         ranges a sequence can have) */
+  int grid_units;     /* longest first: (sequence, range) units in the grid (its z), each
+                         8 blocks (one per kv head); else 0 */
   int early_trigger;  /* the grid fits one wave: dependents may start after the prefetch */
-  int longest_first;  /* several waves of ticket blocks: sequences taken longest first */
+  int longest_first;  /* several waves of ticket blocks: units taken longest sequence first */
 } pkv_plan;
 
 /* INVALID_ARG for null pointers, figures out of range (num_sms, blocks per

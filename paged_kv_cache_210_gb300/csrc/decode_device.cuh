@@ -97,7 +97,7 @@ struct alignas(1024) DecodeSmem {
     struct {                           // longest-first order (prologue only)
       int hist[kMaxPages + 1];
       int wsum[kWarps];
-      int pick[3];
+      int pick[5];                     // bucket, rank in it, sequence, range, range size
     } order;
   };
   int pages[kMaxPages];      // this sequence's block-table row
@@ -143,8 +143,10 @@ struct DecodeParams {
   int max_splits;
   int num_splits;             // > 0: S ranges per sequence
   int chunk_pages;            // > 0: ranges of this many pages (used when num_splits == 0)
+  int range_div;              // longest first: ranges of at least ceil(batch pages / range_div)
+  int batch;
   int early_trigger;          // let the next launch start right after the prefetch (one wave)
-  int longest_first;          // blockIdx.z is a rank by length, not a sequence index
+  int longest_first;          // grid (1, kv heads, units), units longest sequence first
   const float* rope_cos;      // rotary angles [max_seq_len][32] FP32, or null: no rotation
   const float* rope_sin;
 };
@@ -664,23 +666,37 @@ __device__ __forceinline__ void cluster_merge_async(AsyncInbox& inbox, float M, 
 }
 
 // ---------------------------------------------------------------- dispatch order
-// Blocks start in linear block order (x fastest, z slowest). With mixed
-// lengths, handing out the longest sequences first shortens the launch's
-// tail (the longest-processing-time-first rule), so a ticket-mode launch
-// reads blockIdx.z as a rank: rank z is the z-th sequence by page count,
-// most pages first, ties by index. Each block finds its own sequence with a
-// counting sort of the page counts in shared memory: O(batch / threads +
-// 128) work and four block barriers, reading only seq_lens (which may be
-// read before the wait for the previous launch).
-__device__ __forceinline__ int page_count(int len) {
-  return min(max((len + kPage - 1) / kPage, 0), kMaxPages);
+// Blocks start in linear block order (x fastest). With mixed lengths,
+// handing out the longest sequences first shortens the launch's tail (the
+// longest-processing-time-first rule), and ranges sized to the batch keep
+// the blocks' work even. So a longest-first ticket launch has the grid
+// (1, kv heads, units): unit u is the u-th (sequence, range) pair with the
+// sequences ordered by page count, most pages first, ties by index, and each
+// sequence's ranges in order. The range size comes from the batch itself:
+// at least `least_pages`, else ceil(T / range_div) for T the batch's pages
+// (per kv head), at most kMaxPages. Since ceil(p / r) < p / r + 1 and
+// r >= T / range_div (or r = kMaxPages, one range per sequence), the units
+// number fewer than batch + range_div, the units in the grid. Each block finds
+// its own unit with a counting sort of the page counts in shared memory:
+// O(batch / threads + 128) work and four block barriers, reading only
+// seq_lens (which may be read before the wait for the previous launch).
+// Pages of a sequence, clamped to [0, max_pages] (an over-long sequence
+// counts as max_pages: its blocks only report the length).
+__device__ __forceinline__ int page_count(int len, int max_pages) {
+  return min(max((len + kPage - 1) / kPage, 0), max_pages);
 }
 
-// Returns -1 without the second pass when `useful(pages)` says a block of
-// that rank has no work (split slots past the sequence's last range).
-template <int kWarps, class Smem, class Useful>
-__device__ int longest_first_sequence(int z, int batch, const int32_t* seq_lens, Smem& sm,
-                                      Useful useful) {
+// Returns the sequence of unit u (and its range index and the range size),
+// or -1 past the last unit. A sequence of length < 1 has one unit (its block
+// reports the length). max_pages <= kMaxPages: the handle's pages per
+// sequence. kWhole: ranges of all of max_pages (least_pages >= max_pages),
+// every sequence one unit and the grid one unit per sequence, so the pass
+// skips the page total and the range arithmetic: every block's first
+// copies wait on it.
+template <int kWarps, bool kWhole, class Smem>
+__device__ int longest_first_unit(int u, int batch, const int32_t* seq_lens, int max_pages,
+                                  int least_pages, int range_div, Smem& sm, int& split,
+                                  int& range_pages) {
   constexpr int kThreads = kWarps * 32;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -689,7 +705,7 @@ __device__ int longest_first_sequence(int z, int batch, const int32_t* seq_lens,
   #pragma unroll
   for (int e = 0; e < kHeld; ++e) {
     const int s = static_cast<int>(threadIdx.x) + e * kThreads;
-    held[e] = s < batch ? page_count(seq_lens[s]) : -1;
+    held[e] = s < batch ? page_count(seq_lens[s], max_pages) : -1;
   }
   for (int i = threadIdx.x; i <= kMaxPages; i += kThreads) sm.order.hist[i] = 0;
   __syncthreads();
@@ -697,16 +713,39 @@ __device__ int longest_first_sequence(int z, int batch, const int32_t* seq_lens,
   for (int e = 0; e < kHeld; ++e)
     if (held[e] >= 0) atomicAdd(&sm.order.hist[held[e]], 1);
   for (int s = static_cast<int>(threadIdx.x) + kHeld * kThreads; s < batch; s += kThreads)
-    atomicAdd(&sm.order.hist[page_count(seq_lens[s])], 1);
+    atomicAdd(&sm.order.hist[page_count(seq_lens[s], max_pages)], 1);
   __syncthreads();
-  // bucket of rank z: lane l owns the buckets kMaxPages - 4l - e (e < 4),
-  // most pages first; bucket 0 comes last
+  // lane l owns the buckets kMaxPages - 4l - e (e < 4), most pages first;
+  // bucket 0 comes last
   if (warp == 0) {
-    int cnt[4], sum = 0;
+    int cnt[4];
+    #pragma unroll
+    for (int e = 0; e < 4; ++e) cnt[e] = sm.order.hist[kMaxPages - 4 * lane - e];
+    // Split launches: the ranges of a p-page sequence, ceil(p / range), and
+    // the unit's rank and range come by float reciprocals (exact here: p +
+    // range - 1 < 256, so a true quotient is an integer or at least 1/128
+    // above one, and the rank is corrected by one step), not divisions.
+    int range = least_pages;
+    float inv_range = 0.f;
+    if constexpr (!kWhole) {
+      int pages = 0;
+      #pragma unroll
+      for (int e = 0; e < 4; ++e) pages += cnt[e] * (kMaxPages - 4 * lane - e);
+      #pragma unroll
+      for (int o = 16; o > 0; o >>= 1) pages += __shfl_xor_sync(0xffffffffu, pages, o);
+      if (range_div > 0)
+        range = max(least_pages, min(kMaxPages, (pages + range_div - 1) / range_div));
+      inv_range = __frcp_rn(static_cast<float>(range));
+    }
+    auto ranges_of = [&](int p) {
+      if constexpr (kWhole) return 1;
+      return static_cast<int>(static_cast<float>(p + range - 1) * inv_range + (1.f / 256.f));
+    };
+    int units[4], sum = 0;
     #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      cnt[e] = sm.order.hist[kMaxPages - 4 * lane - e];
-      sum += cnt[e];
+      units[e] = kWhole ? cnt[e] : cnt[e] * ranges_of(kMaxPages - 4 * lane - e);
+      sum += units[e];
     }
     int incl = sum;
     #pragma unroll
@@ -717,22 +756,47 @@ __device__ int longest_first_sequence(int z, int batch, const int32_t* seq_lens,
     int excl = incl - sum;
     #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      if (z >= excl && z < excl + cnt[e]) {
-        sm.order.pick[0] = kMaxPages - 4 * lane - e;
-        sm.order.pick[1] = z - excl;
+      if (u >= excl && u < excl + units[e]) {
+        const int p = kMaxPages - 4 * lane - e;
+        sm.order.pick[0] = p;
+        if constexpr (kWhole) {
+          sm.order.pick[1] = u - excl;
+        } else {
+          const int per_seq = ranges_of(p);
+          const int off = u - excl;
+          int k = off;
+          if (per_seq > 1) {
+            k = static_cast<int>(__fdividef(static_cast<float>(off), static_cast<float>(per_seq)));
+            if (k * per_seq > off) --k;
+            if ((k + 1) * per_seq <= off) ++k;
+          }
+          sm.order.pick[1] = k;
+          sm.order.pick[3] = off - k * per_seq;
+        }
       }
-      excl += cnt[e];
+      excl += units[e];
     }
     const int total = __shfl_sync(0xffffffffu, incl, 31);
-    if (lane == 0 && z >= total) {
-      sm.order.pick[0] = 0;
-      sm.order.pick[1] = z - total;
+    if (lane == 0) {
+      if (u >= total) {   // the sequences without pages, then nothing
+        sm.order.pick[0] = 0;
+        sm.order.pick[1] = u - total;
+        if constexpr (!kWhole) sm.order.pick[3] = 0;
+      }
+      if constexpr (!kWhole) sm.order.pick[4] = range;
     }
   }
   __syncthreads();
   const int p = sm.order.pick[0];
   const int k = sm.order.pick[1];
-  if (!useful(p)) return -1;                // the same decision in every thread
+  if constexpr (kWhole) {
+    split = 0;
+    range_pages = least_pages;
+  } else {
+    split = sm.order.pick[3];
+    range_pages = sm.order.pick[4];
+    if (p == 0 && k >= sm.order.hist[0]) return -1;   // the same decision in every thread
+  }
   // the k-th sequence (by index) with p pages
   int seen = 0;
   auto scan = [&](int s, int pc) {          // one pass over kThreads sequences
@@ -757,7 +821,7 @@ __device__ int longest_first_sequence(int z, int batch, const int32_t* seq_lens,
   }
   for (int base = kHeld * kThreads; base < batch && seen <= k; base += kThreads) {
     const int s = base + static_cast<int>(threadIdx.x);
-    scan(s, s < batch ? page_count(seq_lens[s]) : -1);
+    scan(s, s < batch ? page_count(seq_lens[s], max_pages) : -1);
   }
   return sm.order.pick[2];
 }

@@ -116,22 +116,22 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   uint8_t* smem_base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Smem& sm = *reinterpret_cast<Smem*>(smem_base);
 
-  const int split = blockIdx.x;
+  int split = blockIdx.x;
   const int kvh = blockIdx.y;
   int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Ticket plans: ranges of chunk_pages pages; a longest-first launch has
+  // the grid (1, kv heads, units) and sizes its ranges to the batch.
+  int range_pages = prm.chunk_pages;
   if (!kCluster && prm.longest_first) {
-    // a split slot past the last range of a sequence with this many pages
-    // has nothing to do (split 0 always goes on: it reports invalid lengths)
-    auto useful = [&](int pages) {
-      if (split == 0) return true;
-      const int chunk = prm.num_splits > 0 ? (pages + prm.num_splits - 1) / prm.num_splits
-                                           : prm.chunk_pages;
-      return pages > 0 && split < (pages + chunk - 1) / chunk;
-    };
-    b = longest_first_sequence<kWarps>(static_cast<int>(blockIdx.z), static_cast<int>(gridDim.z),
-                                       prm.seq_lens, sm, useful);
+    const int u = static_cast<int>(blockIdx.z);
+    b = prm.range_div == 0
+            ? longest_first_unit<kWarps, true>(u, prm.batch, prm.seq_lens, prm.table_stride,
+                                               prm.chunk_pages, 0, sm, split, range_pages)
+            : longest_first_unit<kWarps, false>(u, prm.batch, prm.seq_lens, prm.table_stride,
+                                                prm.chunk_pages, prm.range_div, sm, split,
+                                                range_pages);
     if (b < 0) return;
   }
 
@@ -149,7 +149,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
   const int n_pages = (len + kPage - 1) / kPage;
   const int chunk = prm.num_splits > 0 ? (n_pages + prm.num_splits - 1) / prm.num_splits
-                                       : prm.chunk_pages;
+                                       : range_pages;
   const int n_splits = (n_pages + chunk - 1) / chunk;   // non-empty splits of this sequence
   if (kCluster) {
     if (n_splits == 1 && split > 0) return;   // the same decision in every block of the cluster
@@ -520,28 +520,39 @@ static_assert(kTicketShape == PKV_SHAPE_TICKET && kNarrowShape == PKV_SHAPE_NARR
                   kWideShape == PKV_SHAPE_WIDE,
               "the plan's shape codes are the kernel shapes");
 
-// Pages per block when the caller leaves the choice to the library and the
-// batch is too large for a cluster split: the largest of 128, 64, 32, 16
-// pages for which a batch of full-length sequences still yields at least
-// three (sequence, kv head, range) blocks per resident block slot. Fewer
-// blocks per slot leave SMs idle behind the longest sequences; more, smaller
-// ranges pay a partial merge for nothing (measured: 256 sequences run best
-// unsplit, 64 log-uniform ones with 32-page ranges).
-int auto_chunk_pages(const pkv_device_figures& d, int batch) {
-  const int max_pages = d.max_seq_len / kPage;
-  const int min_chunk = (max_pages + d.max_splits - 1) / d.max_splits;
-  const long long resident = static_cast<long long>(d.ticket_blocks_per_sm) * d.num_sms;
-  int chunk = 16;
-  for (int c = 128; c >= 16; c /= 2) {
-    const long long blocks = static_cast<long long>(batch) * kHkv * ((max_pages + c - 1) / c);
-    if (blocks >= 3 * resident) {
-      chunk = c;
-      break;
-    }
-  }
-  if (chunk > max_pages) chunk = max_pages;
-  return chunk < min_chunk ? min_chunk : chunk;
-}
+// Ticket plans when the caller leaves the choice to the library: ranges of
+// at least kLeastRangePages pages (and few enough per sequence for the
+// partial rows). When the blocks of full-length sequences would not fit one
+// wave of resident ticket blocks, the launch takes (sequence, range) units
+// longest sequence first. Up to kSplitWaves waves of sequences, it sizes the
+// ranges to the batch it finds: ceil(T / range_div) pages, T the batch's
+// pages per kv head, range_div = resident blocks x 5 / 72, i.e. about 1.8
+// times the pages per resident block slot (8 kv heads); sequences longer
+// than that split, the rest run whole. Past that many sequences every
+// sequence runs whole. Measured on a 152-SM GB300 (GB/s per 16-layer fused
+// step; the log-uniform and uniform batches of 64 and 256 are the
+// configured workloads). Ranges of one fixed size:
+//   log-uniform b48:  32 3798, 40 3827, 48 3604, 64 3290, 128 2358
+//   log-uniform b64:  32 3562, 40 3803, 48 3990, 56 3760, 64 3500, 128 2687
+//   log-uniform b96:  32 3495, 48 3901, 64 4220, 96 3502, 128 3123
+//   log-uniform b128: 48 4163, 64 4534, 96 4563, 128 4228
+//   log-uniform b256: 64 5008, 96 5164, 128 5448
+//   uniform b64:      48 4541, 64 4978, 96 5142, 128 4790
+//   uniform b256:     64 6080, 96 6303, 128 6329
+//   full-length b40:  48 4995, 96 4497, 128 5322; b64: 64 5705, 128 6241
+// Ranges sized to the batch, range_div 34 / 38 / 42 / 46:
+//   log-uniform b48 3511 / 3634 / 3794 / 3804; b64 3706 / 3817 / 3927 / 3950;
+//   b96 3964 / 4140 / 4281 / 4166; b128 4456 / 4605 / 4736 / 4622;
+//   uniform b64 4794 / 4937 / 5042 / 5132; full-length b33 4471 / 4815 /
+//   5048 / 4969, b36 5505 / 4829 / 4946 / 5098, b40 5331 / 5516 / 4644 / 4520
+// (a full-length batch just short of range_div sequences splits each into
+// a long and a short range). Splitting into even ranges (round(p / r) of
+// them) lost 5-15 % on the mixes. A grid with a fixed count of blocks per
+// (sequence, kv head), most of them empty for short sequences, cost up to
+// 6 %, hence the units; spare units cost 1-3 % at 256 sequences, hence
+// whole sequences past kSplitWaves waves.
+constexpr int kLeastRangePages = 16;
+constexpr int kSplitWaves = 2;
 
 // The launch plan for a batch. Cluster plans when the library chooses: the
 // split count S (16, 12, 8, 4, 2) and the block shape, from sweeps on a
@@ -601,7 +612,8 @@ pkv_plan plan_decode(const pkv_device_figures& d, int batch, int num_splits) {
     if (p.cluster) {
       p.num_splits = p.cluster;
     } else {
-      p.chunk_pages = auto_chunk_pages(d, batch);
+      p.chunk_pages = std::max(std::min(kLeastRangePages, max_pages),
+                               (max_pages + d.max_splits - 1) / d.max_splits);
     }
   } else {
     p.num_splits = num_splits;
@@ -615,14 +627,26 @@ pkv_plan plan_decode(const pkv_device_figures& d, int batch, int num_splits) {
   }
   p.grid_splits = p.num_splits > 0 ? p.num_splits
                                    : (max_pages + p.chunk_pages - 1) / p.chunk_pages;
-  const long long blocks = static_cast<long long>(p.grid_splits) * kHkv * batch;
+  long long blocks = static_cast<long long>(p.grid_splits) * kHkv * batch;
   const int per_sm = p.shape == kNarrowShape  ? d.narrow_blocks_per_sm
                      : p.shape == kWideShape ? d.wide_blocks_per_sm
                                              : d.ticket_blocks_per_sm;
   const long long resident = static_cast<long long>(per_sm) * d.num_sms;
-  p.early_trigger = blocks <= resident ? 1 : 0;
-  // more than one wave of ticket-mode blocks: longest sequences first
+  // more than one wave of ticket-mode blocks: units, longest first
   p.longest_first = (!p.cluster && num_splits == 0 && blocks > resident) ? 1 : 0;
+  if (p.longest_first) {
+    if (static_cast<long long>(batch) * kHkv > kSplitWaves * resident) {
+      // enough sequences to fill the slots whole: no ranges (and no empty units)
+      p.chunk_pages = max_pages;
+      p.grid_splits = 1;
+      p.grid_units = batch;
+    } else {
+      p.range_div = static_cast<int>(std::max<long long>(resident * 5 / 72, 1));
+      p.grid_units = batch + p.range_div;
+    }
+    blocks = static_cast<long long>(p.grid_units) * kHkv;
+  }
+  p.early_trigger = blocks <= resident ? 1 : 0;
   return p;
 }
 
@@ -694,11 +718,14 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   const int grid_splits = plan.grid_splits;
   prm.num_splits = plan.num_splits;
   prm.chunk_pages = plan.chunk_pages;
+  prm.range_div = plan.range_div;
+  prm.batch = batch;
   prm.early_trigger = plan.early_trigger;
   prm.longest_first = plan.longest_first;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid_splits, kHkv, batch);
+  cfg.gridDim = plan.longest_first ? dim3(1, kHkv, plan.grid_units)
+                                    : dim3(grid_splits, kHkv, batch);
   cfg.blockDim = dim3(block_threads(shape), 1, 1);
   cfg.dynamicSmemBytes = smem_bytes(shape);
   cfg.stream = static_cast<cudaStream_t>(stream);
@@ -824,6 +851,8 @@ pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_
   prm.max_splits = num_splits;     // partial rows are (sequence, head) x num_splits
   prm.num_splits = num_splits;
   prm.chunk_pages = 0;
+  prm.range_div = 0;
+  prm.batch = batch;
   prm.early_trigger = 1;   // launched without programmatic dependent launch: no effect
   prm.longest_first = 0;
   prm.rope_cos = nullptr;

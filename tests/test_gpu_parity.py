@@ -571,21 +571,33 @@ def test_large_batch_fused_chain_matches_oracle(pdl):
 
 
 # ------------------------------------------------------------ large-batch plans
-@pytest.mark.parametrize("case", ["mix", "equal-lengths", "2048-short"])
+@pytest.mark.parametrize("case", ["mix", "equal-lengths", "2048-short", "units-near-bound",
+                                  "one-long", "ranges-just-past"])
 @pytest.mark.parametrize("fused", [True, False])
 def test_large_batch_plans_match_oracle(case, fused):
     """Batches the library splits into page ranges merged by ticket and hands
-    out longest sequence first: a log-uniform length mix with page-boundary
-    lengths, many sequences of equal length (ranks among equals), and 2048
-    short sequences; two layers chained with programmatic dependent launch in
-    a CUDA graph, replayed twice (the tickets must come back to zero),
-    against the oracle."""
+    out longest sequence first, ranges sized to the batch's pages: a
+    log-uniform length mix with page-boundary lengths, many sequences of
+    equal length (ranks among equals), 2048 short sequences, 39 sequences of
+    17 pages beside one of one page (16-page ranges: 79 units, three short
+    of the grid's batch + range_div on a 152-SM device), one 2048-token
+    sequence beside 63 one-token ones (eight 16-page ranges), and 40
+    sequences of 25 pages (1000 pages: 24-page ranges on a 152-SM device,
+    so every sequence ends in a one-page range); two layers chained with programmatic dependent
+    launch in a CUDA graph, replayed twice (the tickets must come back to
+    zero), against the oracle."""
     rng = np.random.default_rng(480)
     if case == "mix":
         lens = np.clip(np.round(np.exp(rng.uniform(np.log(16), np.log(2048), 72))), 1, 2048)
         lens[:8] = [1, 16, 17, 512, 513, 2047, 2048, 33]
     elif case == "equal-lengths":
         lens = np.array([300] * 50 + [16] * 30 + [2048] * 5 + [1] * 10)
+    elif case == "units-near-bound":
+        lens = np.array([16 * 17] * 39 + [16])
+    elif case == "one-long":
+        lens = np.array([2048] + [1] * 63)
+    elif case == "ranges-just-past":
+        lens = np.array([16 * 24 + 1] * 40)
     else:
         lens = rng.integers(1, 40, 2048)
     wl = W.custom(lens.astype(np.int32), num_layers=2, seed=481, hole_every=3, name=case)

@@ -39,16 +39,54 @@ def test_cluster_plans_by_batch(lib, batch, shape, splits):
     assert p.grid_splits == splits and p.longest_first == 0 and p.early_trigger == 1
 
 
-@pytest.mark.parametrize("batch,chunk", [(33, 16), (64, 32), (100, 32), (128, 64), (256, 128),
-                                         (1000, 128)])
-def test_ticket_plans_by_batch(lib, batch, chunk):
+@pytest.mark.parametrize("batch", [33, 34, 35, 64, 100, 128, 152])
+def test_ticket_plans_by_batch(lib, batch):
     p = plan(lib, batch)
-    assert (p.shape, p.cluster, p.num_splits, p.chunk_pages) == (T, 0, 0, chunk)
-    assert p.grid_splits == 128 // chunk
-    blocks = batch * 8 * p.grid_splits
-    # at least three blocks per resident ticket slot, so several waves
-    assert blocks >= 3 * 4 * 152
+    # ranges of at least 16 pages, sized in the launch from the batch's pages
+    assert (p.shape, p.cluster, p.num_splits, p.chunk_pages, p.grid_splits) == (T, 0, 0, 16, 8)
+    assert p.longest_first == 1
+    # 608 resident ticket blocks x 5 / 72: ranges of about 1.8 x the pages per slot
+    assert p.range_div == 42 and p.grid_units == batch + 42
+    assert p.early_trigger == int((batch + 42) * 8 <= 4 * 152)
+
+
+@pytest.mark.parametrize("batch", [153, 256, 1000])
+def test_ticket_plans_unsplit_past_two_waves(lib, batch):
+    """Batches whose sequences alone fill two waves of ticket blocks run each
+    sequence whole, longest first, with no spare units."""
+    p = plan(lib, batch)
+    assert (p.shape, p.chunk_pages, p.grid_splits, p.range_div, p.grid_units) == (
+        T, 128, 1, 0, batch)
     assert p.longest_first == 1 and p.early_trigger == 0
+
+
+def units_of(lens, least, range_div, max_pages=128):
+    """The (sequence, range) units a longest-first launch enumerates, in order."""
+    pages = [min(max((n + 15) // 16, 0), max_pages) for n in lens]
+    r = max(least, min(128, -(-sum(pages) // range_div))) if range_div else least
+    order = sorted(range(len(lens)), key=lambda s: (pages[s] == 0, -pages[s], s))
+    return r, [(s, k) for s in order for k in range(max(1, -(-pages[s] // r)))]
+
+
+def test_units_fit_the_grid():
+    """Fewer units than batch + range_div for any lengths (the grid's units):
+    random mixes, lengths just past a multiple of the range, and invalid
+    lengths; every sequence's ranges cover its pages once."""
+    import random
+    rnd = random.Random(7)
+    cases = [[rnd.choice([0, 1, 17, 33, 257, 2048, 2049, rnd.randint(1, 2048)])
+              for _ in range(rnd.randint(1, 300))] for _ in range(300)]
+    cases += [[16 * 17 + 1] * 35 + [1] * 5, [2048] + [1] * 63, [16 * 16 + 1] * 40]
+    for lens in cases:
+        for rd, mp, least in ((1, 128, 16), (5, 128, 16), (38, 128, 16), (76, 128, 16),
+                              (38, 16, 16), (0, 128, 128), (0, 16, 16)):
+            r, units = units_of(lens, least, rd, mp)
+            assert len(units) < len(lens) + max(rd, 1)
+            for s, n in enumerate(lens):
+                p = min(max((n + 15) // 16, 0), mp)
+                ks = [k for (t, k) in units if t == s]
+                assert ks == list(range(max(1, -(-p // r))))
+                assert p == 0 or (len(ks) - 1) * r < p <= len(ks) * r
 
 
 def test_every_library_plan_keeps_its_limits(lib):
@@ -68,13 +106,26 @@ def test_every_library_plan_keeps_its_limits(lib):
                         # the whole launch is one wave of its shape's blocks
                         assert batch * 8 * s <= per_sm * sms
                         assert p.early_trigger == 1 and p.longest_first == 0
+                        assert p.range_div == 0 and p.grid_units == 0
                     else:
                         assert p.shape == T and p.num_splits == 0
-                        c = p.chunk_pages
-                        assert c in (16, 32, 64, 128) or c == -(-128 // max_splits)
-                        assert p.grid_splits == -(-128 // c) <= max_splits
-                        waves = batch * 8 * p.grid_splits > 4 * sms
-                        assert p.longest_first == int(waves) and p.early_trigger == int(not waves)
+                        least = max(16, -(-128 // max_splits))
+                        waves = batch * 8 * -(-128 // least) > 4 * sms
+                        assert p.longest_first == int(waves)
+                        if waves and batch * 8 > 2 * 4 * sms:      # unsplit
+                            assert (p.chunk_pages, p.grid_splits, p.range_div) == (128, 1, 0)
+                            assert p.grid_units == batch and p.early_trigger == 0
+                        elif waves:
+                            assert p.chunk_pages == least
+                            assert p.grid_splits == -(-128 // least) <= max_splits
+                            assert p.range_div == max(4 * sms * 5 // 72, 1)
+                            assert p.grid_units == batch + p.range_div
+                            assert p.early_trigger == int(p.grid_units * 8 <= 4 * sms)
+                        else:
+                            assert p.chunk_pages == least
+                            assert p.grid_splits == -(-128 // least) <= max_splits
+                            assert p.range_div == 0 and p.grid_units == 0
+                            assert p.early_trigger == 1
 
 
 def test_chosen_split_counts(lib):
