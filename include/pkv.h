@@ -283,8 +283,8 @@ pkv_status pkv_test_layers_wait_timeout(pkv_pool_t pool, int layer_begin, int nu
  * (batch x 8 <= 2 x resident ticket blocks) it sizes the ranges from the
  * lengths it reads: max(chunk_pages, min(128, ceil(T / range_div))) pages,
  * T the batch's total page count (one kv head), range_div = resident
- * ticket blocks x 5 / 72 (about 1.8 times the pages per resident block
- * slot), grid_units = batch + range_div. Past two waves every sequence is
+ * ticket blocks x 3 / 40, rounded (about 1.65 times the pages per resident
+ * block slot), grid_units = batch + range_div. Past two waves every sequence is
  * one unit (chunk_pages = max_seq_len / 16, grid_units = batch). Otherwise
  * the grid is (grid_splits, 8, batch). A chosen
  * num_splits = S takes a cluster for 2 <= S <= max_cluster (narrow while its
@@ -314,7 +314,6 @@ typedef struct {
                          ranges a sequence can have) */
   int grid_units;     /* longest first: (sequence, range) units in the grid (its z), each
                          8 blocks (one per kv head); else 0 */
-  int early_trigger;  /* the grid fits one wave: dependents may start after the prefetch */
   int longest_first;  /* several waves of ticket blocks: units taken longest sequence first */
 } pkv_plan;
 

@@ -73,7 +73,7 @@ class DeviceFigures(ctypes.Structure):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "shape", "cluster", "num_splits", "chunk_pages", "range_div", "grid_splits",
-        "grid_units", "early_trigger", "longest_first")]
+        "grid_units", "longest_first")]
 
 
 PKV_SHAPE_TICKET, PKV_SHAPE_NARROW, PKV_SHAPE_WIDE = 0, 1, 2

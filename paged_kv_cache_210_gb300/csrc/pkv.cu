@@ -287,14 +287,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (line) prefetch_l2(line);
   }
   pdl_wait();
-  // A launch that fits in one wave of resident blocks lets the next launch
-  // start now, so its blocks prefetch while this one computes; a larger
-  // launch triggers after its page loop, so waiting blocks of the next
-  // launch do not take slots this launch's later blocks need. Either way the
-  // trigger comes after the wait: the next launch's pre-wait reads then start
-  // only once every launch before this one has completed, so only the launch
-  // immediately before it can still be writing.
-  if (prm.early_trigger) pdl_launch_dependents();
+  // The next launch may start once every block of this one has passed this
+  // point, so its blocks take the slots this launch frees and prefetch their
+  // pages while this launch's last blocks run (no block of this launch is
+  // still waiting for a slot then: each has started). The trigger comes
+  // after the wait: the next launch's pre-wait reads then start only once
+  // every launch before this one has completed, so only the launch
+  // immediately before it can still be writing. (Measured on GB300 against
+  // a trigger after the page loop for launches of several waves: batch-256
+  // ragged step 6508 vs 6404 GB/s, batch-64 mix 4175 vs 3878.)
+  pdl_launch_dependents();
   // the new row's load goes out before q's, so the two latencies overlap
   const bool new_in_prologue = i_new >= 0 && i_new < n_prefetch;
   uint4 new_val = make_uint4(0u, 0u, 0u, 0u);
@@ -374,7 +376,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     for (int j = consumed; j < issued; ++j) mbar_wait(&bars[j % kStages], (j / kStages) & 1);
   }
 
-  if (!prm.early_trigger) pdl_launch_dependents();
 
   // ---- block merge
   if (timed_out) {
@@ -526,12 +527,13 @@ static_assert(kTicketShape == PKV_SHAPE_TICKET && kNarrowShape == PKV_SHAPE_NARR
 // wave of resident ticket blocks, the launch takes (sequence, range) units
 // longest sequence first. Up to kSplitWaves waves of sequences, it sizes the
 // ranges to the batch it finds: ceil(T / range_div) pages, T the batch's
-// pages per kv head, range_div = resident blocks x 5 / 72, i.e. about 1.8
-// times the pages per resident block slot (8 kv heads); sequences longer
-// than that split, the rest run whole. Past that many sequences every
-// sequence runs whole. Measured on a 152-SM GB300 (GB/s per 16-layer fused
-// step; the log-uniform and uniform batches of 64 and 256 are the
-// configured workloads). Ranges of one fixed size:
+// pages per kv head, range_div = resident blocks x 3 / 40 (rounded), i.e.
+// about 1.65 times the pages per resident block slot (8 kv heads);
+// sequences longer than that split, the rest run whole. Past that many
+// sequences every sequence runs whole. Measured on a 152-SM GB300 (GB/s per
+// 16-layer fused step; the log-uniform and uniform batches of 64 and 256
+// are the configured workloads). Ranges of one fixed size (dependents
+// triggered after the page loop):
 //   log-uniform b48:  32 3798, 40 3827, 48 3604, 64 3290, 128 2358
 //   log-uniform b64:  32 3562, 40 3803, 48 3990, 56 3760, 64 3500, 128 2687
 //   log-uniform b96:  32 3495, 48 3901, 64 4220, 96 3502, 128 3123
@@ -540,17 +542,20 @@ static_assert(kTicketShape == PKV_SHAPE_TICKET && kNarrowShape == PKV_SHAPE_NARR
 //   uniform b64:      48 4541, 64 4978, 96 5142, 128 4790
 //   uniform b256:     64 6080, 96 6303, 128 6329
 //   full-length b40:  48 4995, 96 4497, 128 5322; b64: 64 5705, 128 6241
-// Ranges sized to the batch, range_div 34 / 38 / 42 / 46:
-//   log-uniform b48 3511 / 3634 / 3794 / 3804; b64 3706 / 3817 / 3927 / 3950;
-//   b96 3964 / 4140 / 4281 / 4166; b128 4456 / 4605 / 4736 / 4622;
-//   uniform b64 4794 / 4937 / 5042 / 5132; full-length b33 4471 / 4815 /
-//   5048 / 4969, b36 5505 / 4829 / 4946 / 5098, b40 5331 / 5516 / 4644 / 4520
+// Ranges sized to the batch, range_div 38 / 42 / 46 / 50 (dependents
+// triggered after the wait):
+//   log-uniform b48 3939 / 4048 / 4292 / 4279; b64 3950 / 4214 / 4239 / 4039;
+//   b96 4369 / 4393 / 4227 / 4084; b128 4695 / 4815 / 4708 / 4613;
+//   uniform b64 5046 / 5233 / 5469 / 5443; b128 6494 / 6481 / 6465 / 6450;
+//   full-length b33 4833 / 5078 / 5315 / 5466, b36 4865 / 5202 / 5347 / 5578,
+//   b40 5357 / 4667 / 4693 / 4491
 // (a full-length batch just short of range_div sequences splits each into
 // a long and a short range). Splitting into even ranges (round(p / r) of
 // them) lost 5-15 % on the mixes. A grid with a fixed count of blocks per
 // (sequence, kv head), most of them empty for short sequences, cost up to
-// 6 %, hence the units; spare units cost 1-3 % at 256 sequences, hence
-// whole sequences past kSplitWaves waves.
+// 6 %, hence the units; spare units cost 3-5 % at 192 and 256 sequences
+// (log-uniform b192 4944 vs 5087 whole, b256 5299 vs 5578), hence whole
+// sequences past kSplitWaves waves.
 constexpr int kLeastRangePages = 16;
 constexpr int kSplitWaves = 2;
 
@@ -627,7 +632,7 @@ pkv_plan plan_decode(const pkv_device_figures& d, int batch, int num_splits) {
   }
   p.grid_splits = p.num_splits > 0 ? p.num_splits
                                    : (max_pages + p.chunk_pages - 1) / p.chunk_pages;
-  long long blocks = static_cast<long long>(p.grid_splits) * kHkv * batch;
+  const long long blocks = static_cast<long long>(p.grid_splits) * kHkv * batch;
   const int per_sm = p.shape == kNarrowShape  ? d.narrow_blocks_per_sm
                      : p.shape == kWideShape ? d.wide_blocks_per_sm
                                              : d.ticket_blocks_per_sm;
@@ -641,12 +646,10 @@ pkv_plan plan_decode(const pkv_device_figures& d, int batch, int num_splits) {
       p.grid_splits = 1;
       p.grid_units = batch;
     } else {
-      p.range_div = static_cast<int>(std::max<long long>(resident * 5 / 72, 1));
+      p.range_div = static_cast<int>(std::max<long long>((resident * 3 + 20) / 40, 1));
       p.grid_units = batch + p.range_div;
     }
-    blocks = static_cast<long long>(p.grid_units) * kHkv;
   }
-  p.early_trigger = blocks <= resident ? 1 : 0;
   return p;
 }
 
@@ -720,7 +723,6 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   prm.chunk_pages = plan.chunk_pages;
   prm.range_div = plan.range_div;
   prm.batch = batch;
-  prm.early_trigger = plan.early_trigger;
   prm.longest_first = plan.longest_first;
 
   cudaLaunchConfig_t cfg = {};
@@ -853,7 +855,6 @@ pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_
   prm.chunk_pages = 0;
   prm.range_div = 0;
   prm.batch = batch;
-  prm.early_trigger = 1;   // launched without programmatic dependent launch: no effect
   prm.longest_first = 0;
   prm.rope_cos = nullptr;
   prm.rope_sin = nullptr;

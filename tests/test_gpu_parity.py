@@ -578,11 +578,11 @@ def test_large_batch_plans_match_oracle(case, fused):
     """Batches the library splits into page ranges merged by ticket and hands
     out longest sequence first, ranges sized to the batch's pages: a
     log-uniform length mix with page-boundary lengths, many sequences of
-    equal length (ranks among equals), 2048 short sequences, 39 sequences of
-    17 pages beside one of one page (16-page ranges: 79 units, three short
+    equal length (ranks among equals), 2048 short sequences, 43 sequences of
+    17 pages beside one of one page (16-page ranges: 87 units, three short
     of the grid's batch + range_div on a 152-SM device), one 2048-token
-    sequence beside 63 one-token ones (eight 16-page ranges), and 40
-    sequences of 25 pages (1000 pages: 24-page ranges on a 152-SM device,
+    sequence beside 63 one-token ones (eight 16-page ranges), and 44
+    sequences of 25 pages (1100 pages: 24-page ranges on a 152-SM device,
     so every sequence ends in a one-page range); two layers chained with programmatic dependent
     launch in a CUDA graph, replayed twice (the tickets must come back to
     zero), against the oracle."""
@@ -593,11 +593,11 @@ def test_large_batch_plans_match_oracle(case, fused):
     elif case == "equal-lengths":
         lens = np.array([300] * 50 + [16] * 30 + [2048] * 5 + [1] * 10)
     elif case == "units-near-bound":
-        lens = np.array([16 * 17] * 39 + [16])
+        lens = np.array([16 * 17] * 43 + [16])
     elif case == "one-long":
         lens = np.array([2048] + [1] * 63)
     elif case == "ranges-just-past":
-        lens = np.array([16 * 24 + 1] * 40)
+        lens = np.array([16 * 24 + 1] * 44)
     else:
         lens = rng.integers(1, 40, 2048)
     wl = W.custom(lens.astype(np.int32), num_layers=2, seed=481, hole_every=3, name=case)

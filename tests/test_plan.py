@@ -36,7 +36,7 @@ def plan(lib, batch, num_splits=0, **kw):
 def test_cluster_plans_by_batch(lib, batch, shape, splits):
     p = plan(lib, batch)
     assert (p.shape, p.cluster, p.num_splits, p.chunk_pages) == (shape, splits, splits, 0)
-    assert p.grid_splits == splits and p.longest_first == 0 and p.early_trigger == 1
+    assert p.grid_splits == splits and p.longest_first == 0
 
 
 @pytest.mark.parametrize("batch", [33, 34, 35, 64, 100, 128, 152])
@@ -45,9 +45,8 @@ def test_ticket_plans_by_batch(lib, batch):
     # ranges of at least 16 pages, sized in the launch from the batch's pages
     assert (p.shape, p.cluster, p.num_splits, p.chunk_pages, p.grid_splits) == (T, 0, 0, 16, 8)
     assert p.longest_first == 1
-    # 608 resident ticket blocks x 5 / 72: ranges of about 1.8 x the pages per slot
-    assert p.range_div == 42 and p.grid_units == batch + 42
-    assert p.early_trigger == int((batch + 42) * 8 <= 4 * 152)
+    # 608 resident ticket blocks x 3 / 40: ranges of about 1.65 x the pages per slot
+    assert p.range_div == 46 and p.grid_units == batch + 46
 
 
 @pytest.mark.parametrize("batch", [153, 256, 1000])
@@ -57,7 +56,7 @@ def test_ticket_plans_unsplit_past_two_waves(lib, batch):
     p = plan(lib, batch)
     assert (p.shape, p.chunk_pages, p.grid_splits, p.range_div, p.grid_units) == (
         T, 128, 1, 0, batch)
-    assert p.longest_first == 1 and p.early_trigger == 0
+    assert p.longest_first == 1
 
 
 def units_of(lens, least, range_div, max_pages=128):
@@ -105,7 +104,7 @@ def test_every_library_plan_keeps_its_limits(lib):
                         per_sm = 3 if p.shape == N else 4
                         # the whole launch is one wave of its shape's blocks
                         assert batch * 8 * s <= per_sm * sms
-                        assert p.early_trigger == 1 and p.longest_first == 0
+                        assert p.longest_first == 0
                         assert p.range_div == 0 and p.grid_units == 0
                     else:
                         assert p.shape == T and p.num_splits == 0
@@ -114,18 +113,16 @@ def test_every_library_plan_keeps_its_limits(lib):
                         assert p.longest_first == int(waves)
                         if waves and batch * 8 > 2 * 4 * sms:      # unsplit
                             assert (p.chunk_pages, p.grid_splits, p.range_div) == (128, 1, 0)
-                            assert p.grid_units == batch and p.early_trigger == 0
+                            assert p.grid_units == batch
                         elif waves:
                             assert p.chunk_pages == least
                             assert p.grid_splits == -(-128 // least) <= max_splits
-                            assert p.range_div == max(4 * sms * 5 // 72, 1)
+                            assert p.range_div == max((4 * sms * 3 + 20) // 40, 1)
                             assert p.grid_units == batch + p.range_div
-                            assert p.early_trigger == int(p.grid_units * 8 <= 4 * sms)
                         else:
                             assert p.chunk_pages == least
                             assert p.grid_splits == -(-128 // least) <= max_splits
                             assert p.range_div == 0 and p.grid_units == 0
-                            assert p.early_trigger == 1
 
 
 def test_chosen_split_counts(lib):
