@@ -607,10 +607,12 @@ def run_ours(args, world, rank, local):
     e2e_end, _ = make_event()
 
     # With large layers the copies overlap the layers: the inputs go over on
-    # a copy stream in two parts, layer 0's (which the first launch waits
-    # for) and then the other layers' (which the second launch waits for,
-    # copied while layer 0 runs); layer l's output comes back on a second
-    # copy stream once layer l is done, while the later layers run. With
+    # a copy stream in three parts (layer 0's, which the first launch waits
+    # for; layers 1-3, copied while layer 0 runs; the rest, copied while
+    # layers 1-3 run), each launch waiting for the part holding its layer;
+    # layer l's output comes back on a second copy stream once layer l is
+    # done, while the later layers run (measured at batch 256: one copy per
+    # layer cost more per copy than it hid). With
     # small layers (under 1 MiB of output each) the fixed cost of the extra
     # copies and, in the direct calls, of issuing them exceeds what they
     # hide, so all inputs go first and all outputs come back at the end, as
@@ -618,7 +620,11 @@ def run_ours(args, world, rank, local):
     h2d_stream = torch.cuda.Stream(device=dev)
     d2h_stream = torch.cuda.Stream(device=dev)
     n_layers = wl.num_layers
-    in_ev = [torch.cuda.Event() for _ in range(2)]
+    # input parts: layer 0, then layers 1-3 (copied while layer 0 runs), then
+    # the rest (copied while layers 1-3 run)
+    in_parts = [slice(0, 1), slice(1, min(4, n_layers)), slice(min(4, n_layers), n_layers)]
+    in_parts = [p for p in in_parts if p.start < p.stop]
+    in_ev = [torch.cuda.Event() for _ in in_parts]
     out_ev = [torch.cuda.Event() for _ in range(n_layers)]
 
     pipelined = (not args.persistent and
@@ -637,15 +643,16 @@ def run_ours(args, world, rank, local):
         d2h_stream.wait_stream(s)
         with torch.cuda.stream(h2d_stream):
             run.lens.copy_(lens_h, non_blocking=True)
-            for part, rows in enumerate((slice(0, 1), slice(1, n_layers))):
+            for part, rows in enumerate(in_parts):
                 run.q[rows].copy_(q_h[rows], non_blocking=True)
                 run.k_new[rows].copy_(kn_h[rows], non_blocking=True)
                 run.v_new[rows].copy_(vn_h[rows], non_blocking=True)
                 in_ev[part].record(h2d_stream)
 
         def before(layer):
-            if layer < 2:
-                s.wait_event(in_ev[layer])
+            for part, rows in enumerate(in_parts):
+                if layer == rows.start:
+                    s.wait_event(in_ev[part])
 
         def after(layer):
             out_ev[layer].record(s)
@@ -773,9 +780,10 @@ def run_ours(args, world, rank, local):
                 "how": ("step's CUDA graph replayed with the pinned host->device input copies "
                         "and the device->host output copies captured in it (device events)"
                         + ("" if not pipelined else
-                           "; inputs on a copy stream in two parts (layer 0, then the "
-                           "rest while layer 0 runs), each layer's output back on a second "
-                           "copy stream while the later layers run")),
+                           "; inputs on a copy stream in three parts (layer 0, layers "
+                           "1-3 while layer 0 runs, the rest while layers 1-3 run), each "
+                           "layer's output back on a second copy stream while the later "
+                           "layers run")),
                 "ms_per_step_direct_calls": round(direct_ms, 5),
                 "gbs_direct_calls": round(world * gbs(nbytes, direct_ms), 2),
                 "direct_calls_how": f"{launches} C-ABI calls issued from Python each step "
