@@ -145,6 +145,7 @@ struct DecodeParams {
   int chunk_pages;            // > 0: ranges of this many pages (used when num_splits == 0)
   int range_div;              // longest first: ranges of at least ceil(batch pages / range_div)
   int batch;
+  long long resident_blocks;  // resident blocks of the launch's shape (0: no block counts as late)
   int longest_first;          // grid (1, kv heads, units), units longest sequence first
   const float* rope_cos;      // rotary angles [max_seq_len][32] FP32, or null: no rotation
   const float* rope_sin;

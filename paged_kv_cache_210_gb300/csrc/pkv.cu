@@ -121,6 +121,21 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // A block past the first wave of resident blocks starts only once a slot
+  // has been left, so there is nothing to prefetch ahead of the wait: it
+  // waits and lets the next launch start right away, before its own
+  // prologue, so the launch's trigger does not wait on the prologues of its
+  // last blocks (the wait still comes first in every block).
+  // (Cluster launches fit one wave.)
+  const bool late =
+      !kCluster && prm.resident_blocks > 0 &&
+      static_cast<long long>(blockIdx.x) +
+              gridDim.x * (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z) >=
+          prm.resident_blocks;
+  if (late) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   // Ticket plans: ranges of chunk_pages pages; a longest-first launch has
   // the grid (1, kv heads, units) and sizes its ranges to the batch.
   int range_pages = prm.chunk_pages;
@@ -286,17 +301,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     if (line) prefetch_l2(line);
   }
-  pdl_wait();
-  // The next launch may start once every block of this one has passed this
-  // point, so its blocks take the slots this launch frees and prefetch their
-  // pages while this launch's last blocks run (no block of this launch is
-  // still waiting for a slot then: each has started). The trigger comes
-  // after the wait: the next launch's pre-wait reads then start only once
-  // every launch before this one has completed, so only the launch
-  // immediately before it can still be writing. (Measured on GB300 against
-  // a trigger after the page loop for launches of several waves: batch-256
-  // ragged step 6508 vs 6404 GB/s, batch-64 mix 4175 vs 3878.)
-  pdl_launch_dependents();
+  if (!late) {
+    pdl_wait();
+    // The next launch may start once every block of this one has passed
+    // this point, so its blocks take the slots this launch frees and
+    // prefetch their pages while this launch's last blocks run (no block of
+    // this launch is still waiting for a slot then: each has started). The
+    // trigger comes after the wait: the next launch's pre-wait reads then
+    // start only once every launch before this one has completed, so only
+    // the launch immediately before it can still be writing. (Measured on
+    // GB300 against a trigger after the page loop for launches of several
+    // waves: batch-256 ragged step 6508 vs 6404 GB/s, batch-64 mix 4175 vs
+    // 3878.)
+    pdl_launch_dependents();
+  }
   // the new row's load goes out before q's, so the two latencies overlap
   const bool new_in_prologue = i_new >= 0 && i_new < n_prefetch;
   uint4 new_val = make_uint4(0u, 0u, 0u, 0u);
@@ -375,7 +393,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // (each wait bounded again)
     for (int j = consumed; j < issued; ++j) mbar_wait(&bars[j % kStages], (j / kStages) & 1);
   }
-
 
   // ---- block merge
   if (timed_out) {
@@ -723,6 +740,10 @@ pkv_status launch_decode(pkv_pool_t pool, int layer, const void* q, const void* 
   prm.chunk_pages = plan.chunk_pages;
   prm.range_div = plan.range_div;
   prm.batch = batch;
+  prm.resident_blocks = static_cast<long long>(
+      plan.shape == kNarrowShape ? pool->cluster_blocks_per_sm
+      : plan.shape == kWideShape ? pool->wide_blocks_per_sm
+                                 : pool->blocks_per_sm) * pool->num_sms;
   prm.longest_first = plan.longest_first;
 
   cudaLaunchConfig_t cfg = {};
@@ -855,6 +876,7 @@ pkv_status pkv_decode_attention_noalloc(int layer, const void* q, const void* k_
   prm.chunk_pages = 0;
   prm.range_div = 0;
   prm.batch = batch;
+  prm.resident_blocks = 0;   // launched without programmatic dependent launch
   prm.longest_first = 0;
   prm.rope_cos = nullptr;
   prm.rope_sin = nullptr;
