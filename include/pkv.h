@@ -147,8 +147,9 @@ pkv_status pkv_append(pkv_pool_t pool, int layer, const void* k, const void* v, 
  * partials and a ticket (the last block to finish merges). num_splits = 0
  * lets the library choose: for up to 32 sequences a cluster split and a
  * block shape (page stages per warp, blocks per SM) from plans measured on
- * GB300, for larger batches ranges of a fixed page count with the ticket
- * merge, longest sequences first.
+ * GB300, for larger batches the ticket merge over page ranges sized in the
+ * launch from the batch's lengths (whole sequences past two waves of
+ * blocks), longest sequences first (pkv_plan_decode below).
  * S must not exceed max_splits. The
  * output does not depend on which physical pages hold the data. A sequence
  * with an invalid seq_len is skipped (its out rows are left untouched) and
