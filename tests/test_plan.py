@@ -157,3 +157,35 @@ def test_invalid_arguments(lib):
     for batch, splits in ((0, 0), (-1, 0), (2, -1), (2, 65)):
         with pytest.raises(pkv.PkvError):
             plan(lib, batch, splits)
+
+
+def test_ranges_per_sequence_by_float_reciprocal():
+    """The launch counts a p-page sequence's ranges, ceil(p / r), as
+    trunc(float32(p + r - 1) * rcp(r) + 1/256) and a unit's rank k = off / n
+    as trunc(off / n) corrected by one step, with float32 arithmetic instead
+    of integer division. Checked here for every p, r <= 128 and the offsets a
+    grid can hold, with the product and the add rounded separately and as one
+    fused multiply-add (the compiler may contract them), and with the rank's
+    quotient off by up to 3 ulp (the fast division)."""
+    import numpy as np
+    f32 = np.float32
+    for r in range(1, 129):
+        inv = f32(1.0) / f32(r)                      # correctly rounded reciprocal
+        p = np.arange(1, 129, dtype=np.int64)
+        x = (p + r - 1).astype(f32)
+        sep = (x * inv + f32(1.0 / 256.0)).astype(f32)
+        fused = (x.astype(np.float64) * np.float64(inv) + 1.0 / 256.0).astype(f32)
+        want = -(-p // r)
+        assert np.array_equal(sep.astype(np.int64), want)
+        assert np.array_equal(fused.astype(np.int64), want)
+    off = np.arange(0, 65536 + 256, dtype=np.int64)
+    for n in range(2, 9):
+        q = off.astype(f32) / f32(n)
+        for ulps in (-3, 0, 3):
+            qq = q
+            for _ in range(abs(ulps)):
+                qq = np.nextafter(qq, f32(np.inf) if ulps > 0 else f32(-np.inf)).astype(f32)
+            k = qq.astype(np.int64)
+            k = np.where(k * n > off, k - 1, k)
+            k = np.where((k + 1) * n <= off, k + 1, k)
+            assert np.array_equal(k, off // n)
