@@ -455,6 +455,8 @@ class DecodeRun:
             return "one persistent launch for all layers (cluster per (sequence, kv head))"
         if p.cluster:
             return f"{shape}, S = {p.num_splits} ({p.grid_splits * 8 * self.wl.batch} blocks)"
+        if p.longest_first and p.range_div == 0:
+            return (f"{shape}, whole sequences longest first, {p.grid_units * 8} blocks")
         if p.longest_first:
             return (f"{shape}, (sequence, range) units longest first, ranges of at least "
                     f"{p.chunk_pages} pages sized to the batch (pages / {p.range_div}), "
