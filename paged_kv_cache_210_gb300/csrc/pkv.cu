@@ -279,17 +279,35 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     return val;
   };
 
-  // prefetch; the unfused kernel defers the page holding the appended slot,
-  // which the preceding append kernel may still be writing
+  // Prefetch: the first n_prefetch pages' tiles in one copy instruction,
+  // lane 2i (K) and 2i + 1 (V) serving page i, so the warp pays one copy
+  // round instead of n_prefetch before its first page can land; the rules
+  // are issue_copy's. The unfused kernel defers the page holding the
+  // appended slot, which the preceding append kernel may still be writing.
   const int n_prefetch = min(mine, kStages);
   int deferred = -1;
-  for (int i = 0; i < n_prefetch; ++i) {
+  {
+    const int i = lane >> 1;
     const int phys = __shfl_sync(0xffffffffu, my_phys, i);
-    if (!kFused && page_begin + warp + kWarps * i == last_page) {
-      deferred = i;
-    } else {
-      issue_copy(i, i, phys);
+    const int lp = page_begin + warp + kWarps * i;
+    const bool serves = i < n_prefetch && (kFused || lp != last_page);
+    const bool ok = phys >= 0 && phys < prm.num_pages;
+    const bool rows = !(kFused && lp == last_page && new_slot == 0);
+    if (serves && (lane & 1) == 0) {
+      if (!ok) set_error(prm.err, kErrPage);
+      if (ok && rows) {
+        mbar_arrive_expect_tx(&bars[i], 2 * kTileBytes);
+      } else {
+        mbar_arrive(&bars[i]);
+      }
     }
+    __syncwarp();   // every stage's expected bytes are set before any copy can land
+    if (serves && ok && rows)
+      tma_load_tile((lane & 1) == 0 ? ws.k[i] : ws.v[i], (lane & 1) == 0 ? &tmap_k : &tmap_v,
+                    kvh * kPage, phys, &bars[i]);
+    if (!kFused)
+      for (int j = 0; j < n_prefetch; ++j)
+        if (page_begin + warp + kWarps * j == last_page) deferred = j;
   }
   // q of the 4 heads (512 B) and, fused, the new k/v rows into L2 ahead of the wait
   if (warp == 0 && lane < 6 && active) {
