@@ -1,5 +1,5 @@
 """bench.py's JSON contract on the CPU: the reference arm (the FP64 oracle,
-timed on the host) prints one line with the keys the driver reads, and the
+timed on the host) prints one JSON line with the benchmark contract's keys, and the
 argument checks reject combinations the library does not run."""
 
 import json
