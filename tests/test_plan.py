@@ -189,3 +189,78 @@ def test_ranges_per_sequence_by_float_reciprocal():
             k = np.where(k * n > off, k - 1, k)
             k = np.where((k + 1) * n <= off, k + 1, k)
             assert np.array_equal(k, off // n)
+
+
+def device_unit_of(u, lens, least, range_div, max_pages=128):
+    """The decode launch's unit lookup restated step by step (one block, one
+    unit): the page-count histogram, lane l of warp 0 owning the buckets
+    128 - 4l - e, the range size from the page total, the units per bucket,
+    the inclusive scan over lanes, the bucket holding unit u with the rank
+    and range index inside it (float32 quotient corrected by one step), then
+    the k-th sequence by index with that page count. Returns (sequence,
+    range index) or None past the last unit."""
+    import numpy as np
+    f32 = np.float32
+    pc = [min(max((n + 15) // 16, 0), max_pages) for n in lens]
+    hist = [0] * 129
+    for p in pc:
+        hist[p] += 1
+    whole = range_div == 0 and least >= max_pages
+    rng = least
+    if not whole and range_div > 0:
+        total_pages = sum(hist[p] * p for p in range(1, 129))
+        rng = max(least, min(128, -(-total_pages // range_div)))
+    inv = f32(1.0) / f32(rng)
+
+    def ranges_of(p):
+        if whole:
+            return 1
+        return int(f32(f32(p + rng - 1) * inv) + f32(1.0 / 256.0))
+    lane_units = []
+    for lane in range(32):
+        lane_units.append([hist[128 - 4 * lane - e] * ranges_of(128 - 4 * lane - e)
+                           for e in range(4)])
+    incl = list(np.cumsum([sum(x) for x in lane_units]))
+    pick = None
+    for lane in range(32):
+        excl = incl[lane] - sum(lane_units[lane])
+        for e in range(4):
+            if excl <= u < excl + lane_units[lane][e]:
+                p = 128 - 4 * lane - e
+                per = ranges_of(p)
+                off = u - excl
+                k = off if per == 1 else int(f32(off) / f32(per))
+                if k * per > off:
+                    k -= 1
+                if (k + 1) * per <= off:
+                    k += 1
+                pick = (p, k, off - k * per)
+            excl += lane_units[lane][e]
+    total = incl[-1]
+    if u >= total:
+        pick = (0, u - total, 0)
+    p, k, split = pick
+    if p == 0 and k >= hist[0]:
+        return None
+    same = [s for s in range(len(lens)) if pc[s] == p]
+    return same[k], split
+
+
+def test_device_unit_lookup_matches_the_order():
+    """Every unit of the grid maps, by the device's lookup, to the unit at
+    that place in the plain order (page count descending, index, range),
+    and the units past the last map to nothing: random and adversarial
+    batches, split and whole-sequence launches."""
+    import random
+    rnd = random.Random(11)
+    cases = [[rnd.choice([0, 1, 16, 17, 300, 2048, rnd.randint(1, 2048)])
+              for _ in range(rnd.randint(1, 120))] for _ in range(40)]
+    cases += [[16 * 17] * 43 + [16], [2048] + [1] * 63, [16 * 24 + 1] * 44]
+    for lens in cases:
+        for rd, least in ((46, 16), (0, 128), (5, 16)):
+            r, units = units_of(lens, least, rd)
+            grid = len(lens) + max(rd, 0)
+            for u in range(grid):
+                got = device_unit_of(u, lens, least, rd)
+                want = units[u] if u < len(units) else None
+                assert got == want, (lens, rd, u, got, want)
